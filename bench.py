@@ -1,0 +1,453 @@
+"""Benchmark: batch-invariant paged prefill attention on GB300.
+
+Default workload (the throughput sweep's long-q point): heads 32/8/128, 16
+requests, q_len = kv_len = 8192 (fresh causal prefill), bf16 pages of 16
+tokens, synthetic N(0,1) data.  `value` = algorithmic causal TFLOP/s
+(4 * head_dim * num_qo_heads * sum of unmasked (row, key) pairs) with inputs
+resident in HBM.  The same JSON line carries the sweep's short-extend point
+(16 requests, q_len 4 behind kv_len 32768) as KV-read GB/s, the roofline of
+each against MEASURED_PEAKS.json, an end-to-end number through the public
+API with host buffers, and the float64 oracle timed on host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --sweep        # every sweep point, one JSON line each
+
+Multi-GPU (torchrun): requests are independent, so every rank runs its own
+16-request batch (weak scaling) with no collective on the data path.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged prefill attn TFLOP/s (long q) & KV-read GB/s (short extends), bit-exact"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["bip_host.cpp", "bip_attn.cu", "bip_merge.cu", "bip_internal.h", "bip_numerics.cuh",
+                  "bip_ptx.cuh"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def pairs(q_len: int, kv_len: int) -> int:
+    """Unmasked (row, key) pairs of one head: sum over rows of (position + 1)."""
+    return q_len * (kv_len - q_len) + q_len * (q_len + 1) // 2
+
+
+def flops_of(heads, q_lens, kv_lens) -> float:
+    hq, _, d = heads
+    return float(sum(4 * d * hq * pairs(q, k) for q, k in zip(q_lens, kv_lens)))
+
+
+def kv_bytes_of(heads, kv_lens, elem=2) -> float:
+    _, hkv, d = heads
+    return float(sum(k * 2 * hkv * d * elem for k in kv_lens))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for s in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "invariant_paged_prefill_gb300", "csrc", s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads
+
+WORKLOADS = {
+    # name: (heads, batch, q_len, kv_len)
+    "long_q": ((32, 8, 128), 16, 8192, 8192),
+    "short_extend": ((32, 8, 128), 16, 4, 32768),
+}
+
+
+def make_batch(heads, batch, q_len, kv_len, device, kv_dtype="bf16", seed=0):
+    from invariant_paged_prefill_gb300 import workloads as W
+    return W.sweep_point(heads, q_len, kv_len, batch=batch, kv_dtype=kv_dtype, device=device, seed_data=seed)
+
+
+class Runner:
+    """One workload resident on the device, with its plan and buffers."""
+
+    def __init__(self, b, device):
+        import invariant_paged_prefill_gb300 as bip
+        self.bip, self.b, self.device = bip, b, device
+        self.plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=b.num_qo_heads,
+                             num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
+                             kv_dtype=b.kv_dtype)
+        self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+        self.out = torch.empty_like(b.q)
+        self.lse = torch.empty(b.q.shape[0], b.q.shape[1], dtype=torch.float32, device=device)
+        self.launches_per_step = 1 + (1 if self.plan.info["num_split_units"] else 0)
+
+    def step(self, q=None, kp=None, vp=None, idx=None):
+        b = self.b
+        self.bip.prefill(self.plan, b.q if q is None else q, b.k_pages if kp is None else kp,
+                         b.v_pages if vp is None else vp, b.kv_indices if idx is None else idx,
+                         out=self.out, lse=self.lse, workspace=self.ws)
+
+    def timed(self, steps, warmup, barrier=lambda: None):
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        barrier()
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(steps):
+            self.step()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        return ev[0].elapsed_time(ev[-1]), per
+
+    def timed_e2e(self, steps, warmup):
+        """Public API with host buffers: pinned H2D of the inputs, prefill, D2H of out and lse."""
+        b = self.b
+        hq = b.q.cpu().pin_memory()
+        hk = torch.empty(b.k_pages.untyped_storage().nbytes(), dtype=torch.uint8).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        hk.copy_(torch.as_strided(b.k_pages.view(torch.uint8) if b.k_pages.dtype == torch.uint8 else
+                                  b.k_pages.view(torch.int16), (b.k_pages.untyped_storage().nbytes() //
+                                                                b.k_pages.element_size(),), (1,), 0)
+                 .cpu().view(torch.uint8))
+        hv.copy_(torch.as_strided(b.v_pages.view(torch.uint8) if b.v_pages.dtype == torch.uint8 else
+                                  b.v_pages.view(torch.int16), (b.v_pages.untyped_storage().nbytes() //
+                                                                b.v_pages.element_size(),), (1,), 0)
+                 .cpu().view(torch.uint8))
+        hidx = b.kv_indices.cpu().pin_memory()
+        ho = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        hl = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        dq = torch.empty_like(b.q)
+        dk = torch.empty(hk.numel(), dtype=torch.uint8, device=self.device)
+        dv = torch.empty_like(dk)
+        didx = torch.empty_like(b.kv_indices)
+        kview = dk.view(b.k_pages.dtype).as_strided(b.k_pages.shape, b.k_pages.stride())
+        vview = dv.view(b.v_pages.dtype).as_strided(b.v_pages.shape, b.v_pages.stride())
+
+        def one():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            self.step(dq, kview, vview, didx)
+            ho.copy_(self.out, non_blocking=True)
+            hl.copy_(self.lse, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / steps
+        h2d = hq.numel() * hq.element_size() + hk.numel() + hv.numel() + hidx.numel() * 4
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        assert torch.equal(ho, self.out.cpu()), "end-to-end output differs from the device-resident run"
+        return dt, h2d, d2h
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def oracle_sample(b, rows):
+    from oracle import paged_attention as pa
+    kind = "bf16" if b.kv_dtype == "bf16" else "e4m3"
+    q = b.q.cpu()
+    kp, vp = b.k_pages.cpu(), b.v_pages.cpu()
+    kview = kp.view(torch.int16) if kind == "bf16" else kp
+    vview = vp.view(torch.int16) if kind == "bf16" else vp
+    t0 = time.perf_counter()
+    out, lse = pa.paged_prefill(q.view(torch.int16).numpy(), kview.numpy(), vview.numpy(), b.qo_indptr.tolist(),
+                                b.kv_indptr.tolist(), b.kv_indices.cpu().tolist(), b.kv_last_page_len.tolist(),
+                                b.num_qo_heads, b.num_kv_heads, b.page_size, q_kind="bf16", kv_kind=kind, rows=rows)
+    return out, lse, time.perf_counter() - t0
+
+
+def sample_rows_for(b, n_rows, seed=0):
+    """Rows of request 0 spread over its positions (first, last, evenly spaced)."""
+    lo, hi = b.row_range(0)
+    rng = np.random.default_rng(seed)
+    rows = sorted(set([lo, hi - 1] + [int(x) for x in rng.integers(lo, hi, size=max(n_rows - 2, 0))]))
+    return rows
+
+
+def sample_flops(b, heads, rows):
+    hq, _, d = heads
+    lo, hi = b.row_range(0)
+    ql, kl = hi - lo, b.kv_lens[0]
+    return float(sum(4 * d * hq * (t - lo + kl - ql + 1) for t in rows))
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------- arms
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    name = args.workload
+    heads, batch, q_len, kv_len = WORKLOADS[name]
+    b = make_batch(heads, batch, q_len, kv_len, "cpu")
+    rows = sample_rows_for(b, args.ref_rows)
+    fl = sample_flops(b, heads, rows)
+    for _ in range(args.warmup):
+        oracle_sample(b, rows[:2])
+    times = []
+    for _ in range(args.steps):
+        _, _, dt = oracle_sample(b, rows)
+        times.append(dt)
+    tot = sum(times)
+    value = fl * args.steps / tot / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(name),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                             "sample": f"{len(rows)} q rows of request 0 (all 32 heads) per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name):
+    heads, batch, q_len, kv_len = WORKLOADS[name]
+    return {"workload": f"{name}: {batch} requests x q_len {q_len} behind kv_len {kv_len}, heads "
+                        f"{heads[0]}/{heads[1]}/{heads[2]}, bf16 pages of 16",
+            "heads": list(heads), "batch": batch, "q_len": q_len, "kv_len": kv_len, "page_size": 16,
+            "l2": "inputs larger than L2 (129 MB) between timed iterations"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        barrier = lambda: dist.barrier()
+    else:
+        barrier = lambda: None
+    torch.cuda.set_device(local)
+    device = torch.device(f"cuda:{local}")
+    from invariant_paged_prefill_gb300 import build as B
+    B.ensure_built()
+    peaks, peak_kind = load_peaks()
+
+    name = args.workload
+    heads, batch, q_len, kv_len = WORKLOADS[name]
+    b = make_batch(heads, batch, q_len, kv_len, device, seed=rank)
+    run = Runner(b, device)
+    fl = flops_of(heads, b.q_lens, b.kv_lens)
+    with ClockSampler(local) as clk:
+        total_ms, per = run.timed(args.steps, args.warmup, barrier)
+    ms = total_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * fl / (ms * 1e-3) / 1e12
+    kernel_ms = statistics.mean(per)
+    achieved = fl / (kernel_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"bf16_tflops (burst) of {peak_kind}", "traffic": recorded_traffic(name),
+            "kernel": "bip_attn_kernel<128>", "note": "launch duration from CUDA events around each bip_prefill"}
+
+    # bit-exactness across repeated runs of the timed step
+    o1 = run.out.clone(); l1 = run.lse.clone()
+    run.step(); torch.cuda.synchronize()
+    repeat_exact = bool(torch.equal(o1, run.out) and torch.equal(l1, run.lse))
+
+    # short-extend point: KV-read GB/s
+    sheads, sbatch, sq, skv = WORKLOADS["short_extend"]
+    sb = make_batch(sheads, sbatch, sq, skv, device, seed=100 + rank)
+    srun = Runner(sb, device)
+    s_total, s_per = srun.timed(args.steps, args.warmup, barrier)
+    s_ms = statistics.mean(s_per)
+    kvb = kv_bytes_of(sheads, sb.kv_lens)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    s_gbs = kvb / (s_ms * 1e-3) / 1e9
+    kv_read = {"workload": f"short_extend: {sbatch} requests x q_len {sq} behind kv_len {skv}",
+               "value": world * kvb / (s_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": s_total / args.steps,
+               "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": hbm, "unit": "GB/s", "frac": s_gbs / hbm,
+                            "peak_source": f"hbm_gbs of {peak_kind}", "traffic": recorded_traffic("short_extend")},
+               "split_units": srun.plan.info["num_split_units"], "items": srun.plan.info["num_items"]}
+    launches = args.steps * run.launches_per_step
+
+    line = None
+    if rank == 0:
+        e2e_s, h2d, d2h = run.timed_e2e(max(2, args.steps // 4), 1)
+        # parity and the CPU baseline from the same oracle sample
+        rows = sample_rows_for(b, args.ref_rows)
+        ro, rl, odt = oracle_sample(b, rows)
+        got = run.out.cpu()[rows].float().numpy().astype(np.float64)
+        gl = run.lse.cpu()[rows].numpy().astype(np.float64)
+        parity_ok = bool((np.abs(got - ro) <= 2e-2 + 1e-2 * np.abs(ro)).all() and
+                         (np.abs(gl - rl) <= 2e-2 + 1e-2 * np.abs(rl)).all())
+        cpu_val = sample_flops(b, heads, rows) / odt / 1e12
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(name),
+                "roofline": roof,
+                "cpu_baseline": {"value": cpu_val, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                                 "sample": f"{len(rows)} q rows of request 0, all heads, float64",
+                                 "seconds": odt},
+                "e2e": {"value": world * fl / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches, "clocks": clk.summary(), "kv_read": kv_read,
+                "parity": {"rows": len(rows), "within_tolerance": parity_ok,
+                           "max_abs_out": float(np.abs(got - ro).max()), "max_abs_lse": float(np.abs(gl - rl).max())},
+                "bit_exact_repeat": repeat_exact, "workspace_bytes": run.plan.workspace_bytes,
+                "source_hash": source_hash()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_sweep(args):
+    from invariant_paged_prefill_gb300 import workloads as W
+    from invariant_paged_prefill_gb300 import build as B
+    B.ensure_built()
+    device = torch.device("cuda:0")
+    peaks, kind = load_peaks()
+    for heads, q_len, kv_len in W.sweep_grid():
+        b = make_batch(heads, 16, q_len, kv_len, device)
+        try:
+            run = Runner(b, device)
+        except Exception as e:  # unsupported shapes are reported, not fatal
+            print(json.dumps({"heads": heads, "q_len": q_len, "kv_len": kv_len, "error": str(e)}), flush=True)
+            continue
+        total, per = run.timed(args.steps, args.warmup)
+        ms = statistics.mean(per)
+        fl = flops_of(heads, b.q_lens, b.kv_lens)
+        kvb = kv_bytes_of(heads, b.kv_lens)
+        print(json.dumps({"heads": list(heads), "batch": 16, "q_len": q_len, "kv_len": kv_len, "ms": ms,
+                          "tflops": fl / ms / 1e9, "tensor_frac": fl / ms / 1e9 / peaks["bf16_tflops"],
+                          "kv_gbs": kvb / ms / 1e6, "hbm_frac": kvb / ms / 1e6 / peaks["hbm_gbs"],
+                          "items": run.plan.info["num_items"], "split_units": run.plan.info["num_split_units"]}),
+              flush=True)
+        del run, b
+        torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long_q")
+    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--sweep", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * bip.h -- batch-invariant paged prefill attention for GB300 (sm_103a).
+ *
+ * One operation: causal, GQA, paged-KV prefill attention whose output rows
+ * are bit-identical however the batch is composed.  A request served from a
+ * radix-cache prefix hit sends only its uncached tail rows
+ * (q_len = seq_len - prefix_len; sglang PR 46351, "Root cause"); those rows
+ * get `out` and `lse` bit-identical to the same rows of the full prefill of
+ * the prompt, whatever the other requests, q_len, page placement or plan
+ * policy.  The prior-art failure this removes: a tile size chosen from the
+ * batch-average packed q length changes the softmax reduction order
+ * (sglang PR 46351, "Root cause", and kahyunnam's review comment).
+ *
+ * Semantics (sglang PR 46351, jbymy2000's reply, "Tail alignment"): local q
+ * row i of a request sits at sequence position i + kv_len - q_len and sees
+ * keys 0..position (the diagonal is included).  Query head h reads KV head
+ * h / (num_qo_heads / num_kv_heads).  Scores are q.k / sqrt(head_dim);
+ * lse is the natural-log log-sum-exp of those scores.
+ *
+ * Numerics contract (fixed at compile time; no run-time knob changes bits):
+ * keys are cut at absolute positions into blocks of BN (128 for head_dim
+ * 128, 64 for head_dim 256) and segments of 4096 keys (the fixed 4096-token
+ * KV split of the model-serving-minefield issue 73 correction, item 2).
+ * Blocks are visited in ascending order inside a segment with an fp32 online
+ * softmax; segments are merged in ascending order with one merge formula,
+ * whether one CTA folds them or several CTAs write partials that a merge
+ * kernel combines.  Each row's arithmetic depends only on its own q row and
+ * on K/V at positions <= its own.
+ *
+ * Ownership: the caller owns every device buffer and the stream.  A plan
+ * owns host copies of its work list (pinned when a CUDA device is present)
+ * and is immutable after creation; one plan may serve many bip_prefill
+ * calls (one per layer) with the same lengths and shapes.
+ *
+ * Errors: every entry point returns a status and never aborts or exits the
+ * process (the model-serving-minefield issue 73 correction: a fixed 2 GiB
+ * workspace overflow killed the whole server).
+ */
+#ifndef BIP_H_
+#define BIP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bip_status {
+  BIP_OK = 0,
+  BIP_ERR_INVALID_ARG = 1,          /* malformed lengths, pointers, sizes */
+  BIP_ERR_UNSUPPORTED = 2,          /* a valid request this build does not run */
+  BIP_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the plan's need */
+  BIP_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
+  BIP_ERR_DEVICE_TIMEOUT = 5,       /* a bounded in-kernel wait gave up */
+  BIP_ERR_OUT_OF_MEMORY = 6,        /* host allocation failed */
+  BIP_ERR_BAD_PAGE_INDEX = 7        /* a kv_indices entry outside [0, num_pages) */
+} bip_status;
+
+typedef enum bip_kv_dtype {
+  BIP_KV_BF16 = 0,
+  BIP_KV_FP8_E4M3 = 1 /* OCP E4M3 pages, dequantised to bf16 in the kernel */
+} bip_kv_dtype;
+
+/* How multi-segment units are scheduled.  Numerically neutral: every policy
+ * gives identical bits (tested). */
+typedef enum bip_split_policy {
+  BIP_SPLIT_AUTO = 0,   /* split long units into per-segment partials only when
+                           there are too few units to fill the GPU */
+  BIP_SPLIT_NEVER = 1,  /* every unit folds its segments in one CTA */
+  BIP_SPLIT_ALWAYS = 2  /* split every multi-segment unit the budget allows */
+} bip_split_policy;
+
+typedef struct bip_plan_options {
+  bip_split_policy split_policy; /* default BIP_SPLIT_AUTO */
+  size_t split_budget_bytes;     /* cap on partial-state bytes; default 256 MiB */
+  int32_t num_sms;               /* CTAs to fill; 0 = query the current device */
+  uint64_t wait_limit_ns;        /* bound on every in-kernel wait; 0 = 4 s */
+} bip_plan_options;
+
+typedef struct bip_plan_info {
+  int32_t batch, total_q, num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype;
+  int32_t gqa_group;       /* num_qo_heads / num_kv_heads */
+  int32_t tile_positions;  /* q positions per 128-row tile: floor(128 / gqa_group) */
+  int32_t kv_block;        /* keys per block (BN) */
+  int32_t split_len;       /* keys per segment (4096) */
+  int32_t num_units;       /* (request, kv head, q tile) units */
+  int32_t num_items;       /* attention work items (units, or their segments) */
+  int32_t num_split_units; /* units computed as per-segment partials + merge */
+  int32_t grid;            /* CTAs of the persistent attention kernel */
+  int32_t reserved;
+  int64_t partial_rows;    /* rows of fp32 partial state (m, l, o[head_dim]) */
+  int64_t kv_blocks;       /* KV blocks streamed, summed over items */
+  uint64_t workspace_bytes;
+  uint64_t partial_bytes;
+  uint64_t scratch_bytes;  /* per-CTA fold state */
+  uint64_t upload_bytes;   /* host->device bytes each bip_prefill copies */
+} bip_plan_info;
+
+typedef struct bip_plan_s* bip_plan_t;
+
+/* Human-readable name of a status (static storage). */
+const char* bip_status_string(bip_status s);
+
+/* Upper bound of bip_plan's workspace_bytes for any batch with at most
+ * max_batch requests and max_total_q q rows, any KV lengths, the given
+ * heads/head_dim, and a split budget of at most split_budget_bytes.
+ * Allocate this once and reuse it.  Returns 0 for unsupported shapes.
+ * Host only; no device work. */
+size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, int32_t num_qo_heads,
+                           int32_t num_kv_heads, int32_t head_dim, size_t split_budget_bytes);
+
+/* Build a plan from HOST arrays (copied; the caller may free them after):
+ *   qo_indptr[batch+1]      exclusive prefix sum of q rows, qo_indptr[0] = 0
+ *   kv_indptr[batch+1]      exclusive prefix sum of pages,  kv_indptr[0] = 0
+ *   kv_last_page_len[batch] valid slots of each request's last page,
+ *                           1..page_size when it has pages
+ * kv_len = (pages - 1) * page_size + last_page_len (0 with no pages);
+ * 0 <= q_len <= kv_len is required; q_len = 0 is legal and yields no rows.
+ * Supported now: head_dim 128 or 256, gqa_group <= 128, page_size a power of
+ * two in [8, BN], kv_dtype BIP_KV_BF16 (FP8 returns BIP_ERR_UNSUPPORTED).
+ * opts may be NULL (defaults).  On success *plan owns the result and
+ * *workspace_bytes (if not NULL) receives the exact workspace size, never
+ * above bip_workspace_bound for the same shapes.  No device work except a
+ * pinned host allocation and an SM-count query when a device is present. */
+bip_status bip_plan(bip_plan_t* plan, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                    const int32_t* kv_last_page_len, int32_t batch, int32_t num_qo_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                    bip_kv_dtype kv_dtype, const bip_plan_options* opts, size_t* workspace_bytes);
+
+bip_status bip_plan_get_info(bip_plan_t plan, bip_plan_info* info);
+
+/* Work items in launch order, 8 int32 each:
+ *   request, kv_head, q_tile, seg_lo, seg_hi, split (0/1), kv_blocks, 0
+ * q_tile is absolute: it covers sequence positions
+ * [q_tile * tile_positions, (q_tile + 1) * tile_positions).  Writes at most
+ * capacity items; *count receives the total. */
+bip_status bip_plan_get_items(bip_plan_t plan, int32_t* items, int32_t capacity, int32_t* count);
+
+/* Release a plan.  Call only after work enqueued with it has completed. */
+bip_status bip_plan_destroy(bip_plan_t plan);
+
+/* Enqueue the attention on `stream`; never synchronizes.  DEVICE pointers:
+ *   q        bf16 [num_q_rows, num_qo_heads, head_dim], rows contiguous;
+ *            num_q_rows must equal qo_indptr[batch] (the shape check the
+ *            paged wrapper of sglang PR 46351 raised, Woody-Hu's report)
+ *   k_pages, v_pages  [num_pages, page_size, num_kv_heads, head_dim] (NHD),
+ *            bf16 (or E4M3 bytes); page p starts at p * page_stride_elems
+ *            elements, slots and heads contiguous inside a page
+ *   kv_indices int32 [kv_indptr[batch]] page ids, each in [0, num_pages)
+ *   out      bf16 [num_q_rows, num_qo_heads, head_dim]
+ *   lse      fp32 [num_q_rows, num_qo_heads], natural log
+ *   workspace  >= the plan's workspace_bytes, 256-byte aligned; its first
+ *            bytes receive this call's work list (one host->device copy on
+ *            `stream`) and a status word.
+ * q, pages and out must be 16-byte aligned; page_stride_elems * element size
+ * must be a multiple of 16 bytes.  k_scale multiplies the logits (folded
+ * into the softmax scale) and v_scale the output; use 1.0 for bf16 pages.
+ * Page slots at or beyond a request's kv_len may hold anything (NaN too).
+ * Calls sharing one workspace must be ordered on the GPU. */
+bip_status bip_prefill(bip_plan_t plan, const void* q, int64_t num_q_rows, const void* k_pages,
+                       const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                       const int32_t* kv_indices, float k_scale, float v_scale, void* out,
+                       float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronize `stream` and read the status word the last bip_prefill on this
+ * workspace left: BIP_OK, BIP_ERR_DEVICE_TIMEOUT (a bounded wait expired; the
+ * kernel returned early and its outputs are undefined) or
+ * BIP_ERR_BAD_PAGE_INDEX (an out-of-range page id was read as zeros). */
+bip_status bip_read_device_status(const void* workspace, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIP_H_ */

@@ -1,0 +1,167 @@
+"""Batch-invariant paged prefill attention for GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/bip.h`` (libbip.so, loaded with
+ctypes).  This layer only marshals arguments: every step of the attention
+runs in the library's CUDA kernels, and there is no CPU or PyTorch fallback
+(the library missing is an error).
+
+    plan = Plan(qo_indptr, kv_indptr, kv_last_page_len, num_qo_heads=32,
+                num_kv_heads=8, head_dim=128, page_size=16)
+    out, lse = prefill(plan, q, k_pages, v_pages, kv_indices)
+
+PyTorch supplies device memory and streams only.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+
+from . import _lib
+
+__all__ = ["BipError", "Plan", "prefill", "workspace_bound", "read_device_status", "STATUS"]
+
+STATUS = {
+    0: "BIP_OK", 1: "BIP_ERR_INVALID_ARG", 2: "BIP_ERR_UNSUPPORTED", 3: "BIP_ERR_WORKSPACE_TOO_SMALL",
+    4: "BIP_ERR_CUDA", 5: "BIP_ERR_DEVICE_TIMEOUT", 6: "BIP_ERR_OUT_OF_MEMORY", 7: "BIP_ERR_BAD_PAGE_INDEX",
+}
+_POLICY = {"auto": 0, "never": 1, "always": 2}
+_KV = {"bf16": 0, "fp8_e4m3": 1}
+
+
+class BipError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = int(code)
+        super().__init__(f"{what}: {STATUS.get(self.code, self.code)}")
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise BipError(code, what)
+
+
+def _i32_array(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def workspace_bound(max_batch: int, max_total_q: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                    split_budget_bytes: int = 256 << 20) -> int:
+    """Workspace bytes that suffice for any plan up to these sizes (0 if unsupported)."""
+    return int(_lib.load().bip_workspace_bound(max_batch, max_total_q, num_qo_heads, num_kv_heads, head_dim,
+                                               split_budget_bytes))
+
+
+class Plan:
+    """A batch's tile schedule and work list (host only; immutable)."""
+
+    def __init__(self, qo_indptr, kv_indptr, kv_last_page_len, *, num_qo_heads: int, num_kv_heads: int,
+                 head_dim: int, page_size: int = 16, kv_dtype: str = "bf16", split_policy: str = "auto",
+                 split_budget_bytes: int = 256 << 20, num_sms: int = 0, wait_limit_ns: int = 0):
+        self._lib = _lib.load()
+        self._h = ctypes.c_void_p()
+        qo, kv, last = _i32_array(qo_indptr), _i32_array(kv_indptr), _i32_array(kv_last_page_len)
+        batch = len(qo) - 1
+        if batch < 0 or len(kv) != batch + 1 or len(last) != batch:
+            raise BipError(1, "indptr lengths disagree")
+        opts = _lib.PlanOptions(_POLICY[split_policy], int(split_budget_bytes), int(num_sms), int(wait_limit_ns))
+        ws = ctypes.c_size_t()
+        _check(self._lib.bip_plan(ctypes.byref(self._h), _ptr(qo), _ptr(kv), _ptr(last) if batch else None,
+                                  batch, num_qo_heads, num_kv_heads, head_dim, page_size, _KV[kv_dtype],
+                                  ctypes.byref(opts), ctypes.byref(ws)), "bip_plan")
+        self.workspace_bytes = int(ws.value)
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+        self.page_size, self.kv_dtype = page_size, kv_dtype
+        self.total_q = int(qo[-1]) if batch >= 0 else 0
+
+    @property
+    def info(self) -> dict:
+        inf = _lib.PlanInfo()
+        _check(self._lib.bip_plan_get_info(self._h, ctypes.byref(inf)), "bip_plan_get_info")
+        return inf.as_dict()
+
+    def items(self) -> np.ndarray:
+        """Work items in launch order: request, kv_head, q_tile, seg_lo, seg_hi, split, kv_blocks, 0."""
+        n = ctypes.c_int32()
+        _check(self._lib.bip_plan_get_items(self._h, None, 0, ctypes.byref(n)), "bip_plan_get_items")
+        buf = np.zeros((max(n.value, 1), 8), dtype=np.int32)
+        _check(self._lib.bip_plan_get_items(self._h, _ptr(buf), n.value, ctypes.byref(n)), "bip_plan_get_items")
+        return buf[: n.value]
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.bip_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _dev_ptr(t, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise BipError(1, f"{name} must be a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, workspace=None,
+            k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+    """Enqueue the attention on ``stream`` (default: torch's current stream).
+
+    q [total_q, Hq, d] bf16; k_pages / v_pages [num_pages, page_size, Hkv, d]
+    (a page stride other than page_size*Hkv*d is allowed, the same for K and V);
+    kv_indices int32 on the device.  Returns (out bf16, lse fp32 natural log).
+    """
+    import torch
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or lse.dtype != torch.float32:
+        raise BipError(1, "q/out must be bf16 and lse fp32")
+    if not (q.is_contiguous() and out.is_contiguous() and lse.is_contiguous()):
+        raise BipError(1, "q, out and lse must be contiguous")
+    if tuple(q.shape[1:]) != (plan.num_qo_heads, plan.head_dim) or out.shape != q.shape:
+        raise BipError(1, "q/out shape does not match the plan")
+    if kv_indices.dtype != torch.int32:
+        raise BipError(1, "kv_indices must be int32")
+    want = torch.bfloat16 if plan.kv_dtype == "bf16" else torch.uint8
+    for name, pg in (("k_pages", k_pages), ("v_pages", v_pages)):
+        if pg.dtype != want or pg.dim() != 4 or tuple(pg.shape[1:]) != (plan.page_size, plan.num_kv_heads,
+                                                                        plan.head_dim):
+            raise BipError(1, f"{name} must be [num_pages, page_size, Hkv, d] of {want}")
+        if pg.stride()[1:] != (plan.num_kv_heads * plan.head_dim, plan.head_dim, 1):
+            raise BipError(1, f"{name}: slots and heads must be contiguous inside a page")
+    if k_pages.shape[0] != v_pages.shape[0] or k_pages.stride(0) != v_pages.stride(0):
+        raise BipError(1, "k_pages and v_pages must share page count and stride")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    _check(plan._lib.bip_prefill(plan._h, _dev_ptr(q, "q"), q.shape[0], _dev_ptr(k_pages, "k_pages"),
+                                 _dev_ptr(v_pages, "v_pages"), k_pages.shape[0], k_pages.stride(0),
+                                 _dev_ptr(kv_indices, "kv_indices"), float(k_scale), float(v_scale),
+                                 _dev_ptr(out, "out"), _dev_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
+                                 workspace.numel() * workspace.element_size(), sptr), "bip_prefill")
+    return out, lse
+
+
+def read_device_status(workspace, stream=None) -> int:
+    """Synchronise ``stream`` and return the status word of the last call on ``workspace``."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    return int(_lib.load().bip_read_device_status(_dev_ptr(workspace, "workspace"),
+                                                  ctypes.c_void_p(stream.cuda_stream)))

@@ -1,0 +1,499 @@
+// Host side of the C ABI: validation, the batch-independent tile schedule,
+// workspace layout, tensor-map encoding and kernel launches.
+//
+// The schedule never looks at batch statistics (the failure of the prior
+// art: a tile chosen from avg_packed_qo_len, sglang PR 46351 "Root cause").
+// Every unit's geometry is a function of its own request's lengths only:
+// q tiles are T = floor(128 / group) positions aligned at absolute multiples
+// of T, and keys are cut at absolute multiples of the block and segment
+// lengths.  Batch composition, policy and SM count only decide which CTA
+// runs a unit and whether its segments are folded or split, which does not
+// change any row's arithmetic.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/bip.h"
+#include "bip_internal.h"
+
+using bip::MergeUnit;
+using bip::WorkItem;
+
+namespace {
+
+constexpr size_t kDefaultSplitBudget = size_t(256) << 20;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct UnitDesc {
+  int32_t request, kv_head, tile, nseg, rows, blocks;
+  int32_t first_valid;
+};
+
+}  // namespace
+
+struct bip_plan_s {
+  int32_t batch = 0, hq = 0, hkv = 0, d = 0, page_size = 0, kv_dtype = 0;
+  int32_t group = 0, T = 0, bn = 0, total_q = 0;
+  bip_plan_options opts{};
+  std::vector<WorkItem> items;
+  std::vector<MergeUnit> merges;
+  std::vector<int32_t> item_desc;  // 8 int32 per item, see bip_plan_get_items
+  int32_t num_units = 0, num_split_units = 0, grid = 0;
+  int64_t partial_rows = 0, kv_blocks = 0;
+  bool need_scratch = false;
+  size_t off_items = 0, off_merges = 0, off_partials = 0, off_scratch = 0;
+  size_t partial_bytes = 0, scratch_bytes = 0, ws_bytes = 0, upload_bytes = 0;
+  uint8_t* upload = nullptr;  // header + items + merges, as copied to the workspace
+  bool pinned = false;
+};
+
+extern "C" const char* bip_status_string(bip_status s) {
+  switch (s) {
+    case BIP_OK: return "BIP_OK";
+    case BIP_ERR_INVALID_ARG: return "BIP_ERR_INVALID_ARG";
+    case BIP_ERR_UNSUPPORTED: return "BIP_ERR_UNSUPPORTED";
+    case BIP_ERR_WORKSPACE_TOO_SMALL: return "BIP_ERR_WORKSPACE_TOO_SMALL";
+    case BIP_ERR_CUDA: return "BIP_ERR_CUDA";
+    case BIP_ERR_DEVICE_TIMEOUT: return "BIP_ERR_DEVICE_TIMEOUT";
+    case BIP_ERR_OUT_OF_MEMORY: return "BIP_ERR_OUT_OF_MEMORY";
+    case BIP_ERR_BAD_PAGE_INDEX: return "BIP_ERR_BAD_PAGE_INDEX";
+  }
+  return "BIP_ERR_UNKNOWN";
+}
+
+namespace {
+
+bool head_dim_supported(int32_t d) { return d == 128 || d == 256; }
+
+bip_status check_heads(int32_t hq, int32_t hkv, int32_t d) {
+  if (hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv != 0) return BIP_ERR_INVALID_ARG;
+  if (!head_dim_supported(d) || hq / hkv > bip::kTileRows) return BIP_ERR_UNSUPPORTED;
+  return BIP_OK;
+}
+
+size_t partial_row_bytes(int32_t d) { return size_t(d + 4) * sizeof(float); }
+
+size_t layout_bytes(size_t n_items, size_t n_merges, size_t partial_bytes, size_t scratch_bytes,
+                    size_t* off_items, size_t* off_merges, size_t* off_partials, size_t* off_scratch,
+                    size_t* upload_bytes) {
+  size_t o = bip::kHeaderBytes;
+  *off_items = o;
+  o += n_items * sizeof(WorkItem);
+  *off_merges = o;
+  o += n_merges * sizeof(MergeUnit);
+  *upload_bytes = o;
+  o = align_up(o, 256);
+  *off_partials = o;
+  o = align_up(o + partial_bytes, 256);
+  *off_scratch = o;
+  o += scratch_bytes;
+  return align_up(o, 256);
+}
+
+int query_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+extern "C" size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, int32_t num_qo_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, size_t split_budget_bytes) {
+  if (max_batch < 0 || max_total_q < 0 || check_heads(num_qo_heads, num_kv_heads, head_dim) != BIP_OK) return 0;
+  const int64_t group = num_qo_heads / num_kv_heads;
+  const int64_t T = bip::kTileRows / group;
+  // A request with q_len rows touches at most ceil(q_len / T) + 1 tiles.
+  const int64_t units = int64_t(num_kv_heads) * ((int64_t(max_total_q) + T - 1) / T + 2 * int64_t(max_batch));
+  // Each extra split item needs at least `group` partial rows of budget.
+  const int64_t extra = int64_t(split_budget_bytes / (size_t(group) * partial_row_bytes(head_dim)));
+  const size_t scratch = size_t(bip::kMaxCtas) * bip::kTileRows * head_dim * sizeof(float);
+  size_t a, b, c, e, u;
+  return layout_bytes(size_t(units + extra), size_t(units), split_budget_bytes, scratch, &a, &b, &c, &e, &u);
+}
+
+extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                               const int32_t* kv_last_page_len, int32_t batch, int32_t num_qo_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               bip_kv_dtype kv_dtype, const bip_plan_options* opts_in,
+                               size_t* workspace_bytes) {
+  if (!plan_out) return BIP_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  if (batch < 0 || !qo_indptr || !kv_indptr || (batch > 0 && !kv_last_page_len)) return BIP_ERR_INVALID_ARG;
+  bip_status st = check_heads(num_qo_heads, num_kv_heads, head_dim);
+  if (st != BIP_OK) return st;
+  if (kv_dtype != BIP_KV_BF16 && kv_dtype != BIP_KV_FP8_E4M3) return BIP_ERR_INVALID_ARG;
+  if (kv_dtype != BIP_KV_BF16) return BIP_ERR_UNSUPPORTED;
+  const int32_t bn = bip::kv_block_for(head_dim);
+  if (page_size <= 0) return BIP_ERR_INVALID_ARG;
+  if ((page_size & (page_size - 1)) != 0 || page_size < 8 || page_size > bn) return BIP_ERR_UNSUPPORTED;
+
+  bip_plan_options opts;
+  opts.split_policy = BIP_SPLIT_AUTO;
+  opts.split_budget_bytes = kDefaultSplitBudget;
+  opts.num_sms = 0;
+  opts.wait_limit_ns = 0;
+  if (opts_in) opts = *opts_in;
+  if (opts.split_policy != BIP_SPLIT_AUTO && opts.split_policy != BIP_SPLIT_NEVER &&
+      opts.split_policy != BIP_SPLIT_ALWAYS)
+    return BIP_ERR_INVALID_ARG;
+  if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
+  if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
+
+  // ---- lengths and validation
+  if (qo_indptr[0] != 0 || kv_indptr[0] != 0) return BIP_ERR_INVALID_ARG;
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const int32_t T = bip::kTileRows / group;
+  std::vector<int32_t> q_len(batch), kv_len(batch);
+  for (int32_t r = 0; r < batch; ++r) {
+    const int64_t ql = int64_t(qo_indptr[r + 1]) - qo_indptr[r];
+    const int64_t np = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
+    if (ql < 0 || np < 0) return BIP_ERR_INVALID_ARG;
+    int64_t kl = 0;
+    if (np > 0) {
+      if (kv_last_page_len[r] < 1 || kv_last_page_len[r] > page_size) return BIP_ERR_INVALID_ARG;
+      kl = (np - 1) * page_size + kv_last_page_len[r];
+    }
+    if (ql > kl) return BIP_ERR_INVALID_ARG;
+    if (kl > int64_t(32767) * bip::kSplitLen) return BIP_ERR_UNSUPPORTED;  // segment ids are int16
+    q_len[r] = int32_t(ql);
+    kv_len[r] = int32_t(kl);
+  }
+
+  // ---- units: (request, kv head, absolute q tile)
+  std::vector<UnitDesc> units;
+  for (int32_t r = 0; r < batch; ++r) {
+    if (q_len[r] == 0) continue;
+    const int32_t q_lo = kv_len[r] - q_len[r];
+    const int32_t t0 = q_lo / T, t1 = (kv_len[r] - 1) / T;
+    for (int32_t t = t0; t <= t1; ++t) {
+      const int32_t tile_end = std::min(t * T + T - 1, kv_len[r] - 1);
+      const int32_t first_valid = std::max(t * T, q_lo);
+      UnitDesc u;
+      u.request = r;
+      u.tile = t;
+      u.nseg = tile_end / bip::kSplitLen + 1;
+      u.rows = (tile_end - first_valid + 1) * group;
+      u.blocks = tile_end / bn + 1;
+      u.first_valid = first_valid;
+      for (int32_t h = 0; h < num_kv_heads; ++h) {
+        u.kv_head = h;
+        units.push_back(u);
+      }
+    }
+  }
+
+  // ---- split decision (numerically neutral; see the header)
+  int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
+  num_sms = std::min(num_sms, bip::kMaxCtas);
+  std::vector<char> split(units.size(), 0);
+  size_t partial_bytes = 0;
+  int64_t n_items = int64_t(units.size());
+  if (opts.split_policy != BIP_SPLIT_NEVER) {
+    std::vector<size_t> cand;
+    for (size_t i = 0; i < units.size(); ++i)
+      if (units[i].nseg > 1) cand.push_back(i);
+    std::stable_sort(cand.begin(), cand.end(),
+                     [&](size_t a, size_t b) { return units[a].blocks > units[b].blocks; });
+    const int64_t target = 2 * int64_t(num_sms);
+    for (size_t i : cand) {
+      if (opts.split_policy == BIP_SPLIT_AUTO && n_items >= target) break;
+      const size_t need = size_t(units[i].nseg) * units[i].rows * partial_row_bytes(head_dim);
+      if (partial_bytes + need > opts.split_budget_bytes) continue;
+      split[i] = 1;
+      partial_bytes += need;
+      n_items += units[i].nseg - 1;
+    }
+  }
+
+  // ---- items and merge units
+  bip_plan_s* p = new (std::nothrow) bip_plan_s;
+  if (!p) return BIP_ERR_OUT_OF_MEMORY;
+  p->batch = batch;
+  p->hq = num_qo_heads;
+  p->hkv = num_kv_heads;
+  p->d = head_dim;
+  p->page_size = page_size;
+  p->kv_dtype = kv_dtype;
+  p->group = group;
+  p->T = T;
+  p->bn = bn;
+  p->total_q = qo_indptr[batch];
+  p->opts = opts;
+  p->num_units = int32_t(units.size());
+
+  struct Pending {
+    WorkItem w;
+    int32_t desc[8];
+    int32_t order_blocks;
+    size_t seq;
+  };
+  std::vector<Pending> pend;
+  pend.reserve(size_t(n_items));
+  int64_t part_rows = 0;
+  size_t seq = 0;
+  for (size_t i = 0; i < units.size(); ++i) {
+    const UnitDesc& u = units[i];
+    const int32_t r = u.request;
+    WorkItem w;
+    w.kv_len = kv_len[r];
+    w.page_base = kv_indptr[r];
+    w.q_tok0 = qo_indptr[r] - (kv_len[r] - q_len[r]);
+    w.q_lo = kv_len[r] - q_len[r];
+    w.tile = u.tile;
+    w.kv_head = int16_t(u.kv_head);
+    w.flags = 0;
+    w.part_base = 0;
+    const int32_t bps = bip::kSplitLen / bn;
+    if (!split[i]) {
+      w.seg_lo = 0;
+      w.seg_hi = int16_t(u.nseg - 1);
+      pend.push_back({w, {r, u.kv_head, u.tile, 0, u.nseg - 1, 0, u.blocks, 0}, u.blocks, seq++});
+    } else {
+      MergeUnit m;
+      m.q_tok0 = w.q_tok0;
+      m.q_lo = w.q_lo;
+      m.tile = u.tile;
+      m.part_base = int32_t(part_rows);
+      m.rows = u.rows;
+      m.kv_head = int16_t(u.kv_head);
+      m.nseg = int16_t(u.nseg);
+      m.pad[0] = m.pad[1] = 0;
+      p->merges.push_back(m);
+      for (int32_t s = 0; s < u.nseg; ++s) {
+        WorkItem ws = w;
+        ws.seg_lo = ws.seg_hi = int16_t(s);
+        ws.flags = bip::kItemSplit;
+        ws.part_base = int32_t(part_rows + int64_t(s) * u.rows);
+        const int32_t blocks = std::min(u.blocks, (s + 1) * bps) - s * bps;
+        pend.push_back({ws, {r, u.kv_head, u.tile, s, s, 1, blocks, 0}, blocks, seq++});
+      }
+      part_rows += int64_t(u.nseg) * u.rows;
+      p->num_split_units++;
+    }
+  }
+  // Longest first; ties in construction order.
+  std::stable_sort(pend.begin(), pend.end(),
+                   [](const Pending& a, const Pending& b) { return a.order_blocks > b.order_blocks; });
+  p->items.reserve(pend.size());
+  p->item_desc.reserve(pend.size() * 8);
+  for (const Pending& e : pend) {
+    p->items.push_back(e.w);
+    p->item_desc.insert(p->item_desc.end(), e.desc, e.desc + 8);
+    p->kv_blocks += e.order_blocks;
+    if (!(e.w.flags & bip::kItemSplit) && e.w.seg_hi > e.w.seg_lo) p->need_scratch = true;
+  }
+  p->partial_rows = part_rows;
+  p->partial_bytes = size_t(part_rows) * partial_row_bytes(head_dim);
+  p->grid = int32_t(std::min<int64_t>(int64_t(p->items.size()), num_sms));
+  p->scratch_bytes = p->need_scratch ? size_t(p->grid) * bip::kTileRows * head_dim * sizeof(float) : 0;
+  p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->partial_bytes, p->scratch_bytes, &p->off_items,
+                             &p->off_merges, &p->off_partials, &p->off_scratch, &p->upload_bytes);
+
+  // ---- host image of what each call uploads: header + items + merge units
+  void* buf = nullptr;
+  if (cudaMallocHost(&buf, p->upload_bytes) == cudaSuccess) {
+    p->pinned = true;
+  } else {
+    cudaGetLastError();
+    buf = std::malloc(p->upload_bytes);
+    if (!buf) {
+      delete p;
+      return BIP_ERR_OUT_OF_MEMORY;
+    }
+  }
+  p->upload = static_cast<uint8_t*>(buf);
+  std::memset(p->upload, 0, bip::kHeaderBytes);
+  if (!p->items.empty())
+    std::memcpy(p->upload + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem));
+  if (!p->merges.empty())
+    std::memcpy(p->upload + p->off_merges, p->merges.data(), p->merges.size() * sizeof(MergeUnit));
+
+  *plan_out = p;
+  if (workspace_bytes) *workspace_bytes = p->ws_bytes;
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_plan_get_info(bip_plan_t p, bip_plan_info* info) {
+  if (!p || !info) return BIP_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->batch = p->batch;
+  info->total_q = p->total_q;
+  info->num_qo_heads = p->hq;
+  info->num_kv_heads = p->hkv;
+  info->head_dim = p->d;
+  info->page_size = p->page_size;
+  info->kv_dtype = p->kv_dtype;
+  info->gqa_group = p->group;
+  info->tile_positions = p->T;
+  info->kv_block = p->bn;
+  info->split_len = bip::kSplitLen;
+  info->num_units = p->num_units;
+  info->num_items = int32_t(p->items.size());
+  info->num_split_units = p->num_split_units;
+  info->grid = p->grid;
+  info->partial_rows = p->partial_rows;
+  info->kv_blocks = p->kv_blocks;
+  info->workspace_bytes = p->ws_bytes;
+  info->partial_bytes = p->partial_bytes;
+  info->scratch_bytes = p->scratch_bytes;
+  info->upload_bytes = p->upload_bytes;
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_plan_get_items(bip_plan_t p, int32_t* items, int32_t capacity, int32_t* count) {
+  if (!p || capacity < 0 || (capacity > 0 && !items)) return BIP_ERR_INVALID_ARG;
+  const int32_t n = int32_t(p->items.size());
+  if (count) *count = n;
+  const int32_t m = std::min(n, capacity);
+  if (m > 0) std::memcpy(items, p->item_desc.data(), size_t(m) * 8 * sizeof(int32_t));
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_plan_destroy(bip_plan_t p) {
+  if (!p) return BIP_ERR_INVALID_ARG;
+  if (p->upload) {
+    if (p->pinned)
+      cudaFreeHost(p->upload);
+    else
+      std::free(p->upload);
+  }
+  delete p;
+  return BIP_OK;
+}
+
+// ---------------------------------------------------------------- launch
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const void* k_pages,
+                                  const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                                  const int32_t* kv_indices, float k_scale, float v_scale, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!p) return BIP_ERR_INVALID_ARG;
+  if (num_q_rows != p->total_q) return BIP_ERR_INVALID_ARG;
+  if (p->items.empty()) return BIP_OK;  // nothing to compute (all q_len = 0)
+  if (!q || !k_pages || !v_pages || !kv_indices || !out || !lse || !workspace) return BIP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return BIP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return BIP_ERR_INVALID_ARG;
+  if (workspace_bytes < p->ws_bytes) return BIP_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t page_elems = int64_t(p->page_size) * p->hkv * p->d;
+  const int64_t elem = p->kv_dtype == BIP_KV_BF16 ? 2 : 1;
+  if (num_pages <= 0 || num_pages > INT32_MAX || page_stride_elems < page_elems ||
+      (page_stride_elems * elem) % 16 != 0)
+    return BIP_ERR_INVALID_ARG;
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return BIP_ERR_INVALID_ARG;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return BIP_ERR_CUDA;
+
+  // q: [rows, Hq, d] as dims (d, Hq, rows); box (64, group, T) = one tile chunk.
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    cuuint64_t dims[3] = {cuuint64_t(p->d), cuuint64_t(p->hq), cuuint64_t(num_q_rows)};
+    cuuint64_t strides[2] = {cuuint64_t(p->d) * 2, cuuint64_t(p->hq) * p->d * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(p->group), cuuint32_t(p->T)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return BIP_ERR_CUDA;
+  }
+  // pages: [pages, slot, Hkv, d] as dims (d, Hkv, slot, page); box (64, 1, page_size, 1) = one page chunk.
+  for (int which = 0; which < 2; ++which) {
+    const void* base = which == 0 ? k_pages : v_pages;
+    cuuint64_t dims[4] = {cuuint64_t(p->d), cuuint64_t(p->hkv), cuuint64_t(p->page_size), cuuint64_t(num_pages)};
+    cuuint64_t strides[3] = {cuuint64_t(p->d) * 2, cuuint64_t(p->hkv) * p->d * 2,
+                             cuuint64_t(page_stride_elems) * 2};
+    cuuint32_t box[4] = {64, 1, cuuint32_t(p->page_size), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (encode(which == 0 ? &tm_k : &tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return BIP_ERR_CUDA;
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemcpyAsync(ws, p->upload, p->upload_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return BIP_ERR_CUDA;
+
+  bip::AttnParams ap;
+  ap.items = reinterpret_cast<const WorkItem*>(ws + p->off_items);
+  ap.n_items = int32_t(p->items.size());
+  ap.num_qo_heads = p->hq;
+  ap.group = p->group;
+  ap.tile_pos = p->T;
+  ap.page_size = p->page_size;
+  ap.num_pages = int32_t(num_pages);
+  ap.kv_indices = kv_indices;
+  ap.out = static_cast<uint16_t*>(out);
+  ap.lse = lse;
+  ap.partials = reinterpret_cast<float*>(ws + p->off_partials);
+  ap.scratch = reinterpret_cast<float*>(ws + p->off_scratch);
+  ap.header = reinterpret_cast<bip::WsHeader*>(ws);
+  ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
+  ap.v_scale = v_scale;
+  ap.wait_limit_ns = p->opts.wait_limit_ns;
+  if (bip::launch_attention(p->d, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess) return BIP_ERR_CUDA;
+
+  if (!p->merges.empty()) {
+    bip::MergeParams mp;
+    mp.units = reinterpret_cast<const MergeUnit*>(ws + p->off_merges);
+    mp.n_units = int32_t(p->merges.size());
+    mp.num_qo_heads = p->hq;
+    mp.group = p->group;
+    mp.tile_pos = p->T;
+    mp.partials = ap.partials;
+    mp.out = ap.out;
+    mp.lse = lse;
+    mp.v_scale = v_scale;
+    if (bip::launch_merge(p->d, mp, stream) != cudaSuccess) return BIP_ERR_CUDA;
+  }
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_read_device_status(const void* workspace, cudaStream_t stream) {
+  if (!workspace) return BIP_ERR_INVALID_ARG;
+  bip::WsHeader h;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return BIP_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BIP_ERR_CUDA;
+  if (h.status != 0) return static_cast<bip_status>(h.status);
+  if (h.bad_pages != 0) return BIP_ERR_BAD_PAGE_INDEX;
+  return BIP_OK;
+}

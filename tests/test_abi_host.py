@@ -1,0 +1,179 @@
+"""The C ABI on the host (no GPU): exports, validation, workspace bound, schedule.
+
+The planner is host-only, so everything here runs through libbip.so on a
+machine without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import invariant_paged_prefill_gb300 as bip
+from invariant_paged_prefill_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "bip.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bip_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code, name in bip.STATUS.items():
+        assert lib.bip_status_string(code).decode() == name
+
+
+def plan_code(qo, kv, last, hq=32, hkv=8, d=128, ps=16, kv_dtype=0, opts=None):
+    lib = _lib.load()
+    h = ctypes.c_void_p()
+    a = [np.ascontiguousarray(np.asarray(x, dtype=np.int32)) for x in (qo, kv, last)]
+    ptrs = [x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) for x in a]
+    ws = ctypes.c_size_t()
+    rc = lib.bip_plan(ctypes.byref(h), ptrs[0], ptrs[1], ptrs[2], len(a[0]) - 1, hq, hkv, d, ps, kv_dtype,
+                      opts, ctypes.byref(ws))
+    if rc == 0:
+        lib.bip_plan_destroy(h)
+    return rc
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(qo=[0, 5], kv=[0, 1], last=[4]), 1),            # q_len 5 > kv_len 4
+    (dict(qo=[0, 2, 1], kv=[0, 1, 2], last=[3, 3]), 1),   # decreasing qo_indptr
+    (dict(qo=[1, 2], kv=[0, 1], last=[3]), 1),            # qo_indptr[0] != 0
+    (dict(qo=[0, 1], kv=[0, 1], last=[17]), 1),           # last page overfull
+    (dict(qo=[0, 1], kv=[0, 1], last=[0]), 1),            # empty last page
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], hq=30), 1),     # heads do not divide
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], d=64), 2),      # unsupported head_dim
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], ps=12), 2),     # page size not a power of two
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=1), 2),  # fp8 not built yet
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=9), 1),
+    (dict(qo=[0, 0, 3], kv=[0, 0, 1], last=[0, 3]), 0),   # zero-length request with no pages
+    (dict(qo=[0, 0, 3], kv=[0, 2, 3], last=[16, 3]), 0),  # zero-length request behind a prefix
+])
+def test_plan_validation(lib, case, code):
+    assert plan_code(**case) == code
+
+
+def test_prefill_rejects_before_touching_memory(lib):
+    plan = bip.Plan([0, 3], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    fake = ctypes.c_void_p(1 << 20)
+    # q row count disagreeing with qo_indptr[-1] (the wrapper's shape check)
+    rc = lib.bip_prefill(plan._h, fake, 4, fake, fake, 1, 16 * 8 * 128, fake, 1.0, 1.0, fake, fake, fake,
+                         plan.workspace_bytes, None)
+    assert rc == 1
+    # too-small workspace
+    rc = lib.bip_prefill(plan._h, fake, 3, fake, fake, 1, 16 * 8 * 128, fake, 1.0, 1.0, fake, fake, fake,
+                         plan.workspace_bytes - 1, None)
+    assert rc == 3
+    # misaligned q
+    rc = lib.bip_prefill(plan._h, ctypes.c_void_p((1 << 20) + 2), 3, fake, fake, 1, 16 * 8 * 128, fake, 1.0, 1.0,
+                         fake, fake, fake, plan.workspace_bytes, None)
+    assert rc == 1
+    # page stride smaller than a page
+    rc = lib.bip_prefill(plan._h, fake, 3, fake, fake, 1, 16 * 8 * 128 - 8, fake, 1.0, 1.0, fake, fake, fake,
+                         plan.workspace_bytes, None)
+    assert rc == 1
+    # a plan with only q_len = 0 requests has nothing to run
+    empty = bip.Plan([0, 0], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    assert lib.bip_prefill(empty._h, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, None, None, 0, None) == 0
+
+
+def random_batch(rng, batch, max_kv, ps=16):
+    kv_len = rng.integers(1, max_kv + 1, size=batch)
+    q_len = np.minimum(kv_len, rng.integers(0, max_kv + 1, size=batch))
+    npages = (kv_len + ps - 1) // ps
+    qo = np.concatenate([[0], np.cumsum(q_len)])
+    kv = np.concatenate([[0], np.cumsum(npages)])
+    last = kv_len - (npages - 1) * ps
+    return qo, kv, last
+
+
+@pytest.mark.parametrize("heads", [(32, 8, 128), (24, 4, 256), (8, 8, 128), (16, 1, 256)])
+def test_workspace_never_exceeds_bound(lib, heads):
+    rng = np.random.default_rng(sum(heads))
+    hq, hkv, d = heads
+    for trial in range(25):
+        batch = int(rng.integers(1, 12))
+        qo, kv, last = random_batch(rng, batch, int(rng.choice([40, 900, 9000, 20000])))
+        for policy in ("auto", "always", "never"):
+            budget = int(rng.choice([0, 1 << 20, 64 << 20]))
+            p = bip.Plan(qo, kv, last, num_qo_heads=hq, num_kv_heads=hkv, head_dim=d, split_policy=policy,
+                         split_budget_bytes=budget, num_sms=int(rng.integers(1, 200)))
+            bound = bip.workspace_bound(batch, int(qo[-1]), hq, hkv, d, budget)
+            assert p.workspace_bytes <= bound
+            assert p.info["partial_bytes"] <= budget
+
+
+def test_large_head_workspace_is_small():
+    # The pages' failure: one 8192-token 24/4/256 prefill needed 2,415,919,104
+    # bytes of split buffers and overflowed a fixed 2 GiB workspace.
+    for n in (8192, 32768):
+        pages = n // 16
+        p = bip.Plan([0, n], [0, pages], [16], num_qo_heads=24, num_kv_heads=4, head_dim=256)
+        assert p.workspace_bytes < 64 << 20
+        assert p.workspace_bytes <= bip.workspace_bound(1, n, 24, 4, 256)
+
+
+def unit_geometry(plan, request):
+    """(kv_head, q_tile) pairs and folded segment ranges of one request."""
+    it = plan.items()
+    mine = it[it[:, 0] == request]
+    return sorted({(int(r[1]), int(r[2])) for r in mine}), sorted(tuple(int(x) for x in r[1:6]) for r in mine)
+
+
+def test_schedule_of_a_request_does_not_depend_on_its_batch_mates(lib):
+    rng = np.random.default_rng(7)
+    for trial in range(20):
+        batch = int(rng.integers(2, 9))
+        qo, kv, last = random_batch(rng, batch, 9000)
+        together = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_policy="never")
+        for r in range(batch):
+            ql, np_ = qo[r + 1] - qo[r], kv[r + 1] - kv[r]
+            alone = bip.Plan([0, ql], [0, np_], [last[r]], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                             split_policy="never")
+            t_units, t_items = unit_geometry(together, r)
+            a_units, a_items = unit_geometry(alone, 0)
+            assert t_units == a_units and t_items == a_items
+            # the tiles are the absolute ones: tile t covers positions [32 t, 32 t + 32)
+            kv_len = (np_ - 1) * 16 + last[r] if np_ else 0
+            if ql:
+                tiles = sorted({t for _, t in a_units})
+                assert tiles == list(range((kv_len - ql) // 32, (kv_len - 1) // 32 + 1))
+
+
+def test_split_policies_cover_the_same_units():
+    qo, kv, last = [0, 40, 41], [0, 600, 1200], [7, 16]
+    plans = {pol: bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_policy=pol)
+             for pol in ("never", "always", "auto")}
+    assert plans["never"].info["num_split_units"] == 0
+    assert plans["always"].info["num_split_units"] > 0
+    ref = {(r[0], r[1], r[2]) for r in plans["never"].items()}
+    for pol, p in plans.items():
+        assert {(r[0], r[1], r[2]) for r in p.items()} == ref
+        # every segment of every unit is covered exactly once
+        seen = {}
+        for r in p.items():
+            for s in range(r[3], r[4] + 1):
+                key = (r[0], r[1], r[2], s)
+                assert key not in seen
+                seen[key] = 1
+        assert len(seen) == sum(r[4] - r[3] + 1 for r in plans["never"].items())
+
+
+def test_items_are_longest_first():
+    qo, kv, last = [0, 3000, 3001], [0, 400, 800], [16, 16]
+    it = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128).items()
+    assert (np.diff(it[:, 6]) <= 0).all()
