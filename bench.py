@@ -279,6 +279,26 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(rank: int, base: int = 0) -> int:
+    """Data seed of a rank's batch: every rank prefills its own 16 requests (weak scaling)."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The slowest rank's time (identity with one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time (per second)."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -330,18 +350,13 @@ def run_ours(args):
 
     name = args.workload
     heads, batch, q_len, kv_len = WORKLOADS[name]
-    b = make_batch(heads, batch, q_len, kv_len, device, seed=rank)
+    b = make_batch(heads, batch, q_len, kv_len, device, seed=rank_seed(rank))
     run = Runner(b, device)
     fl = flops_of(heads, b.q_lens, b.kv_lens)
     with ClockSampler(local) as clk:
         total_ms, per = run.timed(args.steps, args.warmup, barrier)
-    ms = total_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * fl / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(total_ms / args.steps, device)
+    value = aggregate_value(fl, world, ms) / 1e12
     kernel_ms = statistics.mean(per)
     achieved = fl / (kernel_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -356,15 +371,16 @@ def run_ours(args):
 
     # short-extend point: KV-read GB/s
     sheads, sbatch, sq, skv = WORKLOADS["short_extend"]
-    sb = make_batch(sheads, sbatch, sq, skv, device, seed=100 + rank)
+    sb = make_batch(sheads, sbatch, sq, skv, device, seed=rank_seed(rank, 100))
     srun = Runner(sb, device)
     s_total, s_per = srun.timed(args.steps, args.warmup, barrier)
+    s_total = max_over_ranks(s_total, device)
     s_ms = statistics.mean(s_per)
     kvb = kv_bytes_of(sheads, sb.kv_lens)
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     s_gbs = kvb / (s_ms * 1e-3) / 1e9
     kv_read = {"workload": f"short_extend: {sbatch} requests x q_len {sq} behind kv_len {skv}",
-               "value": world * kvb / (s_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+               "value": aggregate_value(kvb, world, s_total / args.steps) / 1e9, "unit": "GB/s",
                "ms_per_step": s_total / args.steps,
                "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": hbm, "unit": "GB/s", "frac": s_gbs / hbm,
                             "peak_source": f"hbm_gbs of {peak_kind}", "traffic": recorded_traffic("short_extend")},

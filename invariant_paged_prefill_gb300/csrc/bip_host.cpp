@@ -288,9 +288,15 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
       p->num_split_units++;
     }
   }
-  // Longest first; ties in construction order.
-  std::stable_sort(pend.begin(), pend.end(),
-                   [](const Pending& a, const Pending& b) { return a.order_blocks > b.order_blocks; });
+  // Order: by (request, KV head) group, longest first inside a group, ties in
+  // construction order.  Concurrent CTAs then stream the same group's pages,
+  // so each KV block comes from HBM about once and from L2 for the other q
+  // tiles; the short tiles of the last group fill the tail.
+  std::stable_sort(pend.begin(), pend.end(), [](const Pending& a, const Pending& b) {
+    const int64_t ga = int64_t(a.desc[0]) * 65536 + a.desc[1], gb = int64_t(b.desc[0]) * 65536 + b.desc[1];
+    if (ga != gb) return ga < gb;
+    return a.order_blocks > b.order_blocks;
+  });
   p->items.reserve(pend.size());
   p->item_desc.reserve(pend.size() * 8);
   for (const Pending& e : pend) {

@@ -173,7 +173,10 @@ def test_split_policies_cover_the_same_units():
         assert len(seen) == sum(r[4] - r[3] + 1 for r in plans["never"].items())
 
 
-def test_items_are_longest_first():
+def test_items_grouped_by_request_and_head_longest_first():
     qo, kv, last = [0, 3000, 3001], [0, 400, 800], [16, 16]
     it = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128).items()
-    assert (np.diff(it[:, 6]) <= 0).all()
+    keys = it[:, 0] * 65536 + it[:, 1]
+    assert (np.diff(keys) >= 0).all()
+    for k in np.unique(keys):
+        assert (np.diff(it[keys == k, 6]) <= 0).all()
