@@ -419,6 +419,25 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile(args):
+    """The timed step alone (no extras), for ncu: --workload, --batch override."""
+    from invariant_paged_prefill_gb300 import build as B
+    B.ensure_built()
+    device = torch.device("cuda:0")
+    heads, batch, q_len, kv_len = WORKLOADS[args.workload]
+    batch = args.batch or batch
+    b = make_batch(heads, batch, q_len, kv_len, device)
+    run = Runner(b, device)
+    total, per = run.timed(args.steps, args.warmup)
+    ms = statistics.mean(per)
+    fl = flops_of(heads, b.q_lens, b.kv_lens)
+    kvb = kv_bytes_of(heads, b.kv_lens)
+    print(json.dumps({"profile": args.workload, "batch": batch, "ms": ms, "tflops": fl / ms / 1e9,
+                      "kv_gbs": kvb / ms / 1e6, "launches_per_step": run.launches_per_step,
+                      "items": run.plan.info["num_items"], "grid": run.plan.info["grid"],
+                      "source_hash": source_hash()}), flush=True)
+
+
 def run_sweep(args):
     from invariant_paged_prefill_gb300 import workloads as W
     from invariant_paged_prefill_gb300 import build as B
@@ -454,6 +473,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long_q")
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="time only the main step (for ncu captures)")
+    ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -461,6 +482,8 @@ def main():
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.profile:
+        run_profile(args)
     else:
         run_ours(args)
 

@@ -211,9 +211,15 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
       if (units[i].nseg > 1) cand.push_back(i);
     std::stable_sort(cand.begin(), cand.end(),
                      [&](size_t a, size_t b) { return units[a].blocks > units[b].blocks; });
-    const int64_t target = 2 * int64_t(num_sms);
+    // AUTO: split by segment when there are too few units to balance a
+    // persistent grid (fewer than 8 per SM), or when a unit is longer than
+    // half of one CTA's fair share of KV blocks (it would dominate the tail).
+    int64_t total_blocks = 0;
+    for (const UnitDesc& u : units) total_blocks += u.blocks;
+    const int64_t fair_half = total_blocks / (2 * int64_t(num_sms));
+    const bool few_units = int64_t(units.size()) < 8 * int64_t(num_sms);
     for (size_t i : cand) {
-      if (opts.split_policy == BIP_SPLIT_AUTO && n_items >= target) break;
+      if (opts.split_policy == BIP_SPLIT_AUTO && !few_units && units[i].blocks <= fair_half) break;
       const size_t need = size_t(units[i].nseg) * units[i].rows * partial_row_bytes(head_dim);
       if (partial_bytes + need > opts.split_budget_bytes) continue;
       split[i] = 1;
