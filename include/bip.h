@@ -78,6 +78,8 @@ typedef struct bip_plan_options {
   size_t split_budget_bytes;     /* cap on partial-state bytes; default 256 MiB */
   int32_t num_sms;               /* CTAs to fill; 0 = query the current device */
   uint64_t wait_limit_ns;        /* bound on every in-kernel wait; 0 = 4 s */
+  int32_t tiles_per_unit;        /* q tiles per CTA: 0 = auto, 1, or 2 (head_dim 128 only);
+                                    numerically neutral (tested) */
 } bip_plan_options;
 
 typedef struct bip_plan_info {
@@ -86,11 +88,11 @@ typedef struct bip_plan_info {
   int32_t tile_positions;  /* q positions per 128-row tile: floor(128 / gqa_group) */
   int32_t kv_block;        /* keys per block (BN) */
   int32_t split_len;       /* keys per segment (4096) */
-  int32_t num_units;       /* (request, kv head, q tile) units */
+  int32_t num_units;       /* (request, kv head, tiles_per_unit q tiles) units */
   int32_t num_items;       /* attention work items (units, or their segments) */
   int32_t num_split_units; /* units computed as per-segment partials + merge */
   int32_t grid;            /* CTAs of the persistent attention kernel */
-  int32_t reserved;
+  int32_t tiles_per_unit;  /* q tiles a unit (and a CTA) carries at once: 2 (d 128) or 1 */
   int64_t partial_rows;    /* rows of fp32 partial state (m, l, o[head_dim]) */
   int64_t kv_blocks;       /* KV blocks streamed, summed over items */
   uint64_t workspace_bytes;
@@ -120,7 +122,8 @@ size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, int32_t num_q
  * kv_len = (pages - 1) * page_size + last_page_len (0 with no pages);
  * 0 <= q_len <= kv_len is required; q_len = 0 is legal and yields no rows.
  * Supported now: head_dim 128 or 256, gqa_group <= 128, page_size a power of
- * two in [8, BN], kv_dtype BIP_KV_BF16 (FP8 returns BIP_ERR_UNSUPPORTED).
+ * two in [8, BN], kv_dtype BIP_KV_BF16 or BIP_KV_FP8_E4M3 (FP8 runs one q tile
+ * per CTA; tiles_per_unit = 2 with FP8 returns BIP_ERR_UNSUPPORTED).
  * opts may be NULL (defaults).  On success *plan owns the result and
  * *workspace_bytes (if not NULL) receives the exact workspace size, never
  * above bip_workspace_bound for the same shapes.  No device work except a
@@ -133,10 +136,10 @@ bip_status bip_plan(bip_plan_t* plan, const int32_t* qo_indptr, const int32_t* k
 bip_status bip_plan_get_info(bip_plan_t plan, bip_plan_info* info);
 
 /* Work items in launch order, 8 int32 each:
- *   request, kv_head, q_tile, seg_lo, seg_hi, split (0/1), kv_blocks, 0
- * q_tile is absolute: it covers sequence positions
- * [q_tile * tile_positions, (q_tile + 1) * tile_positions).  Writes at most
- * capacity items; *count receives the total. */
+ *   request, kv_head, q_tile, seg_lo, seg_hi, split (0/1), kv_blocks, tile_mask
+ * The item carries absolute tiles q_tile + t for every bit t of tile_mask;
+ * tile u covers sequence positions [u * tile_positions, (u + 1) * tile_positions).
+ * Writes at most capacity items; *count receives the total. */
 bip_status bip_plan_get_items(bip_plan_t plan, int32_t* items, int32_t capacity, int32_t* count);
 
 /* Release a plan.  Call only after work enqueued with it has completed. */

@@ -64,14 +64,16 @@ class Plan:
 
     def __init__(self, qo_indptr, kv_indptr, kv_last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                  head_dim: int, page_size: int = 16, kv_dtype: str = "bf16", split_policy: str = "auto",
-                 split_budget_bytes: int = 256 << 20, num_sms: int = 0, wait_limit_ns: int = 0):
+                 split_budget_bytes: int = 256 << 20, num_sms: int = 0, wait_limit_ns: int = 0,
+                 tiles_per_unit: int = 0):
         self._lib = _lib.load()
         self._h = ctypes.c_void_p()
         qo, kv, last = _i32_array(qo_indptr), _i32_array(kv_indptr), _i32_array(kv_last_page_len)
         batch = len(qo) - 1
         if batch < 0 or len(kv) != batch + 1 or len(last) != batch:
             raise BipError(1, "indptr lengths disagree")
-        opts = _lib.PlanOptions(_POLICY[split_policy], int(split_budget_bytes), int(num_sms), int(wait_limit_ns))
+        opts = _lib.PlanOptions(_POLICY[split_policy], int(split_budget_bytes), int(num_sms), int(wait_limit_ns),
+                                int(tiles_per_unit))
         ws = ctypes.c_size_t()
         _check(self._lib.bip_plan(ctypes.byref(self._h), _ptr(qo), _ptr(kv), _ptr(last) if batch else None,
                                   batch, num_qo_heads, num_kv_heads, head_dim, page_size, _KV[kv_dtype],
@@ -88,7 +90,7 @@ class Plan:
         return inf.as_dict()
 
     def items(self) -> np.ndarray:
-        """Work items in launch order: request, kv_head, q_tile, seg_lo, seg_hi, split, kv_blocks, 0."""
+        """Work items in launch order: request, kv_head, q_tile, seg_lo, seg_hi, split, kv_blocks, tile_mask."""
         n = ctypes.c_int32()
         _check(self._lib.bip_plan_get_items(self._h, None, 0, ctypes.byref(n)), "bip_plan_get_items")
         buf = np.zeros((max(n.value, 1), 8), dtype=np.int32)

@@ -21,18 +21,18 @@ P_i32 = ctypes.POINTER(ctypes.c_int32)
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("split_policy", ctypes.c_int), ("split_budget_bytes", c_size), ("num_sms", c_i32),
-                ("wait_limit_ns", c_u64)]
+                ("wait_limit_ns", c_u64), ("tiles_per_unit", c_i32)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("batch", "total_q", "num_qo_heads", "num_kv_heads", "head_dim", "page_size",
                                      "kv_dtype", "gqa_group", "tile_positions", "kv_block", "split_len",
-                                     "num_units", "num_items", "num_split_units", "grid", "reserved")] + \
+                                     "num_units", "num_items", "num_split_units", "grid", "tiles_per_unit")] + \
                [("partial_rows", c_i64), ("kv_blocks", c_i64)] + \
                [(n, c_u64) for n in ("workspace_bytes", "partial_bytes", "scratch_bytes", "upload_bytes")]
 
     def as_dict(self) -> dict:
-        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 # name -> (restype, argtypes); every symbol include/bip.h declares.

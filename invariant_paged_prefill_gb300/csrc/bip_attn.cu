@@ -1,17 +1,23 @@
 // Persistent paged prefill attention for sm_103a: TMA page loads, tcgen05
 // MMAs with TMEM accumulators, an fp32 online softmax with one thread per
-// row, and a fixed-order segment merge.
+// row, P kept in TMEM, and a fixed-order segment merge.
 //
-// One CTA (192 threads, one per SM) walks work items (a request x KV head
-// x absolute q tile, over some of its 4096-key segments):
-//   warp 0      TMA producer: the q tile once per item, then K and V blocks
-//               page by page through a 2-deep ring of each.
-//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM S buffers,
-//               O += P V into the TMEM O accumulator; zeroes V rows past
-//               kv_len before they enter a product.
-//   warps 2-5   softmax: thread i owns packed row i (TMEM lane i); masks,
-//               keeps m and l, writes P (bf16) to shared memory, rescales
-//               O, and at each segment end folds or writes the segment.
+// One CTA (one per SM) walks work items: a unit = (request, KV head, NT
+// consecutive absolute q tiles that share the same keys) over some of its
+// 4096-key segments.  Roles:
+//   warp 0          TMA producer: the unit's q tiles once, then K and V
+//                   blocks page by page through ST-deep rings.
+//   warp 1          tcgen05 issuer: S_t = Q_t K^T into TMEM, then
+//                   O_t += P_t V with P_t read from TMEM; zeroes V rows past
+//                   kv_len before they enter a product.
+//   warps 2..       one softmax warpgroup per q tile slot t: thread i owns
+//                   packed row i (TMEM lane i); masks, keeps the row's running
+//                   max and sum, writes P_t (bf16) over S_t in TMEM, rescales
+//                   O_t when needed, and at each segment end folds or writes
+//                   the segment.
+// With two slots (head_dim 128) the softmax of one tile overlaps the MMAs of
+// the other.  Slots and ring depth only decide scheduling; every row's
+// arithmetic is the same in every variant.
 //
 // Packed rows (GQA group inside the 128-row tile, sglang PR 46351 "Root
 // cause": packed q length = q_len * group): row = local_pos * group + head
@@ -22,8 +28,12 @@
 // rows never mix; blocks beyond a row's position contribute exact zeros
 // (p = 0 against finite V: rows of V past kv_len are zeroed in shared
 // memory), and segments wholly beyond it are empty and skipped by the merge.
+// The running max is moved (and O rescaled) only when a row's block max
+// exceeds it by more than kLazyRescale in log2 units: a per-row decision.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "bip_internal.h"
@@ -33,40 +43,62 @@
 namespace bip {
 namespace {
 
-template <int D>
+// A row keeps a stale running max until a block raises it by more than this
+// (log2 units): probabilities then stay below 2^8 and O is rescaled rarely.
+constexpr float kLazyRescale = 8.0f;
+
+template <int D, int NT, int ST, bool KV8 = false>
 struct Cfg {
   static constexpr int BN = kv_block_for(D);        // keys per block
+  static constexpr int NS = NT == 1 ? 2 : 1;        // S buffers per tile slot
   static constexpr int DCH = D / 64;                // 64-column (128-byte) chunks of a d-row
   static constexpr int Q_CHUNK = kTileRows * 128;   // bytes of one q chunk (128 rows)
-  static constexpr int Q_BYTES = DCH * Q_CHUNK;
+  static constexpr int Q_BYTES = DCH * Q_CHUNK;     // one tile slot
   static constexpr int KV_CHUNK = BN * 128;         // bytes of one K/V chunk (BN rows)
   static constexpr int KV_BYTES = DCH * KV_CHUNK;   // one K or V block
-  static constexpr int PCH = BN / 64;               // chunks of a P row
-  static constexpr int P_BYTES = PCH * Q_CHUNK;
-  static constexpr int STAGES = 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + room to align the base to 1024
-  static constexpr int TM_S = 0;                     // S buffers: columns [0, BN) and [BN, 2 BN)
-  static constexpr int TM_O = 256;                   // O accumulator: columns [256, 256 + D)
+  static constexpr int OFF_K = OFF_Q + NT * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + ST * KV_BYTES;
+  // FP8 pages land raw (BN rows x D bytes, unswizzled) in a staging ring and
+  // are converted to the bf16 operand layout by the dequant warpgroup.
+  static constexpr int SS = KV8 ? (D == 128 ? 2 : 1) : 0;  // staging stages
+  static constexpr int KV8_BYTES = BN * D;
+  static constexpr int OFF_K8 = OFF_V + ST * KV_BYTES;
+  static constexpr int OFF_V8 = OFF_K8 + SS * KV8_BYTES;
+  static constexpr int OFF_BAR = OFF_V8 + SS * KV8_BYTES;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
+  static constexpr int DQ_WARP0 = 2 + 4 * NT;        // first dequant warp
+  static constexpr int THREADS = 64 + 128 * NT + (KV8 ? 128 : 0);
   static constexpr int TM_COLS = 512;
   static constexpr int BPS = kSplitLen / BN;         // blocks per segment
-  static_assert(2 * BN <= TM_O && TM_O + D <= TM_COLS, "TMEM budget");
+  // TMEM columns: two slots use [0,256) and [256,512), each S (BN) then O (D);
+  // one slot keeps two S buffers at [0, 2 BN) and O at [256, 256 + D).
+  __host__ __device__ static constexpr uint32_t tm_s(int t, int s) {
+    return NT == 2 ? uint32_t(t * 256) : uint32_t(s * BN);
+  }
+  __host__ __device__ static constexpr uint32_t tm_o(int t) { return NT == 2 ? uint32_t(t * 256 + BN) : 256u; }
+  static_assert(NT == 1 || (BN + D <= 256), "two slots need S and O in 256 columns each");
+  static_assert(NT == 2 || (2 * BN <= 256 && 256 + D <= TM_COLS), "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(!KV8 || NT == 1, "FP8 pages use the one-tile variant");
 };
 
 // Barrier slots (8 bytes each) at OFF_BAR.
 enum Bar {
-  B_Q_FULL = 0, B_Q_FREE = 1, B_K_FULL = 2, B_K_FREE = 4, B_V_FULL = 6, B_V_FREE = 8,
-  B_S_FULL = 10, B_S_FREE = 12, B_P_FULL = 14, B_O_DONE = 15, B_DRAIN = 16, B_COUNT = 17
+  B_Q_FULL = 0, B_Q_FREE = 1,
+  B_K_FULL = 2, B_K_FREE = 6, B_V_FULL = 10, B_V_FREE = 14,  // up to 4 ring stages
+  // Per slot and per S buffer (index 2 slot + buffer).  P_FULL and O_DONE
+  // are kept per buffer too: with two S buffers the softmax may finish two
+  // blocks before the issuer waits on the first, and a single barrier two
+  // phases ahead of its waiter reads as zero under a parity wait.
+  B_S_FULL = 18, B_P_FULL = 22, B_O_DONE = 26,
+  B_DRAIN = 30,
+  B_K8_FULL = 31, B_K8_FREE = 33, B_V8_FULL = 35, B_V8_FREE = 37,  // FP8 staging, up to 2 stages
+  B_COUNT = 39
 };
 constexpr int OFF_TMEM_SLOT = 8 * B_COUNT;    // u32: TMEM base address
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;  // u32: a wait expired somewhere in this CTA
-
-constexpr int kThreads = 192;
+static_assert(OFF_ABORT + 4 <= 512, "barrier area");
 
 struct Ctx {
   uint32_t bar0;
@@ -110,172 +142,245 @@ __device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
 }
 
 struct Geom {
-  int kv_len, tile_start, tile_end, first_valid;
-  int blk_lo, blk_hi;  // inclusive block range of the item
+  int tile_start[kMaxTilesPerUnit];  // first position of each slot's tile
+  int tile_end[kMaxTilesPerUnit];    // last position with a q row or key in each slot's tile
+  int first_valid[kMaxTilesPerUnit];
+  int mask, last_slot;
+  int blk_lo, blk_hi;  // inclusive block range of the item (union of the slots' keys)
 };
 
-template <int D>
+template <int NT, int BN>
 __device__ __forceinline__ Geom geom_of(const WorkItem& w, int T) {
-  using C = Cfg<D>;
   Geom g;
-  g.kv_len = w.kv_len;
-  g.tile_start = w.tile * T;
-  g.tile_end = min(g.tile_start + T - 1, w.kv_len - 1);
-  g.first_valid = max(g.tile_start, w.q_lo);
-  g.blk_lo = w.seg_lo * C::BPS;
-  g.blk_hi = min((int(w.seg_hi) + 1) * kSplitLen - 1, g.tile_end) / C::BN;
+  g.mask = (w.flags / kSlotPresent) & ((1 << NT) - 1);
+  g.last_slot = 0;
+  int unit_end = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    g.tile_start[t] = (w.tile + t) * T;
+    g.tile_end[t] = min(g.tile_start[t] + T - 1, w.kv_len - 1);
+    g.first_valid[t] = max(g.tile_start[t], w.q_lo);
+    if (g.mask >> t & 1) {
+      g.last_slot = t;
+      unit_end = g.tile_end[t];
+    }
+  }
+  g.blk_lo = w.seg_lo * (kSplitLen / BN);
+  g.blk_hi = min((int(w.seg_hi) + 1) * kSplitLen - 1, unit_end) / BN;
   return g;
 }
 
 // ------------------------------------------------------------------ roles
 
-template <int D>
+// Page ids of one KV block, range-checked (bad ids are counted and read as 0).
+template <int MAXP>
+__device__ __forceinline__ void load_page_ids(const AttnParams& p, const WorkItem& w, int blk, int pages_per_blk,
+                                              int npages_req, int (&ids)[MAXP], int& n) {
+  const int p0 = blk * pages_per_blk;
+  n = min(p0 + pages_per_blk, npages_req) - p0;
+#pragma unroll
+  for (int i = 0; i < MAXP; ++i) ids[i] = (i < n) ? __ldg(p.kv_indices + w.page_base + p0 + i) : 0;
+}
+
+template <int D, int NT, int ST, bool KV8>
 __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, const CUtensorMap* tk,
                          const CUtensorMap* tv, const AttnParams& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, NT, ST, KV8>;
+  constexpr int MAXP = C::BN / 8;  // pages per block at the smallest page size
   const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
   const int pages_per_blk = C::BN / p.page_size;
+  const uint32_t q_slot_bytes = uint32_t(C::DCH * 128 * p.group * p.tile_pos);
   uint32_t b = 0;  // blocks started by this CTA
   int n = 0;       // items started by this CTA
-  uint32_t k_issued[2] = {0u, 0u}, v_issued[2] = {0u, 0u}, q_issued = 0u;  // loads per barrier
-  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++n) {
+  uint32_t k_issued[ST] = {}, v_issued[ST] = {}, q_issued = 0u;  // loads per barrier
+  bool ok = true;
+  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
     const WorkItem w = p.items[it];
-    const Geom g = geom_of<D>(w, p.tile_pos);
-    if (n > 0 && !wait_phase(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) break;
-    mbar_arrive_expect_tx(bar(c, B_Q_FULL), uint32_t(C::DCH * 128 * p.group * p.tile_pos));
-    ++q_issued;
-    for (int ch = 0; ch < C::DCH; ++ch)
-      tma_load_3d(sQ + ch * C::Q_CHUNK, tq, bar(c, B_Q_FULL), ch * 64, w.kv_head * p.group,
-                  w.q_tok0 + g.tile_start);
+    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int npages_req = (w.kv_len + p.page_size - 1) / p.page_size;
-    bool ok = true;
-    for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {
-      const int slot = b & 1;
-      const uint32_t use = b >> 1;
-      const int p0 = blk * pages_per_blk;
-      const int p1 = min(p0 + pages_per_blk, npages_req);
-      int ids[C::BN / 8];
+    int ids[MAXP], nid;
+    load_page_ids<MAXP>(p, w, g.blk_lo, pages_per_blk, npages_req, ids, nid);
+    if (n > 0 && !wait_phase(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) break;
+    mbar_arrive_expect_tx(bar(c, B_Q_FULL), q_slot_bytes * __popc(g.mask));
+    ++q_issued;
 #pragma unroll
-      for (int i = 0; i < C::BN / 8; ++i) {
-        int id = 0;
-        if (i < p1 - p0) {
-          id = __ldg(p.kv_indices + w.page_base + p0 + i);
-          if (id < 0 || id >= p.num_pages) {
-            atomicAdd(&c.header->bad_pages, 1u);
-            id = 0;
-          }
+    for (int t = 0; t < NT; ++t) {
+      if (!(g.mask >> t & 1)) continue;
+      for (int ch = 0; ch < C::DCH; ++ch)
+        tma_load_3d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tq, bar(c, B_Q_FULL), ch * 64, w.kv_head * p.group,
+                    w.q_tok0 + g.tile_start[t]);
+    }
+    for (int blk = g.blk_lo; blk <= g.blk_hi; ++blk, ++b) {
+      const int slot = b % ST;
+      const uint32_t use = b / ST;
+      int cur[MAXP];
+      const int ncur = nid;
+#pragma unroll
+      for (int i = 0; i < MAXP; ++i) {
+        int id = ids[i];
+        if (i < ncur && (id < 0 || id >= p.num_pages)) {
+          atomicAdd(&c.header->bad_pages, 1u);
+          id = 0;
         }
-        ids[i] = id;
+        cur[i] = id;
       }
-      const uint32_t bytes = uint32_t((p1 - p0) * p.page_size * D * 2);
-      // K block
+      if (blk < g.blk_hi) load_page_ids<MAXP>(p, w, blk + 1, pages_per_blk, npages_req, ids, nid);  // next block
+      if constexpr (KV8) {
+        // raw E4M3 pages into the staging ring; the dequant warps fill the bf16 slots
+        const int ss = b % C::SS;
+        const uint32_t suse = b / C::SS;
+        const uint32_t bytes8 = uint32_t(ncur * p.page_size * D);
+        if (suse > 0 && !wait_phase(c, bar(c, B_K8_FREE + ss), (suse - 1) & 1, 4)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(c, B_K8_FULL + ss), bytes8);
+        ++k_issued[ss];
+        for (int i = 0; i < ncur; ++i)
+          tma_load_4d(sbase + C::OFF_K8 + ss * C::KV8_BYTES + i * p.page_size * D, tk, bar(c, B_K8_FULL + ss), 0,
+                      w.kv_head, 0, cur[i]);
+        if (suse > 0 && !wait_phase(c, bar(c, B_V8_FREE + ss), (suse - 1) & 1, 5)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(c, B_V8_FULL + ss), bytes8);
+        ++v_issued[ss];
+        for (int i = 0; i < ncur; ++i)
+          tma_load_4d(sbase + C::OFF_V8 + ss * C::KV8_BYTES + i * p.page_size * D, tv, bar(c, B_V8_FULL + ss), 0,
+                      w.kv_head, 0, cur[i]);
+        continue;
+      }
+      const uint32_t bytes = uint32_t(ncur * p.page_size * D * 2);
       if (use > 0 && !wait_phase(c, bar(c, B_K_FREE + slot), (use - 1) & 1, 2)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(c, B_K_FULL + slot), bytes);
       ++k_issued[slot];
-      for (int i = 0; i < p1 - p0; ++i)
+#pragma unroll
+      for (int i = 0; i < MAXP; ++i) {
+        if (i >= ncur) break;
         for (int ch = 0; ch < C::DCH; ++ch)
           tma_load_4d(sK + slot * C::KV_BYTES + ch * C::KV_CHUNK + i * p.page_size * 128, tk,
-                      bar(c, B_K_FULL + slot), ch * 64, w.kv_head, 0, ids[i]);
-      // V block
+                      bar(c, B_K_FULL + slot), ch * 64, w.kv_head, 0, cur[i]);
+      }
       if (use > 0 && !wait_phase(c, bar(c, B_V_FREE + slot), (use - 1) & 1, 3)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(c, B_V_FULL + slot), bytes);
       ++v_issued[slot];
-      for (int i = 0; i < p1 - p0; ++i)
+#pragma unroll
+      for (int i = 0; i < MAXP; ++i) {
+        if (i >= ncur) break;
         for (int ch = 0; ch < C::DCH; ++ch)
           tma_load_4d(sV + slot * C::KV_BYTES + ch * C::KV_CHUNK + i * p.page_size * 128, tv,
-                      bar(c, B_V_FULL + slot), ch * 64, w.kv_head, 0, ids[i]);
+                      bar(c, B_V_FULL + slot), ch * 64, w.kv_head, 0, cur[i]);
+      }
     }
-    if (!ok) break;
   }
   // Drain: the last load on every barrier must have landed before exit
   // (on the normal path these phases completed long ago).
   if (q_issued) drain_wait(bar(c, B_Q_FULL), (q_issued - 1) & 1);
-  for (int slot = 0; slot < 2; ++slot) {
-    if (k_issued[slot]) drain_wait(bar(c, B_K_FULL + slot), (k_issued[slot] - 1) & 1);
-    if (v_issued[slot]) drain_wait(bar(c, B_V_FULL + slot), (v_issued[slot] - 1) & 1);
+#pragma unroll
+  for (int slot = 0; slot < ST; ++slot) {
+    const int kf = KV8 ? B_K8_FULL : B_K_FULL, vf = KV8 ? B_V8_FULL : B_V_FULL;
+    if (k_issued[slot]) drain_wait(bar(c, kf + slot), (k_issued[slot] - 1) & 1);
+    if (v_issued[slot]) drain_wait(bar(c, vf + slot), (v_issued[slot] - 1) & 1);
   }
 }
 
-template <int D>
+template <int D, int NT, int ST, bool KV8>
 __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const AttnParams& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, NT, ST, KV8>;
   const int lane = threadIdx.x & 31;
-  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P;
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);  // S = Q K^T, both K-major
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);       // O += P V, V MN-major
-  uint32_t b = 0;
+  uint32_t gb = 0;                       // KV blocks consumed by this CTA (ring position)
+  uint32_t s_cnt[NT] = {}, pv_cnt[NT] = {};  // blocks whose S / PV was issued, per slot
   int n = 0;
   bool ok = true;
   for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
     const WorkItem w = p.items[it];
-    const Geom g = geom_of<D>(w, p.tile_pos);
+    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int nb = g.blk_hi - g.blk_lo + 1;
     if (!wait_warp(c, bar(c, B_Q_FULL), n & 1, 10)) { ok = false; break; }
     tc_fence_after();
 
-    // Issue S for block i of this item (global block counter bb).
-    auto issue_s = [&](uint32_t bb, bool last_of_item) -> bool {
-      const int slot = bb & 1;
-      if (!wait_warp(c, bar(c, B_K_FULL + slot), (bb >> 1) & 1, 11)) return false;
-      if (bb >= 2 && !wait_warp(c, bar(c, B_S_FREE + slot), ((bb >> 1) - 1) & 1, 12)) return false;
+    // S_t for item-local block j into the slot's next S buffer.
+    auto issue_s = [&](int t, int j) -> bool {
+      const uint32_t kb = gb + j;
+      const int kslot = kb % ST;
+      if (!wait_warp(c, bar(c, B_K_FULL + kslot), (kb / ST) & 1, 11)) return false;
       tc_fence_after();
+      const int sbuf = s_cnt[t] % C::NS;
       if (lane == 0) {
-        const uint32_t d_tmem = tmem + C::TM_S + slot * C::BN;
+        const uint32_t d_tmem = tmem + C::tm_s(t, sbuf);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off_q = (k >> 2) * C::Q_CHUNK + (k & 3) * 32;
-          const uint32_t off_k = slot * C::KV_BYTES + (k >> 2) * C::KV_CHUNK + (k & 3) * 32;
+          const uint32_t off_q = t * C::Q_BYTES + (k >> 2) * C::Q_CHUNK + (k & 3) * 32;
+          const uint32_t off_k = kslot * C::KV_BYTES + (k >> 2) * C::KV_CHUNK + (k & 3) * 32;
           tc_mma_ss(d_tmem, sdesc_sw128(sQ + off_q, 16, 1024), sdesc_sw128(sK + off_k, 16, 1024), kIdescS,
                     k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(c, B_S_FULL + slot));
-        tc_commit(bar(c, B_K_FREE + slot));
-        if (last_of_item) tc_commit(bar(c, B_Q_FREE));
+        tc_commit(bar(c, B_S_FULL + 2 * t + sbuf));
+        if (t == g.last_slot) {
+          tc_commit(bar(c, B_K_FREE + kslot));                // last reader of this K block
+          if (j == nb - 1) tc_commit(bar(c, B_Q_FREE));       // last reader of the q tiles
+        }
       }
       __syncwarp();
+      ++s_cnt[t];
       return true;
     };
 
-    if (!issue_s(b, nb == 1)) { ok = false; break; }
-    for (int i = 0; i < nb; ++i) {
-      const uint32_t bb = b + i;
-      const int blk = g.blk_lo + i;
-      const int slot = bb & 1;
-      if (i + 1 < nb && !issue_s(bb + 1, i + 2 == nb)) { ok = false; break; }
-      if (!wait_warp(c, bar(c, B_P_FULL), bb & 1, 13)) { ok = false; break; }
-      if (!wait_warp(c, bar(c, B_V_FULL + slot), (bb >> 1) & 1, 14)) { ok = false; break; }
-      tc_fence_after();
-      // Rows of V at or past kv_len (the tail of the last page, and pages the
-      // request does not have) are zeroed so that p = 0 meets a finite value.
-      const int valid_rows = g.kv_len - blk * C::BN;
-      if (valid_rows < C::BN) {
-        const uint32_t vbase = sV + slot * C::KV_BYTES;
-        const int nz = (C::BN - valid_rows) * C::DCH * 8;  // 16-byte units to clear
-        for (int u = lane; u < nz; u += 32) {
-          const int ch = u / ((C::BN - valid_rows) * 8);
-          const int rem = u % ((C::BN - valid_rows) * 8);
-          const int row = valid_rows + rem / 8;
-          const uint32_t addr = vbase + ch * C::KV_CHUNK + row * 128 + (rem % 8) * 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      if (lane == 0) {
-        const bool first_in_seg = (blk % C::BPS) == 0;
+    for (int j = 0; j < C::NS && j < nb && ok; ++j)
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {
-          const uint32_t off_p = (k >> 2) * C::Q_CHUNK + (k & 3) * 32;
-          const uint32_t off_v = slot * C::KV_BYTES + k * 16 * 128;
-          tc_mma_ss(tmem + C::TM_O, sdesc_sw128(sP + off_p, 16, 1024),
-                    sdesc_sw128(sV + off_v, C::KV_CHUNK, 1024), kIdescO, (k > 0 || !first_in_seg) ? 1u : 0u);
+      for (int t = 0; t < NT; ++t)
+        if ((g.mask >> t & 1) && !issue_s(t, j)) { ok = false; break; }
+    if (!ok) break;
+
+    for (int j = 0; j < nb && ok; ++j) {
+      const uint32_t vb = gb + j;
+      const int vslot = vb % ST;
+      const int blk = g.blk_lo + j;
+      const bool first_in_seg = (blk % C::BPS) == 0;
+      bool v_ready = false;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (!(g.mask >> t & 1)) continue;
+        const int pbuf = pv_cnt[t] % C::NS;
+        if (!wait_warp(c, bar(c, B_P_FULL + 2 * t + pbuf), (pv_cnt[t] / C::NS) & 1, 13)) { ok = false; break; }
+        if (!v_ready) {
+          if (!wait_warp(c, bar(c, B_V_FULL + vslot), (vb / ST) & 1, 14)) { ok = false; break; }
+          tc_fence_after();
+          // Rows of V at or past kv_len (the tail of the last page, and pages the
+          // request does not have) are zeroed so that p = 0 meets a finite value.
+          const int valid_rows = w.kv_len - blk * C::BN;
+          if (!KV8 && valid_rows < C::BN) {  // (FP8: the dequant warps wrote these zeros)
+            const uint32_t vbase = sV + vslot * C::KV_BYTES;
+            const int per_chunk = (C::BN - valid_rows) * 8;  // 16-byte units per chunk
+            for (int u = lane; u < per_chunk * C::DCH; u += 32) {
+              const int ch = u / per_chunk, rem = u % per_chunk;
+              const uint32_t addr = vbase + ch * C::KV_CHUNK + (valid_rows + rem / 8) * 128 + (rem % 8) * 16;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          v_ready = true;
         }
-        tc_commit(bar(c, B_O_DONE));
-        tc_commit(bar(c, B_V_FREE + slot));
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t p_tmem = tmem + C::tm_s(t, pbuf);  // P_t (bf16) over its S buffer
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            const uint32_t off_v = vslot * C::KV_BYTES + k * 16 * 128;
+            tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, sdesc_sw128(sV + off_v, C::KV_CHUNK, 1024), kIdescO,
+                      (k > 0 || !first_in_seg) ? 1u : 0u);
+          }
+          tc_commit(bar(c, B_O_DONE + 2 * t + pbuf));
+        }
+        __syncwarp();
+        ++pv_cnt[t];
+        // The slot's next S goes into the buffer this PV has just been queued
+        // to read; tcgen05 MMAs of one thread execute in issue order.
+        if (j + C::NS < nb && !issue_s(t, j + C::NS)) { ok = false; break; }
       }
+      if (!ok) break;
+      if (lane == 0) tc_commit(bar(c, B_V_FREE + vslot));
       __syncwarp();
     }
-    b += nb;
+    gb += nb;
   }
   // Drain: every MMA this thread issued has completed before TMEM is freed.
   if (lane == 0) {
@@ -285,126 +390,153 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
   __syncwarp();
 }
 
-template <int D>
-__device__ void softmax_role(const Ctx& c, uint32_t sbase, uint32_t tmem, const AttnParams& p) {
-  using C = Cfg<D>;
+template <int D, int NT, int ST, bool KV8>
+__device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t) {
+  using C = Cfg<D, NT, ST, KV8>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;          // TMEM lanes this warp may access
   const int row = quarter * 32 + lane;   // packed tile row == TMEM lane
   const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16);
-  const uint32_t sP = sbase + C::OFF_P;
   const float scale = p.scale_log2;
-  uint32_t b = 0, pv_seen = 0;
-  int n = 0;
+  uint32_t cnt = 0, pv_seen = 0;  // blocks of this slot processed / PVs known complete
   bool ok = true;
 
-  // PV of global block x has completed (its o_done phase observed).
+  // PV of this slot's block x has completed.  PVs complete in order, so
+  // pv_seen only skips waits already satisfied.
   auto wait_pv = [&](uint32_t x) -> bool {
     if (pv_seen > x) return true;
-    if (!wait_warp(c, bar(c, B_O_DONE), x & 1, 20)) return false;
+    if (!wait_warp(c, bar(c, B_O_DONE + 2 * t + x % C::NS), (x / C::NS) & 1, 20)) return false;
     pv_seen = x + 1;
     return true;
   };
 
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
     const WorkItem w = p.items[it];
-    const Geom g = geom_of<D>(w, p.tile_pos);
+    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
+    if (!(g.mask >> t & 1)) continue;
     const int local_pos = row / p.group;
     const int hg = row - local_pos * p.group;
-    const int pos = g.tile_start + local_pos;
-    const bool valid = row < p.tile_pos * p.group && pos >= g.first_valid && pos <= g.tile_end;
+    const int pos = g.tile_start[t] + local_pos;
+    const bool valid = row < p.tile_pos * p.group && pos >= g.first_valid[t] && pos <= g.tile_end[t];
     const bool split = (w.flags & kItemSplit) != 0;
     float Mrun = -INFINITY, Lrun = 0.f;  // merged state of the segments before this one
-    float* scratch_row = p.scratch + (size_t(blockIdx.x) * kTileRows + row) * D;
+    float* scratch_row = p.scratch + ((size_t(blockIdx.x) * NT + t) * kTileRows + row) * D;
+    const uint32_t o_addr = t_lane + C::tm_o(t);
 
     for (int s = w.seg_lo; s <= w.seg_hi && ok; ++s) {
-      const int sb_lo = max(s * C::BPS, g.blk_lo);
+      const int sb_lo = s * C::BPS;
       const int sb_hi = min((s + 1) * C::BPS - 1, g.blk_hi);
-      float m = -INFINITY, l = 0.f;  // raw-score max and sum over this segment
-      for (int blk = sb_lo; blk <= sb_hi; ++blk, ++b) {
-        const int slot = b & 1;
-        if (!wait_warp(c, bar(c, B_S_FULL + slot), (b >> 1) & 1, 21)) { ok = false; break; }
+      float m = -INFINITY, l = 0.f;  // running raw-score max (possibly stale) and sum over this segment
+      for (int blk = sb_lo; blk <= sb_hi; ++blk, ++cnt) {
+        const int sbuf = cnt % C::NS;
+        if (!wait_warp(c, bar(c, B_S_FULL + 2 * t + sbuf), (cnt / C::NS) & 1, 21)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[C::BN];
-        if constexpr (C::BN == 128) tmem_ld_x128(t_lane + C::TM_S + slot * C::BN, sv);
-        else tmem_ld_x64(t_lane + C::TM_S + slot * C::BN, sv);
-        tc_fence_before();
-        mbar_arrive(bar(c, B_S_FREE + slot));
+        const uint32_t sa = t_lane + C::tm_s(t, sbuf);
+        const int lim = valid ? pos - blk * C::BN : -1;  // columns 0..lim are visible
 
-        float alpha = 1.f;
-        if (valid) {
-          const int lim = pos - blk * C::BN;  // columns 0..lim are visible
-          float mx = -INFINITY;
+        // Blocks wholly visible to every row of the warp skip the per-column
+        // mask (same values, fewer instructions).  A warp with no visible
+        // column in this block skips the arithmetic but still stores P = 0:
+        // its rows may be valid rows past whose position the block lies, and
+        // their O keeps accumulating P V.
+        const bool whole = __all_sync(0xffffffffu, lim >= C::BN - 1);
+        const bool live = __any_sync(0xffffffffu, lim >= 0);
+
+        // pass 1: block max over the visible columns
+        float mx = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < C::BN; ++j)
-            if (j <= lim) mx = fmaxf(mx, __uint_as_float(sv[j]));
-          const float m_new = fmaxf(m, mx);
-          if (m_new != -INFINITY) {
-            const float ms = __fmul_rn(m_new, scale);
-            if (m_new != m) alpha = ex2(__fsub_rn(__fmul_rn(m, scale), ms));  // m = -inf gives 0
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c0 = 0; c0 < (live ? C::BN : 0); c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(sa + c0, v);
+          if (whole) {
 #pragma unroll
-            for (int j = 0; j < C::BN; ++j) {
-              const float pj = (j <= lim) ? ex2(__fmaf_rn(__uint_as_float(sv[j]), scale, -ms)) : 0.f;
-              acc[j & 3] = __fadd_rn(acc[j & 3], pj);
-              sv[j] = __float_as_uint(pj);
-            }
-            const float rowsum = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
-            l = __fadd_rn(__fmul_rn(l, alpha), rowsum);
-            m = m_new;
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
           } else {
 #pragma unroll
-            for (int j = 0; j < C::BN; ++j) sv[j] = 0u;
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j <= lim) mx = fmaxf(mx, __uint_as_float(v[j]));
           }
         }
-        // P buffer and O are free once PV of the previous block completed.
-        if (b > 0 && !wait_pv(b - 1)) { ok = false; break; }
-        tc_fence_after();
-        if ((blk % C::BPS) != 0) {  // the first block of a segment overwrites O instead
-          // Rescale O where the running max moved (alpha is exactly 1 elsewhere).
-          if (__any_sync(0xffffffffu, valid && alpha != 1.f)) {
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t ov[32];
-              tmem_ld_x32(t_lane + C::TM_O + c0, ov);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__fmul_rn(__uint_as_float(ov[j]), alpha));
-              tmem_st_x32(t_lane + C::TM_O + c0, ov);
+        float alpha = 1.f;
+        if (mx != -INFINITY) {
+          if (m == -INFINITY) {
+            m = mx;  // first visible block of the segment: O starts fresh
+          } else {
+            const float ms_old = __fmul_rn(m, scale), ms_new = __fmul_rn(mx, scale);
+            if (__fsub_rn(ms_new, ms_old) > kLazyRescale) {
+              alpha = ex2(__fsub_rn(ms_old, ms_new));
+              m = mx;
             }
           }
         }
-        if (valid) {
+        const float ms = (m == -INFINITY) ? 0.f : __fmul_rn(m, scale);
+
+        // pass 2: probabilities, the row sum in ascending column order, and
+        // P (bf16 pairs) written over the S columns already read.  Column
+        // j = 3 (mod 4) takes 2^x on the FMA pipe, the others on MUFU.
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!live) {
+          const uint32_t zero[16] = {};
 #pragma unroll
-          for (int u = 0; u < C::BN / 8; ++u) {
-            const uint32_t w0 = pack_bf16x2(__uint_as_float(sv[8 * u + 0]), __uint_as_float(sv[8 * u + 1]));
-            const uint32_t w1 = pack_bf16x2(__uint_as_float(sv[8 * u + 2]), __uint_as_float(sv[8 * u + 3]));
-            const uint32_t w2 = pack_bf16x2(__uint_as_float(sv[8 * u + 4]), __uint_as_float(sv[8 * u + 5]));
-            const uint32_t w3 = pack_bf16x2(__uint_as_float(sv[8 * u + 6]), __uint_as_float(sv[8 * u + 7]));
-            const uint32_t addr = sP + (u >> 3) * C::Q_CHUNK + row * 128 + (((u & 7) ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2),
-                         "r"(w3)
-                         : "memory");
+          for (int c0 = 0; c0 < C::BN; c0 += 32) tmem_st_x16(sa + c0 / 2, zero);
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < (live ? C::BN : 0); c0 += 32) {
+          uint32_t v[32], pk[16];
+          tmem_ld_x32(sa + c0, v);
+          float pr[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = __fmaf_rn(__uint_as_float(v[j]), scale, -ms);
+            const float e = (j & 3) == 3 ? ex2_fma(x) : ex2(x);
+            pr[j] = (whole || c0 + j <= lim) ? e : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            acc[j & 3] = __fadd_rn(acc[j & 3], pr[j]);
+            acc[(j + 1) & 3] = __fadd_rn(acc[(j + 1) & 3], pr[j + 1]);
+            pk[j >> 1] = pack_bf16x2(pr[j], pr[j + 1]);
+          }
+          tmem_st_x16(sa + c0 / 2, pk);
+        }
+        if (valid) {
+          const float rowsum = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+          l = __fadd_rn(__fmul_rn(l, alpha), rowsum);
+        }
+        // Rescale O where the running max moved (alpha is exactly 1 elsewhere);
+        // the first block of a segment overwrites O instead.  With one S
+        // buffer the S_FULL phase already implies the previous PV completed.
+        if ((blk % C::BPS) != 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (C::NS == 2 && !wait_pv(cnt - 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld_x32(o_addr + c0, ov);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__fmul_rn(__uint_as_float(ov[j]), alpha));
+            tmem_st_x32(o_addr + c0, ov);
           }
         }
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(c, B_P_FULL));
+        mbar_arrive(bar(c, B_P_FULL + 2 * t + sbuf));
       }
       if (!ok) break;
 
       // ---- segment end: O of this segment is complete after the last PV
-      if (!wait_pv(b - 1)) { ok = false; break; }
+      if (!wait_pv(cnt - 1)) { ok = false; break; }
       tc_fence_after();
       const float m_seg = (m == -INFINITY) ? -INFINITY : __fmul_rn(m, scale);
-      const int vr = (pos - g.first_valid) * p.group + hg;  // row among the tile's valid rows
+      const int vr = (pos - g.first_valid[t]) * p.group + hg;  // row among the tile's valid rows
       if (split) {
-        float* prow = p.partials + (size_t(w.part_base) + vr) * (D + 4);
-        if (valid) *reinterpret_cast<float4*>(prow) = make_float4(m_seg, l, 0.f, 0.f);
+        const bool write = valid && s < w.nseg[t];
+        float* prow = p.partials + (size_t(w.part_base[t]) + vr) * (D + 4);
+        if (write) *reinterpret_cast<float4*>(prow) = make_float4(m_seg, l, 0.f, 0.f);
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t ov[32];
-          tmem_ld_x32(t_lane + C::TM_O + c0, ov);
-          if (valid) {
+          tmem_ld_x32(o_addr + c0, ov);
+          if (write) {
             float4* dst = reinterpret_cast<float4*>(prow + 4 + c0);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -423,7 +555,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t sbase, uint32_t tmem, const 
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t ov[32];
-          tmem_ld_x32(t_lane + C::TM_O + c0, ov);
+          tmem_ld_x32(o_addr + c0, ov);
           if (valid) {
             float o[32];
             if (use_scratch && st.kind != 1) {
@@ -464,11 +596,77 @@ __device__ void softmax_role(const Ctx& c, uint32_t sbase, uint32_t tmem, const 
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// Two E4M3 codes (low byte first) -> two bf16 (low half first).  Exact: every
+// E4M3 value, subnormals included, is representable in f16, f32 and bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16x2(f.x, f.y);
+}
+
+// FP8 pages: convert each staged block (BN rows x D codes, row-major) into the
+// bf16, 128-byte-swizzled K/V ring slot the MMAs read; V rows at or past
+// kv_len are written as zeros.  K, then V, per block; the bf16 slot is taken
+// once the MMA that last read it has completed.
+template <int D, int NT, int ST, bool KV8>
+__device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) {
+  if constexpr (KV8) {
+    using C = Cfg<D, NT, ST, KV8>;
+    const int tid = int(threadIdx.x) - C::DQ_WARP0 * 32;  // 0..127
+    constexpr int GROUPS = D / 16;                          // 16-code groups per row
+    uint32_t b = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      const WorkItem w = p.items[it];
+      const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
+      for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {
+        const int ss = b % C::SS, slot = b % ST;
+        const uint32_t suse = b / C::SS, use = b / ST;
+        const int valid_rows = w.kv_len - blk * C::BN;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const int full8 = which ? B_V8_FULL : B_K8_FULL, free8 = which ? B_V8_FREE : B_K8_FREE;
+          const int full = which ? B_V_FULL : B_K_FULL, freeb = which ? B_V_FREE : B_K_FREE;
+          if (!wait_warp(c, bar(c, full8 + ss), suse & 1, 30 + which)) { ok = false; break; }
+          if (use > 0 && !wait_warp(c, bar(c, freeb + slot), (use - 1) & 1, 32 + which)) { ok = false; break; }
+          const uint32_t src = sbase + (which ? C::OFF_V8 : C::OFF_K8) + ss * C::KV8_BYTES;
+          const uint32_t dst = sbase + (which ? C::OFF_V : C::OFF_K) + slot * C::KV_BYTES;
+          for (int u = tid; u < C::BN * GROUPS; u += 128) {
+            const int r = u / GROUPS, gi = u % GROUPS;
+            uint32_t x, y, z, q;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x), "=r"(y), "=r"(z), "=r"(q)
+                         : "r"(src + r * D + gi * 16));
+            uint32_t o[8] = {e4m3x2_to_bf16x2(x), e4m3x2_to_bf16x2(x >> 16), e4m3x2_to_bf16x2(y),
+                             e4m3x2_to_bf16x2(y >> 16), e4m3x2_to_bf16x2(z), e4m3x2_to_bf16x2(z >> 16),
+                             e4m3x2_to_bf16x2(q), e4m3x2_to_bf16x2(q >> 16)};
+            if (which == 1 && r >= valid_rows) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o[j] = 0u;
+            }
+            const int ch = gi >> 2, u8 = (gi & 3) * 2;
+            const uint32_t rowb = dst + ch * C::KV_CHUNK + r * 128;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + ((u8 ^ (r & 7)) << 4)), "r"(o[0]),
+                         "r"(o[1]), "r"(o[2]), "r"(o[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + (((u8 + 1) ^ (r & 7)) << 4)),
+                         "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(c, full + slot));
+          mbar_arrive(bar(c, free8 + ss));
+        }
+      }
+    }
+  }
+}
+
+template <int D, int NT, int ST, bool KV8>
+__global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
     bip_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, NT, ST, KV8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -486,16 +684,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(c, B_Q_FULL), 1);
     mbar_init(bar(c, B_Q_FREE), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(c, B_K_FULL + s), 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(bar(c, B_K_FULL + s), KV8 ? 128 : 1);  // FP8: the dequant warps arrive
       mbar_init(bar(c, B_K_FREE + s), 1);
-      mbar_init(bar(c, B_V_FULL + s), 1);
+      mbar_init(bar(c, B_V_FULL + s), KV8 ? 128 : 1);
       mbar_init(bar(c, B_V_FREE + s), 1);
-      mbar_init(bar(c, B_S_FULL + s), 1);
-      mbar_init(bar(c, B_S_FREE + s), 128);
     }
-    mbar_init(bar(c, B_P_FULL), 128);
-    mbar_init(bar(c, B_O_DONE), 1);
+    for (int s = 0; s < C::SS; ++s) {
+      mbar_init(bar(c, B_K8_FULL + s), 1);
+      mbar_init(bar(c, B_K8_FREE + s), 128);
+      mbar_init(bar(c, B_V8_FULL + s), 1);
+      mbar_init(bar(c, B_V8_FREE + s), 128);
+    }
+    for (int t = 0; t < NT; ++t)
+      for (int s = 0; s < C::NS; ++s) {
+        mbar_init(bar(c, B_S_FULL + 2 * t + s), 1);
+        mbar_init(bar(c, B_P_FULL + 2 * t + s), 128);
+        mbar_init(bar(c, B_O_DONE + 2 * t + s), 1);
+      }
     mbar_init(bar(c, B_DRAIN), 1);
     *c.abort = 0u;
     fence_mbar_init();
@@ -514,12 +720,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      producer<D>(c, sbase, &tm_q, &tm_k, &tm_v, p);
+      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, &tm_v, p);
     }
   } else if (warp == 1) {
-    mma_issuer<D>(c, sbase, tmem, p);
+    mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
+  } else if (warp < C::DQ_WARP0) {
+    softmax_role<D, NT, ST, KV8>(c, tmem, p, (warp - 2) / 4);
   } else {
-    softmax_role<D>(c, sbase, tmem, p);
+    dequant_role<D, NT, ST, KV8>(c, sbase, p);
   }
 
   tc_fence_before();
@@ -528,27 +736,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-template <int D>
+template <int D, int NT, int ST, bool KV8>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                    int grid, cudaStream_t stream) {
-  using C = Cfg<D>;
+  using C = Cfg<D, NT, ST, KV8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D, NT, ST, KV8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  bip_attn_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  bip_attn_kernel<D, NT, ST, KV8><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                             const CUtensorMap& tm_v, const AttnParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                             cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch<128>(tm_q, tm_k, tm_v, p, grid, stream);
-  if (head_dim == 256) return launch<256>(tm_q, tm_k, tm_v, p, grid, stream);
+  if (!kv_fp8) {
+    if (head_dim == 128 && tiles_per_unit == 2) return launch<128, 2, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128 && tiles_per_unit == 1) return launch<128, 1, 3, false>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 256 && tiles_per_unit == 1) return launch<256, 1, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
+  } else if (tiles_per_unit == 1) {
+    if (head_dim == 128) return launch<128, 1, 2, true>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 256) return launch<256, 1, 2, true>(tm_q, tm_k, tm_v, p, grid, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -34,15 +34,17 @@ constexpr size_t kDefaultSplitBudget = size_t(256) << 20;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct UnitDesc {
-  int32_t request, kv_head, tile, nseg, rows, blocks;
-  int32_t first_valid;
+  int32_t request, kv_head, tile;  // tile = absolute tile of slot 0
+  int32_t mask;                    // slots present
+  int32_t rows[bip::kMaxTilesPerUnit], nseg[bip::kMaxTilesPerUnit];
+  int32_t nseg_unit, blocks;       // over the union of the slots' keys
 };
 
 }  // namespace
 
 struct bip_plan_s {
   int32_t batch = 0, hq = 0, hkv = 0, d = 0, page_size = 0, kv_dtype = 0;
-  int32_t group = 0, T = 0, bn = 0, total_q = 0;
+  int32_t group = 0, T = 0, bn = 0, nt = 1, total_q = 0;
   bip_plan_options opts{};
   std::vector<WorkItem> items;
   std::vector<MergeUnit> merges;
@@ -119,11 +121,13 @@ extern "C" size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, in
   if (max_batch < 0 || max_total_q < 0 || check_heads(num_qo_heads, num_kv_heads, head_dim) != BIP_OK) return 0;
   const int64_t group = num_qo_heads / num_kv_heads;
   const int64_t T = bip::kTileRows / group;
-  // A request with q_len rows touches at most ceil(q_len / T) + 1 tiles.
+  // A request with q_len rows touches at most ceil(q_len / T) + 1 tiles, so
+  // at most that many units (a unit holds one or two tiles).
   const int64_t units = int64_t(num_kv_heads) * ((int64_t(max_total_q) + T - 1) / T + 2 * int64_t(max_batch));
   // Each extra split item needs at least `group` partial rows of budget.
   const int64_t extra = int64_t(split_budget_bytes / (size_t(group) * partial_row_bytes(head_dim)));
-  const size_t scratch = size_t(bip::kMaxCtas) * bip::kTileRows * head_dim * sizeof(float);
+  const size_t scratch =
+      size_t(bip::kMaxCtas) * bip::max_tiles_per_unit_for(head_dim) * bip::kTileRows * head_dim * sizeof(float);
   size_t a, b, c, e, u;
   return layout_bytes(size_t(units + extra), size_t(units), split_budget_bytes, scratch, &a, &b, &c, &e, &u);
 }
@@ -139,7 +143,6 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   bip_status st = check_heads(num_qo_heads, num_kv_heads, head_dim);
   if (st != BIP_OK) return st;
   if (kv_dtype != BIP_KV_BF16 && kv_dtype != BIP_KV_FP8_E4M3) return BIP_ERR_INVALID_ARG;
-  if (kv_dtype != BIP_KV_BF16) return BIP_ERR_UNSUPPORTED;
   const int32_t bn = bip::kv_block_for(head_dim);
   if (page_size <= 0) return BIP_ERR_INVALID_ARG;
   if ((page_size & (page_size - 1)) != 0 || page_size < 8 || page_size > bn) return BIP_ERR_UNSUPPORTED;
@@ -149,11 +152,16 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   opts.split_budget_bytes = kDefaultSplitBudget;
   opts.num_sms = 0;
   opts.wait_limit_ns = 0;
+  opts.tiles_per_unit = 0;
   if (opts_in) opts = *opts_in;
   if (opts.split_policy != BIP_SPLIT_AUTO && opts.split_policy != BIP_SPLIT_NEVER &&
       opts.split_policy != BIP_SPLIT_ALWAYS)
     return BIP_ERR_INVALID_ARG;
   if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
+  if (opts.tiles_per_unit < 0 || opts.tiles_per_unit > bip::max_tiles_per_unit_for(head_dim))
+    return BIP_ERR_INVALID_ARG;
+  // FP8 pages run in the one-tile variant (its dequant warpgroup needs the room).
+  if (kv_dtype == BIP_KV_FP8_E4M3 && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
   if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
 
   // ---- lengths and validation
@@ -176,28 +184,58 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     kv_len[r] = int32_t(kl);
   }
 
-  // ---- units: (request, kv head, absolute q tile)
+  // ---- tiles per unit (numerically neutral).  Two tiles per CTA share every
+  // KV block and overlap one tile's softmax with the other's MMAs; one tile
+  // per CTA leaves room for a deeper KV ring, which short extends (bound by
+  // HBM, one tile per request) need more.
+  int32_t NT = opts.tiles_per_unit;
+  if (NT == 0) {
+    int64_t tiles = 0, active = 0;
+    for (int32_t r = 0; r < batch; ++r) {
+      if (q_len[r] == 0) continue;
+      ++active;
+      tiles += (kv_len[r] - 1) / T - (kv_len[r] - q_len[r]) / T + 1;
+    }
+    NT = (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 && tiles >= 2 * active) ? 2 : 1;
+  }
+
+  // ---- units: (request, kv head, NT consecutive absolute q tiles sharing keys)
   std::vector<UnitDesc> units;
   for (int32_t r = 0; r < batch; ++r) {
     if (q_len[r] == 0) continue;
     const int32_t q_lo = kv_len[r] - q_len[r];
     const int32_t t0 = q_lo / T, t1 = (kv_len[r] - 1) / T;
-    for (int32_t t = t0; t <= t1; ++t) {
-      const int32_t tile_end = std::min(t * T + T - 1, kv_len[r] - 1);
-      const int32_t first_valid = std::max(t * T, q_lo);
+    for (int32_t g0 = (t0 / NT) * NT; g0 <= t1; g0 += NT) {
       UnitDesc u;
       u.request = r;
-      u.tile = t;
-      u.nseg = tile_end / bip::kSplitLen + 1;
-      u.rows = (tile_end - first_valid + 1) * group;
-      u.blocks = tile_end / bn + 1;
-      u.first_valid = first_valid;
+      u.tile = g0;
+      u.mask = 0;
+      int32_t unit_end = -1;
+      for (int32_t t = 0; t < NT; ++t) {
+        const int32_t tile = g0 + t;
+        u.rows[t] = 0;
+        u.nseg[t] = 0;
+        if (tile < t0 || tile > t1) continue;
+        const int32_t tile_end = std::min(tile * T + T - 1, kv_len[r] - 1);
+        const int32_t first_valid = std::max(tile * T, q_lo);
+        u.mask |= 1 << t;
+        u.rows[t] = (tile_end - first_valid + 1) * group;
+        u.nseg[t] = tile_end / bip::kSplitLen + 1;
+        unit_end = std::max(unit_end, tile_end);
+      }
+      u.nseg_unit = unit_end / bip::kSplitLen + 1;
+      u.blocks = unit_end / bn + 1;
       for (int32_t h = 0; h < num_kv_heads; ++h) {
         u.kv_head = h;
         units.push_back(u);
       }
     }
   }
+  auto split_need = [&](const UnitDesc& u) {
+    size_t rows = 0;
+    for (int t = 0; t < NT; ++t) rows += size_t(u.nseg[t]) * u.rows[t];
+    return rows * partial_row_bytes(head_dim);
+  };
 
   // ---- split decision (numerically neutral; see the header)
   int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
@@ -208,7 +246,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   if (opts.split_policy != BIP_SPLIT_NEVER) {
     std::vector<size_t> cand;
     for (size_t i = 0; i < units.size(); ++i)
-      if (units[i].nseg > 1) cand.push_back(i);
+      if (units[i].nseg_unit > 1) cand.push_back(i);
     std::stable_sort(cand.begin(), cand.end(),
                      [&](size_t a, size_t b) { return units[a].blocks > units[b].blocks; });
     // AUTO: split by segment when there are too few units to balance a
@@ -220,11 +258,11 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     const bool few_units = int64_t(units.size()) < 8 * int64_t(num_sms);
     for (size_t i : cand) {
       if (opts.split_policy == BIP_SPLIT_AUTO && !few_units && units[i].blocks <= fair_half) break;
-      const size_t need = size_t(units[i].nseg) * units[i].rows * partial_row_bytes(head_dim);
+      const size_t need = split_need(units[i]);
       if (partial_bytes + need > opts.split_budget_bytes) continue;
       split[i] = 1;
       partial_bytes += need;
-      n_items += units[i].nseg - 1;
+      n_items += units[i].nseg_unit - 1;
     }
   }
 
@@ -240,6 +278,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->group = group;
   p->T = T;
   p->bn = bn;
+  p->nt = NT;
   p->total_q = qo_indptr[batch];
   p->opts = opts;
   p->num_units = int32_t(units.size());
@@ -248,49 +287,53 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     WorkItem w;
     int32_t desc[8];
     int32_t order_blocks;
-    size_t seq;
   };
   std::vector<Pending> pend;
   pend.reserve(size_t(n_items));
   int64_t part_rows = 0;
-  size_t seq = 0;
   for (size_t i = 0; i < units.size(); ++i) {
     const UnitDesc& u = units[i];
     const int32_t r = u.request;
     WorkItem w;
+    std::memset(&w, 0, sizeof(w));
     w.kv_len = kv_len[r];
     w.page_base = kv_indptr[r];
     w.q_tok0 = qo_indptr[r] - (kv_len[r] - q_len[r]);
     w.q_lo = kv_len[r] - q_len[r];
     w.tile = u.tile;
     w.kv_head = int16_t(u.kv_head);
-    w.flags = 0;
-    w.part_base = 0;
+    w.flags = int16_t(u.mask * bip::kSlotPresent);
+    for (int t = 0; t < NT; ++t) w.nseg[t] = int16_t(u.nseg[t]);
     const int32_t bps = bip::kSplitLen / bn;
     if (!split[i]) {
       w.seg_lo = 0;
-      w.seg_hi = int16_t(u.nseg - 1);
-      pend.push_back({w, {r, u.kv_head, u.tile, 0, u.nseg - 1, 0, u.blocks, 0}, u.blocks, seq++});
+      w.seg_hi = int16_t(u.nseg_unit - 1);
+      pend.push_back({w, {r, u.kv_head, u.tile, 0, u.nseg_unit - 1, 0, u.blocks, u.mask}, u.blocks});
     } else {
-      MergeUnit m;
-      m.q_tok0 = w.q_tok0;
-      m.q_lo = w.q_lo;
-      m.tile = u.tile;
-      m.part_base = int32_t(part_rows);
-      m.rows = u.rows;
-      m.kv_head = int16_t(u.kv_head);
-      m.nseg = int16_t(u.nseg);
-      m.pad[0] = m.pad[1] = 0;
-      p->merges.push_back(m);
-      for (int32_t s = 0; s < u.nseg; ++s) {
-        WorkItem ws = w;
-        ws.seg_lo = ws.seg_hi = int16_t(s);
-        ws.flags = bip::kItemSplit;
-        ws.part_base = int32_t(part_rows + int64_t(s) * u.rows);
-        const int32_t blocks = std::min(u.blocks, (s + 1) * bps) - s * bps;
-        pend.push_back({ws, {r, u.kv_head, u.tile, s, s, 1, blocks, 0}, blocks, seq++});
+      int64_t base[bip::kMaxTilesPerUnit] = {0, 0};
+      for (int t = 0; t < NT; ++t) {
+        if (!(u.mask >> t & 1)) continue;
+        MergeUnit m;
+        std::memset(&m, 0, sizeof(m));
+        m.q_tok0 = w.q_tok0;
+        m.q_lo = w.q_lo;
+        m.tile = u.tile + t;
+        m.part_base = int32_t(part_rows);
+        m.rows = u.rows[t];
+        m.kv_head = int16_t(u.kv_head);
+        m.nseg = int16_t(u.nseg[t]);
+        p->merges.push_back(m);
+        base[t] = part_rows;
+        part_rows += int64_t(u.nseg[t]) * u.rows[t];
       }
-      part_rows += int64_t(u.nseg) * u.rows;
+      for (int32_t sg = 0; sg < u.nseg_unit; ++sg) {
+        WorkItem ws = w;
+        ws.seg_lo = ws.seg_hi = int16_t(sg);
+        ws.flags = int16_t(w.flags | bip::kItemSplit);
+        for (int t = 0; t < NT; ++t) ws.part_base[t] = int32_t(base[t] + int64_t(sg) * u.rows[t]);
+        const int32_t blocks = std::min(u.blocks, (sg + 1) * bps) - sg * bps;
+        pend.push_back({ws, {r, u.kv_head, u.tile, sg, sg, 1, blocks, u.mask}, blocks});
+      }
       p->num_split_units++;
     }
   }
@@ -314,7 +357,8 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->partial_rows = part_rows;
   p->partial_bytes = size_t(part_rows) * partial_row_bytes(head_dim);
   p->grid = int32_t(std::min<int64_t>(int64_t(p->items.size()), num_sms));
-  p->scratch_bytes = p->need_scratch ? size_t(p->grid) * bip::kTileRows * head_dim * sizeof(float) : 0;
+  p->scratch_bytes =
+      p->need_scratch ? size_t(p->grid) * NT * bip::kTileRows * head_dim * sizeof(float) : 0;
   p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->partial_bytes, p->scratch_bytes, &p->off_items,
                              &p->off_merges, &p->off_partials, &p->off_scratch, &p->upload_bytes);
 
@@ -360,6 +404,7 @@ extern "C" bip_status bip_plan_get_info(bip_plan_t p, bip_plan_info* info) {
   info->num_items = int32_t(p->items.size());
   info->num_split_units = p->num_split_units;
   info->grid = p->grid;
+  info->tiles_per_unit = p->nt;
   info->partial_rows = p->partial_rows;
   info->kv_blocks = p->kv_blocks;
   info->workspace_bytes = p->ws_bytes;
@@ -447,17 +492,21 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return BIP_ERR_CUDA;
   }
-  // pages: [pages, slot, Hkv, d] as dims (d, Hkv, slot, page); box (64, 1, page_size, 1) = one page chunk.
+  // pages: [pages, slot, Hkv, d] as dims (d, Hkv, slot, page).  bf16: box (64, 1, page_size, 1), one
+  // 128-byte-swizzled chunk of a page.  FP8: box (d, 1, page_size, 1), a whole page row-major, unswizzled
+  // (the dequant warps lay out the bf16 operand).
+  const bool fp8 = p->kv_dtype == BIP_KV_FP8_E4M3;
   for (int which = 0; which < 2; ++which) {
     const void* base = which == 0 ? k_pages : v_pages;
     cuuint64_t dims[4] = {cuuint64_t(p->d), cuuint64_t(p->hkv), cuuint64_t(p->page_size), cuuint64_t(num_pages)};
-    cuuint64_t strides[3] = {cuuint64_t(p->d) * 2, cuuint64_t(p->hkv) * p->d * 2,
-                             cuuint64_t(page_stride_elems) * 2};
-    cuuint32_t box[4] = {64, 1, cuuint32_t(p->page_size), 1};
+    cuuint64_t strides[3] = {cuuint64_t(p->d) * elem, cuuint64_t(p->hkv) * p->d * elem,
+                             cuuint64_t(page_stride_elems) * elem};
+    cuuint32_t box[4] = {fp8 ? cuuint32_t(p->d) : 64u, 1, cuuint32_t(p->page_size), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    if (encode(which == 0 ? &tm_k : &tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (encode(which == 0 ? &tm_k : &tm_v, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return BIP_ERR_CUDA;
   }
 
@@ -482,7 +531,8 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
   ap.v_scale = v_scale;
   ap.wait_limit_ns = p->opts.wait_limit_ns;
-  if (bip::launch_attention(p->d, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess) return BIP_ERR_CUDA;
+  if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
+    return BIP_ERR_CUDA;
 
   if (!p->merges.empty()) {
     bip::MergeParams mp;

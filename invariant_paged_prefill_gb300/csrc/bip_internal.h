@@ -28,22 +28,30 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
 
-// One attention work item: a (request, kv head, q tile) unit over a range
-// of its segments.  32 bytes.
+// One attention work item: a unit (request x KV head x up to two absolute q
+// tiles that share the same keys) over a range of its segments.  48 bytes.
 struct WorkItem {
   int32_t kv_len;
   int32_t page_base;   // first entry of the request in kv_indices
   int32_t q_tok0;      // q row of sequence position 0 (may be negative)
   int32_t q_lo;        // first position that has a q row (kv_len - q_len)
-  int32_t tile;        // absolute tile: positions [tile*T, tile*T + T)
+  int32_t tile;        // absolute tile of slot 0; slot t covers positions [(tile+t)*T, +T)
   int16_t kv_head;
   int16_t seg_lo;      // inclusive segment range
   int16_t seg_hi;
-  int16_t flags;       // kItemSplit: write fp32 partials instead of out/lse
-  int32_t part_base;   // split: partial row of this item's first valid row
+  int16_t flags;       // kItemSplit | tile-present bits (kSlotPresent << t)
+  int32_t part_base[2];  // split: partial row of slot t's first valid row in this segment
+  int16_t nseg[2];       // segments that hold slot t's rows (tile_end / 4096 + 1)
+  int32_t pad[2];
 };
-static_assert(sizeof(WorkItem) == 32, "work item size");
+static_assert(sizeof(WorkItem) == 48, "work item size");
 constexpr int16_t kItemSplit = 1;
+constexpr int16_t kSlotPresent = 1 << 8;
+constexpr int kMaxTilesPerUnit = 2;
+
+// Most q tiles a CTA carries at once: two for head_dim 128 (TMEM holds S and
+// O of both), one for head_dim 256 (O alone takes 256 of the 512 columns).
+constexpr int max_tiles_per_unit_for(int head_dim) { return head_dim == 128 ? 2 : 1; }
 
 // One merge unit: the partials of a split unit, folded in segment order.
 struct MergeUnit {
@@ -90,8 +98,9 @@ struct MergeParams {
 };
 
 // Kernel launchers (bip_attn.cu / bip_merge.cu).
-cudaError_t launch_attention(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                             const CUtensorMap& tm_v, const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
 
 }  // namespace bip

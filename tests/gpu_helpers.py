@@ -26,12 +26,14 @@ def to_device(b: W.PagedBatch, device) -> W.PagedBatch:
 
 
 def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 << 20, num_sms: int = 0,
-            wait_limit_ns: int = 0, check_status: bool = True, k_scale: float = 1.0, v_scale: float = 1.0):
+            wait_limit_ns: int = 0, check_status: bool = True, k_scale: float = 1.0, v_scale: float = 1.0,
+            tiles_per_unit: int = 0):
     """Plan + prefill on the device; returns (out, lse, plan) on the host."""
     d = b if b.q.is_cuda else to_device(b, device)
     plan = bip.Plan(d.qo_indptr, d.kv_indptr, d.kv_last_page_len, num_qo_heads=d.num_qo_heads,
                     num_kv_heads=d.num_kv_heads, head_dim=d.head_dim, page_size=d.page_size, kv_dtype=d.kv_dtype,
-                    split_policy=policy, split_budget_bytes=budget, num_sms=num_sms, wait_limit_ns=wait_limit_ns)
+                    split_policy=policy, split_budget_bytes=budget, num_sms=num_sms, wait_limit_ns=wait_limit_ns,
+                    tiles_per_unit=tiles_per_unit)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     out = torch.full_like(d.q, float("nan"))
     lse = torch.full((d.q.shape[0], d.q.shape[1]), float("nan"), dtype=torch.float32, device=device)
@@ -39,7 +41,8 @@ def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 
                 k_scale=k_scale, v_scale=v_scale)
     status = bip.read_device_status(ws)
     if check_status:
-        assert status == 0, bip.STATUS.get(status, status)
+        where = int(ws[4:8].view(torch.int32).item())  # header: status, wait site, bad page count
+        assert status == 0, f"{bip.STATUS.get(status, status)} (wait site {where})"
     return out.cpu(), lse.cpu(), plan
 
 

@@ -58,7 +58,7 @@ def plan_code(qo, kv, last, hq=32, hkv=8, d=128, ps=16, kv_dtype=0, opts=None):
     (dict(qo=[0, 1], kv=[0, 1], last=[4], hq=30), 1),     # heads do not divide
     (dict(qo=[0, 1], kv=[0, 1], last=[4], d=64), 2),      # unsupported head_dim
     (dict(qo=[0, 1], kv=[0, 1], last=[4], ps=12), 2),     # page size not a power of two
-    (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=1), 2),  # fp8 not built yet
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=1), 0),  # FP8 E4M3 pages
     (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=9), 1),
     (dict(qo=[0, 0, 3], kv=[0, 0, 1], last=[0, 3]), 0),   # zero-length request with no pages
     (dict(qo=[0, 0, 3], kv=[0, 2, 3], last=[16, 3]), 0),  # zero-length request behind a prefix
@@ -128,10 +128,11 @@ def test_large_head_workspace_is_small():
 
 
 def unit_geometry(plan, request):
-    """(kv_head, q_tile) pairs and folded segment ranges of one request."""
+    """(kv_head, absolute q tile) pairs and item geometry of one request."""
     it = plan.items()
     mine = it[it[:, 0] == request]
-    return sorted({(int(r[1]), int(r[2])) for r in mine}), sorted(tuple(int(x) for x in r[1:6]) for r in mine)
+    tiles = {(int(r[1]), int(r[2]) + t) for r in mine for t in range(2) if r[7] >> t & 1}
+    return sorted(tiles), sorted(tuple(int(x) for x in list(r[1:6]) + [r[7]]) for r in mine)
 
 
 def test_schedule_of_a_request_does_not_depend_on_its_batch_mates(lib):
@@ -171,6 +172,29 @@ def test_split_policies_cover_the_same_units():
                 assert key not in seen
                 seen[key] = 1
         assert len(seen) == sum(r[4] - r[3] + 1 for r in plans["never"].items())
+
+
+def test_tiles_per_unit_choice():
+    # long requests pair q tiles; one-tile extends keep one tile per CTA
+    assert bip.Plan([0, 8192], [0, 512], [16], num_qo_heads=32, num_kv_heads=8,
+                    head_dim=128).info["tiles_per_unit"] == 2
+    assert bip.Plan([0, 4], [0, 2048], [16], num_qo_heads=32, num_kv_heads=8,
+                    head_dim=128).info["tiles_per_unit"] == 1
+    assert bip.Plan([0, 8192], [0, 512], [16], num_qo_heads=24, num_kv_heads=4,
+                    head_dim=256).info["tiles_per_unit"] == 1
+    with pytest.raises(bip.BipError):
+        bip.Plan([0, 8], [0, 1], [16], num_qo_heads=24, num_kv_heads=4, head_dim=256, tiles_per_unit=2)
+    # FP8 pages run one tile per CTA
+    assert bip.Plan([0, 8192], [0, 512], [16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                    kv_dtype="fp8_e4m3").info["tiles_per_unit"] == 1
+    with pytest.raises(bip.BipError):
+        bip.Plan([0, 8], [0, 1], [16], num_qo_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="fp8_e4m3",
+                 tiles_per_unit=2)
+    # forcing either variant covers the same tiles
+    for tpu in (1, 2):
+        p = bip.Plan([0, 100, 103], [0, 7, 70], [4, 16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                     tiles_per_unit=tpu)
+        assert unit_geometry(p, 0)[0] == [(h, t) for h in range(8) for t in range(0, 4)]
 
 
 def test_items_grouped_by_request_and_head_longest_first():

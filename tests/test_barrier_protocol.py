@@ -1,0 +1,220 @@
+"""Model check of the attention kernel's mbarrier schedule (CPU, no GPU).
+
+The kernel's roles (TMA producer, optional FP8 dequant warpgroup, tcgen05
+issuer, one softmax warpgroup per q-tile slot of 4 warps) synchronise through
+mbarriers waited on by phase parity.  This test replays that schedule -- the
+same waits, arrivals and commits, in the same order per role as
+csrc/bip_attn.cu -- with random completion delays for TMA loads and MMAs and
+random interleavings of the roles, for every kernel variant, and checks two
+properties on many schedules:
+
+* no deadlock: every role finishes;
+* no aliased wait: when a parity wait returns, the barrier has completed
+  exactly the phase waited for (not one fewer, not two more).  A barrier that
+  can run two phases ahead of its waiter reads as "not yet" forever; one that
+  a waiter can read before its phase completes lets it consume data early.
+
+tcgen05.commit arrives once every MMA issued before it by the same thread has
+completed (modelled as in-order completion of the issuer's operations).
+"""
+
+import random
+
+import pytest
+
+
+class _Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.phase = count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, "over-arrival"
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def done(self, parity):
+        return (self.phase & 1) != parity
+
+
+def _simulate(NT, NS, ST, SS, items, seed, warps=4):
+    """items: list of (nb, mask); SS > 0 models FP8 staging + dequant."""
+    rnd = random.Random(seed)
+    B = {}
+
+    def bar(name, count=1):
+        B.setdefault(name, _Bar(count))
+
+    for s in range(ST):
+        for n in ("K_FULL", "V_FULL"):
+            bar(f"{n}{s}", 128 if SS else 1)
+        bar(f"K_FREE{s}"), bar(f"V_FREE{s}")
+    for s in range(SS):
+        bar(f"K8_FULL{s}"), bar(f"V8_FULL{s}"), bar(f"K8_FREE{s}", 128), bar(f"V8_FREE{s}", 128)
+    for t in range(NT):
+        for s in range(NS):
+            bar(f"S_FULL{t}{s}"), bar(f"P_FULL{t}{s}", 32 * warps), bar(f"O_DONE{t}{s}")
+    bar("Q_FULL"), bar("Q_FREE")
+    clock, pending, last_mma = [0], [], [0]
+
+    def later(name, lo=1, hi=8):
+        pending.append((clock[0] + rnd.randint(lo, hi), name))
+
+    def commit(name):
+        last_mma[0] = max(last_mma[0], clock[0]) + rnd.randint(1, 5)
+        pending.append((last_mma[0], name))
+
+    def wait(name, idx):
+        return ("wait", name, idx)
+
+    def producer():
+        b = 0
+        for n, (nb, mask) in enumerate(items):
+            if n > 0:
+                yield wait("Q_FREE", n - 1)
+            later("Q_FULL")
+            for _ in range(nb):
+                if SS:
+                    ss, use = b % SS, b // SS
+                    for kv in ("K8", "V8"):
+                        if use > 0:
+                            yield wait(f"{kv}_FREE{ss}", use - 1)
+                        later(f"{kv}_FULL{ss}")
+                else:
+                    slot, use = b % ST, b // ST
+                    for kv in ("K", "V"):
+                        if use > 0:
+                            yield wait(f"{kv}_FREE{slot}", use - 1)
+                        later(f"{kv}_FULL{slot}")
+                b += 1
+                yield None
+
+    def dequant():
+        b = 0
+        for nb, _ in items:
+            for _ in range(nb):
+                ss, slot = b % SS, b % ST
+                for kv in ("K", "V"):
+                    yield wait(f"{kv}8_FULL{ss}", b // SS)
+                    if b // ST > 0:
+                        yield wait(f"{kv}_FREE{slot}", b // ST - 1)
+                    for _ in range(128):
+                        B[f"{kv}_FULL{slot}"].arrive()
+                        B[f"{kv}8_FREE{ss}"].arrive()
+                b += 1
+                yield None
+
+    def issuer():
+        gb, s_cnt, pv_cnt = 0, [0] * NT, [0] * NT
+        for n, (nb, mask) in enumerate(items):
+            yield wait("Q_FULL", n)
+            last = max(t for t in range(NT) if mask >> t & 1)
+
+            def issue_s(t, j):
+                kb = gb + j
+                yield wait(f"K_FULL{kb % ST}", kb // ST)
+                commit(f"S_FULL{t}{s_cnt[t] % NS}")
+                if t == last:
+                    commit(f"K_FREE{kb % ST}")
+                    if j == nb - 1:
+                        commit("Q_FREE")
+                s_cnt[t] += 1
+
+            for j in range(min(NS, nb)):
+                for t in range(NT):
+                    if mask >> t & 1:
+                        yield from issue_s(t, j)
+            for j in range(nb):
+                vb = gb + j
+                vready = False
+                for t in range(NT):
+                    if not mask >> t & 1:
+                        continue
+                    yield wait(f"P_FULL{t}{pv_cnt[t] % NS}", pv_cnt[t] // NS)
+                    if not vready:
+                        yield wait(f"V_FULL{vb % ST}", vb // ST)
+                        vready = True
+                    commit(f"O_DONE{t}{pv_cnt[t] % NS}")
+                    pv_cnt[t] += 1
+                    if j + NS < nb:
+                        yield from issue_s(t, j + NS)
+                commit(f"V_FREE{vb % ST}")
+                yield None
+            gb += nb
+
+    def softmax(t):
+        cnt, pv_seen = 0, 0
+
+        def wait_pv(x):
+            nonlocal pv_seen
+            if pv_seen <= x:
+                yield wait(f"O_DONE{t}{x % NS}", x // NS)
+                pv_seen = x + 1
+
+        for nb, mask in items:
+            if not mask >> t & 1:
+                continue
+            for blk in range(nb):
+                yield wait(f"S_FULL{t}{cnt % NS}", cnt // NS)
+                if blk > 0 and NS == 2 and rnd.random() < 0.3:   # a row's max moved: rescale O
+                    yield from wait_pv(cnt - 1)
+                for _ in range(32):
+                    B[f"P_FULL{t}{cnt % NS}"].arrive()
+                cnt += 1
+                yield None
+            yield from wait_pv(cnt - 1)                            # segment end: read O
+
+    roles = [("producer", producer()), ("issuer", issuer())]
+    roles += [(f"softmax{t}.{w}", softmax(t)) for t in range(NT) for w in range(warps)]
+    if SS:
+        roles.append(("dequant", dequant()))
+    state, done = {n: None for n, _ in roles}, set()
+    for _ in range(500000):
+        clock[0] += 1
+        pending.sort()
+        while pending and pending[0][0] <= clock[0]:
+            B[pending.pop(0)[1]].arrive()
+        order = list(roles)
+        rnd.shuffle(order)
+        moved = False
+        for name, gen in order:
+            if name in done:
+                continue
+            st = state[name]
+            if st is not None:
+                _, bname, idx = st
+                if not B[bname].done(idx & 1):
+                    continue
+                assert B[bname].phase == idx + 1, f"{name}: aliased wait on {bname} phase {idx}"
+                state[name] = None
+            moved = True
+            try:
+                state[name] = next(gen)
+            except StopIteration:
+                done.add(name)
+        if len(done) == len(roles):
+            return
+        assert moved or pending, f"deadlock: {state}"
+    raise AssertionError("schedule did not finish")
+
+
+VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages)
+    "d128_two_tiles": (2, 1, 2, 0),
+    "d128_one_tile": (1, 2, 3, 0),
+    "d256": (1, 2, 2, 0),
+    "d128_fp8": (1, 2, 2, 2),
+    "d256_fp8": (1, 2, 2, 1),
+}
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+def test_schedule_never_deadlocks_or_aliases(variant):
+    NT, NS, ST, SS = VARIANTS[variant]
+    full = (1 << NT) - 1
+    item_sets = [[(1, full)], [(9, full)], [(4, full), (1, full), (17, full)], [(3, 1), (2, full), (5, 1)]]
+    if NT == 2:
+        item_sets.append([(6, 2), (2, 1), (7, 3)])
+    for items in item_sets:
+        for seed in range(60):
+            _simulate(NT, NS, ST, SS, items, seed)

@@ -130,3 +130,33 @@ def test_zero_length_requests_and_single_token(cuda):
     alone = W.layout([prompts[3]], [16], 16, seed_pages=4)
     ao, al, _ = run_gpu(alone, cuda)
     assert_bitwise(o[1:], ao)
+
+
+def test_one_and_two_tiles_per_cta_identical(cuda):
+    # The memory-bound variant (one q tile per CTA, deeper KV ring) and the
+    # ping-pong variant (two tiles per CTA) must give the same bits.
+    hq, hkv, d = W.HEADS_A
+    prompts = [W.make_prompt(n, hq, hkv, d, seed=60 + i) for i, n in enumerate((5000, 300, 4100, 77))]
+    b = W.layout(prompts, [5000, 3, 900, 40], 16)
+    r1 = run_gpu(b, cuda, tiles_per_unit=1)
+    r2 = run_gpu(b, cuda, tiles_per_unit=2)
+    assert r1[2].info["tiles_per_unit"] == 1 and r2[2].info["tiles_per_unit"] == 2
+    assert_bitwise(r1[0], r2[0], "out 1 vs 2 tiles per CTA")
+    assert_bitwise(r1[1], r2[1], "lse 1 vs 2 tiles per CTA")
+    r3 = run_gpu(b, cuda, tiles_per_unit=2, policy="always")
+    assert_bitwise(r3[0], r2[0], "out split vs fold, 2 tiles")
+
+
+def test_fp8_extend_equals_full_and_split_equals_fold(cuda):
+    hq, hkv, d = W.HEADS_A
+    p = W.make_prompt(9000, hq, hkv, d, seed=70, kv_dtype="fp8_e4m3")
+    full = W.layout([p], [9000], 16, kv_dtype="fp8_e4m3")
+    ext = W.layout([p], [37], 16, seed_pages=4, kv_dtype="fp8_e4m3")
+    fo, fl, _ = run_gpu(full, cuda)
+    eo, el, _ = run_gpu(ext, cuda, policy="never")
+    so, sl, sp = run_gpu(ext, cuda, policy="always")
+    assert sp.info["num_split_units"] > 0
+    assert_bitwise(eo, fo[9000 - 37:], "fp8 extend vs full")
+    assert_bitwise(el, fl[9000 - 37:])
+    assert_bitwise(so, eo, "fp8 split vs fold")
+    assert_bitwise(sl, el)

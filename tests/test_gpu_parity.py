@@ -82,3 +82,30 @@ def test_sweep_point_short_extend_long_kv(cuda):
     rows = sample_rows(b, per_request=4)
     ro, rl = oracle(b, rows=rows)
     assert_close_to_oracle(o, l, ro, rl, rows=rows)
+
+
+@pytest.mark.parametrize("heads", [W.HEADS_A, W.HEADS_B])
+def test_fp8_pages_match_oracle(cuda, heads):
+    # E4M3 pages (N(0,1) clipped to +-448); the oracle decodes the stored codes itself.
+    hq, hkv, d = heads
+    lens = [(5, 300), (133, 133), (1, 1), (40, 4500)]
+    prompts = [W.make_prompt(kv, hq, hkv, d, seed=41 + i, kv_dtype="fp8_e4m3") for i, (_, kv) in enumerate(lens)]
+    b = W.layout(prompts, [q for q, _ in lens], 16, seed_pages=6, kv_dtype="fp8_e4m3")
+    o, l, plan = run_gpu(b, cuda)
+    assert plan.info["kv_dtype"] == 1
+    ro, rl = oracle(b)
+    assert_close_to_oracle(o, l, ro, rl)
+
+
+def test_fp8_scales_match_oracle(cuda):
+    # K scale multiplies the logits, V scale the output.
+    from oracle import paged_attention as pa
+    hq, hkv, d = W.HEADS_A
+    prompts = [W.make_prompt(n, hq, hkv, d, seed=90 + n, kv_dtype="fp8_e4m3") for n in (70, 200)]
+    b = W.layout(prompts, [70, 9], 16, kv_dtype="fp8_e4m3")
+    o, l, _ = run_gpu(b, cuda, k_scale=0.5, v_scale=2.0)
+    ro, rl = pa.paged_prefill(b.q.view(torch.int16).numpy(), b.k_pages.numpy(), b.v_pages.numpy(),
+                              b.qo_indptr.tolist(), b.kv_indptr.tolist(), b.kv_indices.tolist(),
+                              b.kv_last_page_len.tolist(), hq, hkv, 16, q_kind="bf16", kv_kind="e4m3",
+                              k_scale=0.5, v_scale=2.0)
+    assert_close_to_oracle(o, l, ro, rl)
