@@ -168,6 +168,33 @@ bip_status bip_prefill(bip_plan_t plan, const void* q, int64_t num_q_rows, const
                        const int32_t* kv_indices, float k_scale, float v_scale, void* out,
                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the device array that bip_prefill_no_alloc uses as its workspace. */
+#define BIP_NO_ALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/* No counterpart on the pages: an entry point for callers that cannot allocate
+ * device memory -- an engine plugin whose host framework owns the GPU's memory
+ * through its own pool and gives the plugin no allocation hook, or a serving
+ * loop that forbids allocation on the request path.  Same as bip_prefill, but
+ * the workspace is a file-scope device array of BIP_NO_ALLOC_WORKSPACE_BYTES
+ * inside this library, which every GPU that loads the library holds until
+ * the process exits; the caller still passes inputs and outputs.  Allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Plans whose workspace_bytes exceed the array return
+ *     BIP_ERR_WORKSPACE_TOO_SMALL (a smaller split_budget_bytes makes a plan fit).
+ *   - Uses the current device; the stream and buffers must belong to it.  The
+ *     first call on a device looks up the array's device address with that
+ *     device current (it may load the module): make it before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents:
+ *     calls whose work overlaps on the GPU race, so order them (one stream, or
+ *     events).  Each call rewrites the status word at the head of the array
+ *     before its kernels run, so nothing needs clearing between calls.  The
+ *     array is private, so bip_read_device_status cannot read that word: a
+ *     bounded wait that expires still returns early and leaves out/lse undefined. */
+bip_status bip_prefill_no_alloc(bip_plan_t plan, const void* q, int64_t num_q_rows, const void* k_pages,
+                                const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                                const int32_t* kv_indices, float k_scale, float v_scale, void* out,
+                                float* lse, cudaStream_t stream);
+
 /* Synchronize `stream` and read the status word the last bip_prefill on this
  * workspace left: BIP_OK, BIP_ERR_DEVICE_TIMEOUT (a bounded wait expired; the
  * kernel returned early and its outputs are undefined) or
