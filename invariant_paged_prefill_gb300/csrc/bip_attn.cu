@@ -5,8 +5,9 @@
 // One CTA (one per SM) walks work items: a unit = (request, KV head, NT
 // consecutive absolute q tiles that share the same keys) over some of its
 // 4096-key segments.  Roles:
-//   warp 0          TMA producer: the unit's q tiles once, then K and V
-//                   blocks page by page through ST-deep rings.
+//   warp 0          TMA producer: the unit's q tiles once, then K blocks page
+//                   by page through an ST-deep ring.
+//   last warp       TMA producer of the V blocks (its own ST-deep ring).
 //   warp 1          tcgen05 issuer: S_t = Q_t K^T into TMEM, then
 //                   O_t += P_t V with P_t read from TMEM; zeroes V rows past
 //                   kv_len before they enter a product.
@@ -15,6 +16,7 @@
 //                   max and sum, writes P_t (bf16) over S_t in TMEM, rescales
 //                   O_t when needed, and at each segment end folds or writes
 //                   the segment.
+//   (FP8 pages)     a dequant warpgroup converts staged E4M3 blocks to bf16.
 // With two slots (head_dim 128) the softmax of one tile overlaps the MMAs of
 // the other.  Slots and ring depth only decide scheduling; every row's
 // arithmetic is the same in every variant.
@@ -47,6 +49,24 @@ namespace {
 // (log2 units): probabilities then stay below 2^8 and O is rescaled rarely.
 constexpr float kLazyRescale = 8.0f;
 
+// Packed fp32 pairs (one instruction for two round-to-nearest operations,
+// each lane exactly the scalar __fmaf_rn / __fadd_rn).
+__device__ __forceinline__ uint64_t f2_bits(float a, float b) {
+  return uint64_t(__float_as_uint(a)) | (uint64_t(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+
 template <int D, int NT, int ST, bool KV8 = false>
 struct Cfg {
   static constexpr int BN = kv_block_for(D);        // keys per block
@@ -68,7 +88,8 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_V8 + SS * KV8_BYTES;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
   static constexpr int DQ_WARP0 = 2 + 4 * NT;        // first dequant warp
-  static constexpr int THREADS = 64 + 128 * NT + (KV8 ? 128 : 0);
+  static constexpr int VP_WARP = DQ_WARP0 + (KV8 ? 4 : 0);  // V-stream producer warp
+  static constexpr int THREADS = 32 * (VP_WARP + 1);
   static constexpr int TM_COLS = 512;
   static constexpr int BPS = kSplitLen / BN;         // blocks per segment
   // TMEM columns: two slots use [0,256) and [256,512), each S (BN) then O (D);
@@ -111,9 +132,9 @@ __device__ __forceinline__ uint32_t bar(const Ctx& c, int i) { return c.bar0 + 8
 
 // Bounded wait on an mbarrier phase.  On expiry the CTA is marked aborted,
 // the workspace status records a timeout, and false is returned; any wait
-// that sees the abort mark also returns false.
-__device__ __noinline__ bool wait_phase(const Ctx& c, uint32_t b, uint32_t parity, uint32_t where) {
-  if (mbar_test(b, parity)) return true;
+// that sees the abort mark also returns false.  The first probe is inline;
+// only a miss calls the (out-of-line) polling loop.
+__device__ __noinline__ bool wait_phase_slow(Ctx c, uint32_t b, uint32_t parity, uint32_t where) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
@@ -126,6 +147,11 @@ __device__ __noinline__ bool wait_phase(const Ctx& c, uint32_t b, uint32_t parit
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_phase(const Ctx& c, uint32_t b, uint32_t parity, uint32_t where) {
+  if (mbar_test(b, parity)) return true;
+  return wait_phase_slow(c, b, parity, where);
 }
 
 // Same, with the result made uniform across the warp.
@@ -182,25 +208,33 @@ __device__ __forceinline__ void load_page_ids(const AttnParams& p, const WorkIte
   for (int i = 0; i < MAXP; ++i) ids[i] = (i < n) ? __ldg(p.kv_indices + w.page_base + p0 + i) : 0;
 }
 
+// One TMA stream: warp 0 loads the q tiles and K, the last warp loads V, so a
+// V slot still in use never holds back K loads (or the reverse).  (Two lanes
+// of one warp would serialise: a polling lane can suspend its whole warp.)  Each item's first ring-depth K blocks are issued before its q
+// tiles, whose load waits for the previous item's last S, so the ring keeps
+// streaming across item boundaries.
 template <int D, int NT, int ST, bool KV8>
-__device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, const CUtensorMap* tk,
-                         const CUtensorMap* tv, const AttnParams& p) {
+__device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, const CUtensorMap* tkv,
+                         const AttnParams& p, const bool is_v) {
   using C = Cfg<D, NT, ST, KV8>;
   constexpr int MAXP = C::BN / 8;  // pages per block at the smallest page size
-  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q;
   const int pages_per_blk = C::BN / p.page_size;
   const uint32_t q_slot_bytes = uint32_t(C::DCH * 128 * p.group * p.tile_pos);
+  // bf16: TMA fills the ring slot; FP8: TMA fills the staging ring, the
+  // dequant warps fill the slot.
+  constexpr int RING = KV8 ? C::SS : ST;
+  const int full0 = KV8 ? (is_v ? B_V8_FULL : B_K8_FULL) : (is_v ? B_V_FULL : B_K_FULL);
+  const int free0 = KV8 ? (is_v ? B_V8_FREE : B_K8_FREE) : (is_v ? B_V_FREE : B_K_FREE);
+  const uint32_t ring0 = sbase + (KV8 ? (is_v ? C::OFF_V8 : C::OFF_K8) : (is_v ? C::OFF_V : C::OFF_K));
+  const uint32_t ring_bytes = KV8 ? uint32_t(C::KV8_BYTES) : uint32_t(C::KV_BYTES);
   uint32_t b = 0;  // blocks started by this CTA
   int n = 0;       // items started by this CTA
-  uint32_t k_issued[ST] = {}, v_issued[ST] = {}, q_issued = 0u;  // loads per barrier
+  uint32_t issued[RING > 0 ? RING : 1] = {}, q_issued = 0u;  // loads per barrier
   bool ok = true;
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
-    const WorkItem w = p.items[it];
-    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
-    const int npages_req = (w.kv_len + p.page_size - 1) / p.page_size;
-    int ids[MAXP], nid;
-    load_page_ids<MAXP>(p, w, g.blk_lo, pages_per_blk, npages_req, ids, nid);
-    if (n > 0 && !wait_phase(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) break;
+
+  auto load_q = [&](const WorkItem& w, const Geom& g) -> bool {
+    if (n > 0 && !wait_phase(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) return false;
     mbar_arrive_expect_tx(bar(c, B_Q_FULL), q_slot_bytes * __popc(g.mask));
     ++q_issued;
 #pragma unroll
@@ -210,72 +244,60 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
         tma_load_3d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tq, bar(c, B_Q_FULL), ch * 64, w.kv_head * p.group,
                     w.q_tok0 + g.tile_start[t]);
     }
+    return true;
+  };
+
+  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+    const WorkItem w = p.items[it];
+    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
+    const int npages_req = (w.kv_len + p.page_size - 1) / p.page_size;
+    int ids[MAXP], nid;
+    load_page_ids<MAXP>(p, w, g.blk_lo, pages_per_blk, npages_req, ids, nid);
+    bool q_done = is_v;
     for (int blk = g.blk_lo; blk <= g.blk_hi; ++blk, ++b) {
-      const int slot = b % ST;
-      const uint32_t use = b / ST;
+      if (!q_done && blk - g.blk_lo == min(RING, g.blk_hi - g.blk_lo + 1)) {
+        if (!load_q(w, g)) { ok = false; break; }
+        q_done = true;
+      }
+      const int slot = b % RING;
+      const uint32_t use = b / RING;
       int cur[MAXP];
       const int ncur = nid;
 #pragma unroll
       for (int i = 0; i < MAXP; ++i) {
         int id = ids[i];
         if (i < ncur && (id < 0 || id >= p.num_pages)) {
-          atomicAdd(&c.header->bad_pages, 1u);
+          if (!is_v) atomicAdd(&c.header->bad_pages, 1u);
           id = 0;
         }
         cur[i] = id;
       }
       if (blk < g.blk_hi) load_page_ids<MAXP>(p, w, blk + 1, pages_per_blk, npages_req, ids, nid);  // next block
-      if constexpr (KV8) {
-        // raw E4M3 pages into the staging ring; the dequant warps fill the bf16 slots
-        const int ss = b % C::SS;
-        const uint32_t suse = b / C::SS;
-        const uint32_t bytes8 = uint32_t(ncur * p.page_size * D);
-        if (suse > 0 && !wait_phase(c, bar(c, B_K8_FREE + ss), (suse - 1) & 1, 4)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(c, B_K8_FULL + ss), bytes8);
-        ++k_issued[ss];
-        for (int i = 0; i < ncur; ++i)
-          tma_load_4d(sbase + C::OFF_K8 + ss * C::KV8_BYTES + i * p.page_size * D, tk, bar(c, B_K8_FULL + ss), 0,
-                      w.kv_head, 0, cur[i]);
-        if (suse > 0 && !wait_phase(c, bar(c, B_V8_FREE + ss), (suse - 1) & 1, 5)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(c, B_V8_FULL + ss), bytes8);
-        ++v_issued[ss];
-        for (int i = 0; i < ncur; ++i)
-          tma_load_4d(sbase + C::OFF_V8 + ss * C::KV8_BYTES + i * p.page_size * D, tv, bar(c, B_V8_FULL + ss), 0,
-                      w.kv_head, 0, cur[i]);
-        continue;
-      }
-      const uint32_t bytes = uint32_t(ncur * p.page_size * D * 2);
-      if (use > 0 && !wait_phase(c, bar(c, B_K_FREE + slot), (use - 1) & 1, 2)) { ok = false; break; }
-      mbar_arrive_expect_tx(bar(c, B_K_FULL + slot), bytes);
-      ++k_issued[slot];
+      if (use > 0 && !wait_phase(c, bar(c, free0 + slot), (use - 1) & 1, is_v ? 3 : 2)) { ok = false; break; }
+      const uint32_t page_bytes = uint32_t(p.page_size * D * (KV8 ? 1 : 2));
+      mbar_arrive_expect_tx(bar(c, full0 + slot), uint32_t(ncur) * page_bytes);
+      ++issued[slot];
 #pragma unroll
       for (int i = 0; i < MAXP; ++i) {
         if (i >= ncur) break;
-        for (int ch = 0; ch < C::DCH; ++ch)
-          tma_load_4d(sK + slot * C::KV_BYTES + ch * C::KV_CHUNK + i * p.page_size * 128, tk,
-                      bar(c, B_K_FULL + slot), ch * 64, w.kv_head, 0, cur[i]);
-      }
-      if (use > 0 && !wait_phase(c, bar(c, B_V_FREE + slot), (use - 1) & 1, 3)) { ok = false; break; }
-      mbar_arrive_expect_tx(bar(c, B_V_FULL + slot), bytes);
-      ++v_issued[slot];
-#pragma unroll
-      for (int i = 0; i < MAXP; ++i) {
-        if (i >= ncur) break;
-        for (int ch = 0; ch < C::DCH; ++ch)
-          tma_load_4d(sV + slot * C::KV_BYTES + ch * C::KV_CHUNK + i * p.page_size * 128, tv,
-                      bar(c, B_V_FULL + slot), ch * 64, w.kv_head, 0, cur[i]);
+        if constexpr (KV8) {
+          tma_load_4d(ring0 + slot * ring_bytes + i * page_bytes, tkv, bar(c, full0 + slot), 0, w.kv_head, 0,
+                      cur[i]);
+        } else {
+          for (int ch = 0; ch < C::DCH; ++ch)
+            tma_load_4d(ring0 + slot * ring_bytes + ch * C::KV_CHUNK + i * p.page_size * 128, tkv,
+                        bar(c, full0 + slot), ch * 64, w.kv_head, 0, cur[i]);
+        }
       }
     }
+    if (ok && !q_done && !load_q(w, g)) ok = false;  // items shorter than the ring
   }
   // Drain: the last load on every barrier must have landed before exit
   // (on the normal path these phases completed long ago).
   if (q_issued) drain_wait(bar(c, B_Q_FULL), (q_issued - 1) & 1);
 #pragma unroll
-  for (int slot = 0; slot < ST; ++slot) {
-    const int kf = KV8 ? B_K8_FULL : B_K_FULL, vf = KV8 ? B_V8_FULL : B_V_FULL;
-    if (k_issued[slot]) drain_wait(bar(c, kf + slot), (k_issued[slot] - 1) & 1);
-    if (v_issued[slot]) drain_wait(bar(c, vf + slot), (v_issued[slot] - 1) & 1);
-  }
+  for (int slot = 0; slot < RING; ++slot)
+    if (issued[slot]) drain_wait(bar(c, full0 + slot), (issued[slot] - 1) & 1);
 }
 
 template <int D, int NT, int ST, bool KV8>
@@ -305,12 +327,16 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
       const int sbuf = s_cnt[t] % C::NS;
       if (lane == 0) {
         const uint32_t d_tmem = tmem + C::tm_s(t, sbuf);
-#pragma unroll
+        // K step k: 32 bytes along a 128-byte row, 64 columns per chunk.  The
+        // start address sits in the descriptor's low bits (16-byte units), so
+        // a step is an add; a rolled loop keeps this issue path small.
+        const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sK + kslot * C::KV_BYTES, 16, 1024);
+#pragma unroll 1
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off_q = t * C::Q_BYTES + (k >> 2) * C::Q_CHUNK + (k & 3) * 32;
-          const uint32_t off_k = kslot * C::KV_BYTES + (k >> 2) * C::KV_CHUNK + (k & 3) * 32;
-          tc_mma_ss(d_tmem, sdesc_sw128(sQ + off_q, 16, 1024), sdesc_sw128(sK + off_k, 16, 1024), kIdescS,
-                    k > 0 ? 1u : 0u);
+          const uint32_t cq = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
+          const uint32_t ck = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
+          tc_mma_ss(d_tmem, dq + cq, dk + ck, kIdescS, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(c, B_S_FULL + 2 * t + sbuf));
         if (t == g.last_slot) {
@@ -362,12 +388,11 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
         tc_fence_after();
         if (lane == 0) {
           const uint32_t p_tmem = tmem + C::tm_s(t, pbuf);  // P_t (bf16) over its S buffer
-#pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k) {
-            const uint32_t off_v = vslot * C::KV_BYTES + k * 16 * 128;
-            tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, sdesc_sw128(sV + off_v, C::KV_CHUNK, 1024), kIdescO,
+          const uint64_t dv = sdesc_sw128(sV + vslot * C::KV_BYTES, C::KV_CHUNK, 1024);
+#pragma unroll 1
+          for (int k = 0; k < C::BN / 16; ++k)  // K step k: 16 V rows (2048 bytes), 8 TMEM columns of P
+            tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, dv + uint32_t(k * 128), kIdescO,
                       (k > 0 || !first_in_seg) ? 1u : 0u);
-          }
           tc_commit(bar(c, B_O_DONE + 2 * t + pbuf));
         }
         __syncwarp();
@@ -442,20 +467,29 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         const bool whole = __all_sync(0xffffffffu, lim >= C::BN - 1);
         const bool live = __any_sync(0xffffffffu, lim >= 0);
 
-        // pass 1: block max over the visible columns
+        // Block max.  One TMEM round trip for the whole S row; variants with
+        // more than 256 threads (168 registers a thread) then reread S in two
+        // halves for the exponentials instead of keeping the row in registers.
+        constexpr bool kHalves = C::THREADS > 256 && C::BN == 128;
+        constexpr int HW = kHalves ? C::BN / 2 : C::BN;  // columns per exp pass
         float mx = -INFINITY;
+        uint32_t sv[C::BN];
+        if (live) {
+          if constexpr (C::BN == 128) tmem_ld_x128(sa, sv);
+          else tmem_ld_x64(sa, sv);
+          // eight independent partial maxima (max is exact in any order)
+          float m8[8];
 #pragma unroll
-        for (int c0 = 0; c0 < (live ? C::BN : 0); c0 += 32) {
-          uint32_t v[32];
-          tmem_ld_x32(sa + c0, v);
+          for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
           if (whole) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+            for (int j = 0; j < C::BN; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c0 + j <= lim) mx = fmaxf(mx, __uint_as_float(v[j]));
+            for (int j = 0; j < C::BN; ++j)
+              if (j <= lim) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
           }
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
         float alpha = 1.f;
         if (mx != -INFINITY) {
@@ -471,36 +505,67 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         }
         const float ms = (m == -INFINITY) ? 0.f : __fmul_rn(m, scale);
 
-        // pass 2: probabilities, the row sum in ascending column order, and
-        // P (bf16 pairs) written over the S columns already read.  Column
-        // j = 3 (mod 4) takes 2^x on the FMA pipe, the others on MUFU.
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (!live) {
-          const uint32_t zero[16] = {};
+        // Probabilities, the row sum in ascending column order, and P (bf16
+        // pairs, packed in place) written back over the S columns already
+        // read.  Column j = 7 (mod 8) takes 2^x on the FMA pipe, the others
+        // on MUFU.
+        // Row-sum partials: acc01 holds columns 0, 1 (mod 4), acc23 columns
+        // 2, 3 (mod 4), each pair summed with one packed add.
+        uint64_t acc01 = 0ull, acc23 = 0ull;
+        const uint64_t sc2 = f2_bits(scale, scale), nm2 = f2_bits(-ms, -ms);
 #pragma unroll
-          for (int c0 = 0; c0 < C::BN; c0 += 32) tmem_st_x16(sa + c0 / 2, zero);
-        }
+        for (int h = 0; h < C::BN / HW; ++h) {
+          uint32_t* hv = kHalves ? sv : sv + h * HW;
+          if (live) {
+            if constexpr (kHalves) tmem_ld_x64(sa + h * HW, *reinterpret_cast<uint32_t(*)[64]>(hv));
+            if (whole) {
 #pragma unroll
-        for (int c0 = 0; c0 < (live ? C::BN : 0); c0 += 32) {
-          uint32_t v[32], pk[16];
-          tmem_ld_x32(sa + c0, v);
-          float pr[32];
+              for (int j = 0; j < HW; j += 4) {
+                const int col = h * HW + j;
+                const uint64_t x01 = ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
+                const uint64_t x23 =
+                    ffma2(f2_bits(__uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3])), sc2, nm2);
+                const float e0 = ex2(f2_lo(x01)), e1 = ex2(f2_hi(x01)), e2 = ex2(f2_lo(x23));
+                const float e3 = ((col + 3) & 7) == 7 ? ex2_fma(f2_hi(x23)) : ex2(f2_hi(x23));
+                acc01 = fadd2(acc01, f2_bits(e0, e1));
+                acc23 = fadd2(acc23, f2_bits(e2, e3));
+                hv[j] = __float_as_uint(e0);
+                hv[j + 1] = __float_as_uint(e1);
+                hv[j + 2] = __float_as_uint(e2);
+                hv[j + 3] = __float_as_uint(e3);
+              }
+            } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = __fmaf_rn(__uint_as_float(v[j]), scale, -ms);
-            const float e = (j & 3) == 3 ? ex2_fma(x) : ex2(x);
-            pr[j] = (whole || c0 + j <= lim) ? e : 0.f;
+              for (int j = 0; j < HW; j += 4) {
+                const int col = h * HW + j;
+                const uint64_t x01 = ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
+                const uint64_t x23 =
+                    ffma2(f2_bits(__uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3])), sc2, nm2);
+                const float e0 = col <= lim ? ex2(f2_lo(x01)) : 0.f;
+                const float e1 = col + 1 <= lim ? ex2(f2_hi(x01)) : 0.f;
+                const float e2 = col + 2 <= lim ? ex2(f2_lo(x23)) : 0.f;
+                const float e3 = col + 3 <= lim ? (((col + 3) & 7) == 7 ? ex2_fma(f2_hi(x23)) : ex2(f2_hi(x23))) : 0.f;
+                acc01 = fadd2(acc01, f2_bits(e0, e1));
+                acc23 = fadd2(acc23, f2_bits(e2, e3));
+                hv[j] = __float_as_uint(e0);
+                hv[j + 1] = __float_as_uint(e1);
+                hv[j + 2] = __float_as_uint(e2);
+                hv[j + 3] = __float_as_uint(e3);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < HW / 2; ++k)
+              hv[k] = pack_bf16x2(__uint_as_float(hv[2 * k]), __uint_as_float(hv[2 * k + 1]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < HW / 2; ++k) hv[k] = 0u;
           }
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            acc[j & 3] = __fadd_rn(acc[j & 3], pr[j]);
-            acc[(j + 1) & 3] = __fadd_rn(acc[(j + 1) & 3], pr[j + 1]);
-            pk[j >> 1] = pack_bf16x2(pr[j], pr[j + 1]);
-          }
-          tmem_st_x16(sa + c0 / 2, pk);
+          if constexpr (HW == 128) tmem_st_x64(sa, hv);
+          else tmem_st_x32_p(sa + h * (HW / 2), hv);
         }
         if (valid) {
-          const float rowsum = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+          const float rowsum =
+              __fadd_rn(__fadd_rn(f2_lo(acc01), f2_hi(acc01)), __fadd_rn(f2_lo(acc23), f2_hi(acc23)));
           l = __fadd_rn(__fmul_rn(l, alpha), rowsum);
         }
         // Rescale O where the running max moved (alpha is exactly 1 elsewhere);
@@ -715,19 +780,22 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
+  const int lane = threadIdx.x & 31;
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) {
+    if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, &tm_v, p);
+      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, p, false);
     }
   } else if (warp == 1) {
     mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
   } else if (warp < C::DQ_WARP0) {
     softmax_role<D, NT, ST, KV8>(c, tmem, p, (warp - 2) / 4);
-  } else {
+  } else if (warp < C::VP_WARP) {
     dequant_role<D, NT, ST, KV8>(c, sbase, p);
+  } else if (lane == 0) {
+    prefetch_tmap(&tm_v);
+    producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_v, p, true);
   }
 
   tc_fence_before();

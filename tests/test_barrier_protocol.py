@@ -1,6 +1,7 @@
 """Model check of the attention kernel's mbarrier schedule (CPU, no GPU).
 
-The kernel's roles (TMA producer, optional FP8 dequant warpgroup, tcgen05
+The kernel's roles (two TMA streams -- q tiles and K, and V --, optional FP8
+dequant warpgroup, tcgen05
 issuer, one softmax warpgroup per q-tile slot of 4 warps) synchronise through
 mbarriers waited on by phase parity.  This test replays that schedule -- the
 same waits, arrivals and commits, in the same order per role as
@@ -68,27 +69,32 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
     def wait(name, idx):
         return ("wait", name, idx)
 
-    def producer():
+    def producer(is_v):
+        """Lane 0 streams the q tiles and K, lane 1 streams V; an item's first
+        ring-depth K blocks go out before its q tiles."""
+        ring = SS if SS else ST
+        kv = ("V8" if SS else "V") if is_v else ("K8" if SS else "K")
         b = 0
         for n, (nb, mask) in enumerate(items):
-            if n > 0:
-                yield wait("Q_FREE", n - 1)
-            later("Q_FULL")
-            for _ in range(nb):
-                if SS:
-                    ss, use = b % SS, b // SS
-                    for kv in ("K8", "V8"):
-                        if use > 0:
-                            yield wait(f"{kv}_FREE{ss}", use - 1)
-                        later(f"{kv}_FULL{ss}")
-                else:
-                    slot, use = b % ST, b // ST
-                    for kv in ("K", "V"):
-                        if use > 0:
-                            yield wait(f"{kv}_FREE{slot}", use - 1)
-                        later(f"{kv}_FULL{slot}")
+            q_done = is_v
+
+            def load_q():
+                if n > 0:
+                    yield wait("Q_FREE", n - 1)
+                later("Q_FULL")
+
+            for j in range(nb):
+                if not q_done and j == min(ring, nb):
+                    yield from load_q()
+                    q_done = True
+                slot, use = b % ring, b // ring
+                if use > 0:
+                    yield wait(f"{kv}_FREE{slot}", use - 1)
+                later(f"{kv}_FULL{slot}")
                 b += 1
                 yield None
+            if not q_done:
+                yield from load_q()
 
     def dequant():
         b = 0
@@ -165,7 +171,7 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
                 yield None
             yield from wait_pv(cnt - 1)                            # segment end: read O
 
-    roles = [("producer", producer()), ("issuer", issuer())]
+    roles = [("producer_k", producer(False)), ("producer_v", producer(True)), ("issuer", issuer())]
     roles += [(f"softmax{t}.{w}", softmax(t)) for t in range(NT) for w in range(warps)]
     if SS:
         roles.append(("dequant", dequant()))
