@@ -77,7 +77,9 @@ typedef struct bip_plan_options {
   bip_split_policy split_policy; /* default BIP_SPLIT_AUTO */
   size_t split_budget_bytes;     /* cap on partial-state bytes; default 256 MiB */
   int32_t num_sms;               /* CTAs to fill; 0 = query the current device */
-  uint64_t wait_limit_ns;        /* bound on every in-kernel wait; 0 = 4 s */
+  uint64_t wait_limit_ns;        /* bound on every in-kernel wait; 0 = 4 s.  Counted in SM clock
+                                    cycles at the device's peak clock, so at lower clocks a wait
+                                    runs proportionally longer before it gives up */
   int32_t tiles_per_unit;        /* q tiles per CTA: 0 = auto, 1, or 2 (head_dim 128 only);
                                     numerically neutral (tested) */
 } bip_plan_options;

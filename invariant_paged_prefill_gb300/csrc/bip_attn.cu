@@ -38,6 +38,8 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "bip_internal.h"
 #include "bip_numerics.cuh"
 #include "bip_ptx.cuh"
@@ -49,23 +51,11 @@ namespace {
 // (log2 units): probabilities then stay below 2^8 and O is rescaled rarely.
 constexpr float kLazyRescale = 8.0f;
 
-// Packed fp32 pairs (one instruction for two round-to-nearest operations,
-// each lane exactly the scalar __fmaf_rn / __fadd_rn).
-__device__ __forceinline__ uint64_t f2_bits(float a, float b) {
-  return uint64_t(__float_as_uint(a)) | (uint64_t(__float_as_uint(b)) << 32);
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
-__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+// Column pairs (mod 8) whose exponentials run on the FMA pipe instead of
+// MUFU.  Measured on GB300: every pair moved to the polynomial made the
+// softmax slower (the exp pass is latency- and register-bound, not MUFU
+// throughput-bound), so none is.
+constexpr uint32_t kFmaPairs = 0x00;
 
 template <int D, int NT, int ST, bool KV8 = false>
 struct Cfg {
@@ -87,9 +77,27 @@ struct Cfg {
   static constexpr int OFF_V8 = OFF_K8 + SS * KV8_BYTES;
   static constexpr int OFF_BAR = OFF_V8 + SS * KV8_BYTES;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
-  static constexpr int DQ_WARP0 = 2 + 4 * NT;        // first dequant warp
-  static constexpr int VP_WARP = DQ_WARP0 + (KV8 ? 4 : 0);  // V-stream producer warp
-  static constexpr int THREADS = 32 * (VP_WARP + 1);
+  // Warp roles, whole warpgroups each: softmax warps 0 .. 4 NT - 1 (slot
+  // t = warp / 4, TMEM lane quarter = warp % 4), then the FP8 dequant
+  // warpgroup, then the control warpgroup: q/K producer, MMA issuer, V
+  // producer and one spare warp.
+  static constexpr int SM_WARPS = 4 * NT;
+  static constexpr int DQ_WARP0 = SM_WARPS;
+  static constexpr int CTL_WARP0 = SM_WARPS + (KV8 ? 4 : 0);
+  static constexpr int THREADS = 32 * (CTL_WARP0 + 4);
+  // Register split: launches of more than 256 threads start at LAUNCH_REGS
+  // a thread; the control warpgroup then gives registers back (setmaxnreg)
+  // and the softmax warpgroups take them.  The dequant warpgroup keeps its
+  // launch count.  The sum never exceeds what the launch holds.
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;
+  static constexpr bool SPLIT_REGS = THREADS > 256;
+  static constexpr int CTL_REGS = 56;
+  static constexpr int SM_REGS_FREE =
+      ((LAUNCH_REGS * THREADS - CTL_REGS * 128 - (KV8 ? LAUNCH_REGS * 128 : 0)) / (32 * SM_WARPS)) & ~7;
+  static constexpr int SM_REGS = SPLIT_REGS ? (SM_REGS_FREE < 240 ? SM_REGS_FREE : 240) : 255;
+  static_assert(!SPLIT_REGS || SM_REGS * 32 * SM_WARPS + CTL_REGS * 128 + (KV8 ? LAUNCH_REGS * 128 : 0) <=
+                                   LAUNCH_REGS * THREADS, "register split exceeds the launch's registers");
+  static_assert(!SPLIT_REGS || SM_REGS >= LAUNCH_REGS, "softmax warps must not lose registers");
   static constexpr int TM_COLS = 512;
   static constexpr int BPS = kSplitLen / BN;         // blocks per segment
   // TMEM columns: two slots use [0,256) and [256,512), each S (BN) then O (D);
@@ -125,33 +133,31 @@ struct Ctx {
   uint32_t bar0;
   volatile uint32_t* abort;
   WsHeader* header;
-  uint64_t limit_ns;
+  uint64_t limit_cycles;
 };
 
 __device__ __forceinline__ uint32_t bar(const Ctx& c, int i) { return c.bar0 + 8u * i; }
 
 // Bounded wait on an mbarrier phase.  On expiry the CTA is marked aborted,
 // the workspace status records a timeout, and false is returned; any wait
-// that sees the abort mark also returns false.  The first probe is inline;
-// only a miss calls the (out-of-line) polling loop.
-__device__ __noinline__ bool wait_phase_slow(Ctx c, uint32_t b, uint32_t parity, uint32_t where) {
-  const uint64_t t0 = globaltimer_ns();
+// that sees the abort mark also returns false.  The first probe answers at
+// once; after it the clock is checked before every (suspending) probe, so a
+// wait that is not already complete always meets the limit check.  (Inlined:
+// an out-of-line call cannot be shared by warpgroups running with different
+// register budgets.)
+__device__ __forceinline__ bool wait_phase(const Ctx& c, uint32_t b, uint32_t parity, uint32_t where) {
+  const uint64_t t0 = clock64();
+  if (mbar_ready(b, parity)) return true;
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_test(b, parity)) return true;
-    if (*c.abort) return false;
-    if (globaltimer_ns() - t0 > c.limit_ns) {
+    if (uint64_t(clock64()) - t0 > c.limit_cycles) {
       *c.abort = 1u;
       atomicCAS(&c.header->status, 0u, 5u /* BIP_ERR_DEVICE_TIMEOUT */);
       atomicExch(&c.header->where, where);
       return false;
     }
+    if (mbar_test(b, parity)) return true;
+    if (*c.abort) return false;
   }
-}
-
-__device__ __forceinline__ bool wait_phase(const Ctx& c, uint32_t b, uint32_t parity, uint32_t where) {
-  if (mbar_test(b, parity)) return true;
-  return wait_phase_slow(c, b, parity, where);
 }
 
 // Same, with the result made uniform across the warp.
@@ -198,26 +204,29 @@ __device__ __forceinline__ Geom geom_of(const WorkItem& w, int T) {
 
 // ------------------------------------------------------------------ roles
 
-// Page ids of one KV block, range-checked (bad ids are counted and read as 0).
-template <int MAXP>
-__device__ __forceinline__ void load_page_ids(const AttnParams& p, const WorkItem& w, int blk, int pages_per_blk,
-                                              int npages_req, int (&ids)[MAXP], int& n) {
+// Page id of page `lane` of KV block `blk` (0 for lanes past the block's
+// pages), and the block's page count.  Pages per block <= 16 <= warp size.
+__device__ __forceinline__ int lane_page_id(const AttnParams& p, const WorkItem& w, int blk, int pages_per_blk,
+                                            int npages_req, int lane, int& n) {
   const int p0 = blk * pages_per_blk;
   n = min(p0 + pages_per_blk, npages_req) - p0;
-#pragma unroll
-  for (int i = 0; i < MAXP; ++i) ids[i] = (i < n) ? __ldg(p.kv_indices + w.page_base + p0 + i) : 0;
+  return lane < n ? __ldg(p.kv_indices + w.page_base + p0 + lane) : 0;
 }
 
-// One TMA stream: warp 0 loads the q tiles and K, the last warp loads V, so a
-// V slot still in use never holds back K loads (or the reverse).  (Two lanes
-// of one warp would serialise: a polling lane can suspend its whole warp.)  Each item's first ring-depth K blocks are issued before its q
-// tiles, whose load waits for the previous item's last S, so the ring keeps
-// streaming across item boundaries.
+// One TMA stream, run by a whole warp: the control warpgroup's first warp
+// loads the q tiles and K, its third warp loads V, so a V slot still in use
+// never holds back K loads (or the reverse).  Lane i holds the page id of
+// page i of the next block (fetched one block ahead) and issues that page's
+// loads; lane 0 posts the expected bytes first.  Each item's first
+// ring-depth K blocks are issued before its q tiles, whose load waits for
+// the previous item's last S, so the ring keeps streaming across item
+// boundaries.
 template <int D, int NT, int ST, bool KV8>
 __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, const CUtensorMap* tkv,
                          const AttnParams& p, const bool is_v) {
   using C = Cfg<D, NT, ST, KV8>;
-  constexpr int MAXP = C::BN / 8;  // pages per block at the smallest page size
+  static_assert(C::BN / 8 <= 32, "one lane per page");
+  const int lane = threadIdx.x & 31;
   const uint32_t sQ = sbase + C::OFF_Q;
   const int pages_per_blk = C::BN / p.page_size;
   const uint32_t q_slot_bytes = uint32_t(C::DCH * 128 * p.group * p.tile_pos);
@@ -228,22 +237,24 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
   const int free0 = KV8 ? (is_v ? B_V8_FREE : B_K8_FREE) : (is_v ? B_V_FREE : B_K_FREE);
   const uint32_t ring0 = sbase + (KV8 ? (is_v ? C::OFF_V8 : C::OFF_K8) : (is_v ? C::OFF_V : C::OFF_K));
   const uint32_t ring_bytes = KV8 ? uint32_t(C::KV8_BYTES) : uint32_t(C::KV_BYTES);
+  const uint32_t page_bytes = uint32_t(p.page_size * D * (KV8 ? 1 : 2));
   uint32_t b = 0;  // blocks started by this CTA
   int n = 0;       // items started by this CTA
-  uint32_t issued[RING > 0 ? RING : 1] = {}, q_issued = 0u;  // loads per barrier
   bool ok = true;
 
   auto load_q = [&](const WorkItem& w, const Geom& g) -> bool {
-    if (n > 0 && !wait_phase(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) return false;
-    mbar_arrive_expect_tx(bar(c, B_Q_FULL), q_slot_bytes * __popc(g.mask));
-    ++q_issued;
+    if (n > 0 && !wait_warp(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) return false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(c, B_Q_FULL), q_slot_bytes * __popc(g.mask));
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      if (!(g.mask >> t & 1)) continue;
-      for (int ch = 0; ch < C::DCH; ++ch)
-        tma_load_3d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tq, bar(c, B_Q_FULL), ch * 64, w.kv_head * p.group,
-                    w.q_tok0 + g.tile_start[t]);
+      for (int t = 0; t < NT; ++t) {
+        if (!(g.mask >> t & 1)) continue;
+        for (int ch = 0; ch < C::DCH; ++ch)
+          tma_load_3d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tq, bar(c, B_Q_FULL), ch * 64, w.kv_head * p.group,
+                      w.q_tok0 + g.tile_start[t]);
+      }
     }
+    __syncwarp();
     return true;
   };
 
@@ -251,8 +262,8 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int npages_req = (w.kv_len + p.page_size - 1) / p.page_size;
-    int ids[MAXP], nid;
-    load_page_ids<MAXP>(p, w, g.blk_lo, pages_per_blk, npages_req, ids, nid);
+    int nid;
+    int id_next = lane_page_id(p, w, g.blk_lo, pages_per_blk, npages_req, lane, nid);
     bool q_done = is_v;
     for (int blk = g.blk_lo; blk <= g.blk_hi; ++blk, ++b) {
       if (!q_done && blk - g.blk_lo == min(RING, g.blk_hi - g.blk_lo + 1)) {
@@ -261,43 +272,41 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
       }
       const int slot = b % RING;
       const uint32_t use = b / RING;
-      int cur[MAXP];
       const int ncur = nid;
-#pragma unroll
-      for (int i = 0; i < MAXP; ++i) {
-        int id = ids[i];
-        if (i < ncur && (id < 0 || id >= p.num_pages)) {
-          if (!is_v) atomicAdd(&c.header->bad_pages, 1u);
-          id = 0;
-        }
-        cur[i] = id;
+      int id = id_next;
+      if (lane < ncur && (id < 0 || id >= p.num_pages)) {  // counted once, by the K stream
+        if (!is_v) atomicAdd(&c.header->bad_pages, 1u);
+        id = 0;
       }
-      if (blk < g.blk_hi) load_page_ids<MAXP>(p, w, blk + 1, pages_per_blk, npages_req, ids, nid);  // next block
-      if (use > 0 && !wait_phase(c, bar(c, free0 + slot), (use - 1) & 1, is_v ? 3 : 2)) { ok = false; break; }
-      const uint32_t page_bytes = uint32_t(p.page_size * D * (KV8 ? 1 : 2));
-      mbar_arrive_expect_tx(bar(c, full0 + slot), uint32_t(ncur) * page_bytes);
-      ++issued[slot];
-#pragma unroll
-      for (int i = 0; i < MAXP; ++i) {
-        if (i >= ncur) break;
+      if (blk < g.blk_hi) id_next = lane_page_id(p, w, blk + 1, pages_per_blk, npages_req, lane, nid);
+      if (use > 0 && !wait_warp(c, bar(c, free0 + slot), (use - 1) & 1, is_v ? 3 : 2)) { ok = false; break; }
+      if (lane == 0) mbar_arrive_expect_tx(bar(c, full0 + slot), uint32_t(ncur) * page_bytes);
+      __syncwarp();
+      if (lane < ncur) {
         if constexpr (KV8) {
-          tma_load_4d(ring0 + slot * ring_bytes + i * page_bytes, tkv, bar(c, full0 + slot), 0, w.kv_head, 0,
-                      cur[i]);
+          tma_load_4d(ring0 + slot * ring_bytes + lane * page_bytes, tkv, bar(c, full0 + slot), 0, w.kv_head, 0,
+                      id);
         } else {
           for (int ch = 0; ch < C::DCH; ++ch)
-            tma_load_4d(ring0 + slot * ring_bytes + ch * C::KV_CHUNK + i * p.page_size * 128, tkv,
-                        bar(c, full0 + slot), ch * 64, w.kv_head, 0, cur[i]);
+            tma_load_4d(ring0 + slot * ring_bytes + ch * C::KV_CHUNK + lane * p.page_size * 128, tkv,
+                        bar(c, full0 + slot), ch * 64, w.kv_head, 0, id);
         }
       }
     }
     if (ok && !q_done && !load_q(w, g)) ok = false;  // items shorter than the ring
   }
-  // Drain: the last load on every barrier must have landed before exit
-  // (on the normal path these phases completed long ago).
-  if (q_issued) drain_wait(bar(c, B_Q_FULL), (q_issued - 1) & 1);
+  // Drain: the last load on every barrier must have landed before exit (on
+  // the normal path these phases completed long ago).  Phases issued: one
+  // per item for Q (K stream only), and blocks started / RING per slot.
+  if (lane == 0) {
+    if (!is_v && n > 0) drain_wait(bar(c, B_Q_FULL), (n - 1) & 1);
 #pragma unroll
-  for (int slot = 0; slot < RING; ++slot)
-    if (issued[slot]) drain_wait(bar(c, full0 + slot), (issued[slot] - 1) & 1);
+    for (int slot = 0; slot < RING; ++slot) {
+      const uint32_t issued = b / RING + (uint32_t(slot) < b % RING ? 1u : 0u);
+      if (issued) drain_wait(bar(c, full0 + slot), (issued - 1) & 1);
+    }
+  }
+  __syncwarp();
 }
 
 template <int D, int NT, int ST, bool KV8>
@@ -467,29 +476,36 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         const bool whole = __all_sync(0xffffffffu, lim >= C::BN - 1);
         const bool live = __any_sync(0xffffffffu, lim >= 0);
 
-        // Block max.  One TMEM round trip for the whole S row; variants with
-        // more than 256 threads (168 registers a thread) then reread S in two
-        // halves for the exponentials instead of keeping the row in registers.
-        constexpr bool kHalves = C::THREADS > 256 && C::BN == 128;
+        // Block max.  One TMEM round trip for the whole S row; with fewer than
+        // 248 registers a thread S is then reread in two halves for the
+        // exponentials instead of keeping the row live (which would spill).
+        constexpr bool kHalves = C::SM_REGS < 248 && C::BN == 128;
         constexpr int HW = kHalves ? C::BN / 2 : C::BN;  // columns per exp pass
         float mx = -INFINITY;
         uint32_t sv[C::BN];
-        if (live) {
-          if constexpr (C::BN == 128) tmem_ld_x128(sa, sv);
-          else tmem_ld_x64(sa, sv);
-          // eight independent partial maxima (max is exact in any order)
+        // eight independent partial maxima over column pairs (max is exact in
+        // any order); masked columns enter as -inf.  Whole blocks and masked
+        // blocks get separately compiled loops.
+        auto block_max = [&](auto whole_c) {
+          constexpr bool kWhole = decltype(whole_c)::value;
           float m8[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-          if (whole) {
 #pragma unroll
-            for (int j = 0; j < C::BN; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < C::BN; ++j)
-              if (j <= lim) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
+          for (int j = 0; j < C::BN; j += 2) {
+            float a = __uint_as_float(sv[j]), b = __uint_as_float(sv[j + 1]);
+            if (!kWhole) {
+              a = j <= lim ? a : -INFINITY;
+              b = j + 1 <= lim ? b : -INFINITY;
+            }
+            m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], a, b);
           }
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        };
+        if (live) {
+          if constexpr (C::BN == 128) tmem_ld_x128(sa, sv);
+          else tmem_ld_x64(sa, sv);
+          mx = whole ? block_max(std::true_type{}) : block_max(std::false_type{});
         }
         float alpha = 1.f;
         if (mx != -INFINITY) {
@@ -505,57 +521,46 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         }
         const float ms = (m == -INFINITY) ? 0.f : __fmul_rn(m, scale);
 
-        // Probabilities, the row sum in ascending column order, and P (bf16
-        // pairs, packed in place) written back over the S columns already
-        // read.  Column j = 7 (mod 8) takes 2^x on the FMA pipe, the others
-        // on MUFU.
+        // Probabilities, the row sum and P (bf16 pairs, packed in place)
+        // written back over the S columns already read.  Column pairs (2i,
+        // 2i+1) whose bit i (mod 8) is set in kFmaPairs take 2^x on the FMA
+        // pipe, the rest on MUFU; the choice depends only on the key's
+        // absolute position (blocks start at multiples of 16).  Masked columns
+        // are computed and then replaced by exact zeros, so a row gets the
+        // same bits through the whole-block and the masked path.
         // Row-sum partials: acc01 holds columns 0, 1 (mod 4), acc23 columns
         // 2, 3 (mod 4), each pair summed with one packed add.
         uint64_t acc01 = 0ull, acc23 = 0ull;
-        const uint64_t sc2 = f2_bits(scale, scale), nm2 = f2_bits(-ms, -ms);
+        const uint64_t sc2 = f2_splat(scale), nm2 = f2_splat(-ms);
 #pragma unroll
         for (int h = 0; h < C::BN / HW; ++h) {
           uint32_t* hv = kHalves ? sv : sv + h * HW;
           if (live) {
             if constexpr (kHalves) tmem_ld_x64(sa + h * HW, *reinterpret_cast<uint32_t(*)[64]>(hv));
-            if (whole) {
+            auto exp_pass = [&](auto whole_c) {
+              constexpr bool kWhole = decltype(whole_c)::value;
 #pragma unroll
               for (int j = 0; j < HW; j += 4) {
                 const int col = h * HW + j;
-                const uint64_t x01 = ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
-                const uint64_t x23 =
-                    ffma2(f2_bits(__uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3])), sc2, nm2);
-                const float e0 = ex2(f2_lo(x01)), e1 = ex2(f2_hi(x01)), e2 = ex2(f2_lo(x23));
-                const float e3 = ((col + 3) & 7) == 7 ? ex2_fma(f2_hi(x23)) : ex2(f2_hi(x23));
-                acc01 = fadd2(acc01, f2_bits(e0, e1));
-                acc23 = fadd2(acc23, f2_bits(e2, e3));
-                hv[j] = __float_as_uint(e0);
-                hv[j + 1] = __float_as_uint(e1);
-                hv[j + 2] = __float_as_uint(e2);
-                hv[j + 3] = __float_as_uint(e3);
-              }
-            } else {
+                uint64_t e[2];
 #pragma unroll
-              for (int j = 0; j < HW; j += 4) {
-                const int col = h * HW + j;
-                const uint64_t x01 = ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
-                const uint64_t x23 =
-                    ffma2(f2_bits(__uint_as_float(hv[j + 2]), __uint_as_float(hv[j + 3])), sc2, nm2);
-                const float e0 = col <= lim ? ex2(f2_lo(x01)) : 0.f;
-                const float e1 = col + 1 <= lim ? ex2(f2_hi(x01)) : 0.f;
-                const float e2 = col + 2 <= lim ? ex2(f2_lo(x23)) : 0.f;
-                const float e3 = col + 3 <= lim ? (((col + 3) & 7) == 7 ? ex2_fma(f2_hi(x23)) : ex2(f2_hi(x23))) : 0.f;
-                acc01 = fadd2(acc01, f2_bits(e0, e1));
-                acc23 = fadd2(acc23, f2_bits(e2, e3));
-                hv[j] = __float_as_uint(e0);
-                hv[j + 1] = __float_as_uint(e1);
-                hv[j + 2] = __float_as_uint(e2);
-                hv[j + 3] = __float_as_uint(e3);
+                for (int u = 0; u < 2; ++u) {
+                  const int cu = col + 2 * u;
+                  const uint64_t x = ffma2(
+                      f2_bits(__uint_as_float(hv[j + 2 * u]), __uint_as_float(hv[j + 2 * u + 1])), sc2, nm2);
+                  const int pair = (cu >> 1) & 7;
+                  if (kFmaPairs >> pair & 1) e[u] = ex2_fma2(x);
+                  else e[u] = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
+                  if (!kWhole) e[u] = f2_bits(cu <= lim ? f2_lo(e[u]) : 0.f, cu + 1 <= lim ? f2_hi(e[u]) : 0.f);
+                }
+                acc01 = fadd2(acc01, e[0]);
+                acc23 = fadd2(acc23, e[1]);
+                hv[j / 2] = pack_bf16x2(f2_lo(e[0]), f2_hi(e[0]));
+                hv[j / 2 + 1] = pack_bf16x2(f2_lo(e[1]), f2_hi(e[1]));
               }
-            }
-#pragma unroll
-            for (int k = 0; k < HW / 2; ++k)
-              hv[k] = pack_bf16x2(__uint_as_float(hv[2 * k]), __uint_as_float(hv[2 * k + 1]));
+            };
+            if (whole) exp_pass(std::true_type{});
+            else exp_pass(std::false_type{});
           } else {
 #pragma unroll
             for (int k = 0; k < HW / 2; ++k) hv[k] = 0u;
@@ -743,7 +748,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
   c.bar0 = sbase + C::OFF_BAR;
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + OFF_ABORT);
   c.header = p.header;
-  c.limit_ns = p.wait_limit_ns;
+  c.limit_cycles = p.wait_limit_cycles;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + OFF_TMEM_SLOT);
 
   if (threadIdx.x == 0) {
@@ -771,7 +776,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
     *c.abort = 0u;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == C::CTL_WARP0 + 1) {
     tmem_alloc(smem_addr(tmem_slot), C::TM_COLS);
     tmem_relinquish();
   }
@@ -781,27 +786,32 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   const int lane = threadIdx.x & 31;
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, p, false);
-    }
-  } else if (warp == 1) {
-    mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
-  } else if (warp < C::DQ_WARP0) {
-    softmax_role<D, NT, ST, KV8>(c, tmem, p, (warp - 2) / 4);
-  } else if (warp < C::VP_WARP) {
+  if (warp < C::SM_WARPS) {
+    if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
+    softmax_role<D, NT, ST, KV8>(c, tmem, p, warp / 4);
+  } else if (warp < C::CTL_WARP0) {
     dequant_role<D, NT, ST, KV8>(c, sbase, p);
-  } else if (lane == 0) {
-    prefetch_tmap(&tm_v);
-    producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_v, p, true);
+  } else {
+    if constexpr (C::SPLIT_REGS) reg_dealloc<C::CTL_REGS>();
+    const int role = warp - C::CTL_WARP0;
+    if (role == 0) {
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+      }
+      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, p, false);
+    } else if (role == 1) {
+      mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
+    } else if (role == 2) {
+      if (lane == 0) prefetch_tmap(&tm_v);
+      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_v, p, true);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+  if (warp == C::CTL_WARP0 + 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
 template <int D, int NT, int ST, bool KV8>

@@ -114,6 +114,17 @@ int query_sm_count() {
   return n;
 }
 
+// Peak SM clock of the current device in kHz (2.07 GHz if it cannot be read).
+uint64_t query_clock_khz() {
+  int dev = 0, khz = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0) {
+    cudaGetLastError();
+    return 2070000;
+  }
+  return uint64_t(khz);
+}
+
 }  // namespace
 
 extern "C" size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, int32_t num_qo_heads,
@@ -530,7 +541,13 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   ap.header = reinterpret_cast<bip::WsHeader*>(ws);
   ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
   ap.v_scale = v_scale;
-  ap.wait_limit_ns = p->opts.wait_limit_ns;
+  // In-kernel waits count SM cycles (the global timer ticks too coarsely for
+  // short limits); at any clock up to the peak, the cycle count takes at
+  // least the requested time.
+  {
+    const uint64_t ns = p->opts.wait_limit_ns, khz = query_clock_khz();
+    ap.wait_limit_cycles = ns > (~0ull / khz) ? ~0ull : std::max<uint64_t>(1, ns * khz / 1000000ull);
+  }
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;
 

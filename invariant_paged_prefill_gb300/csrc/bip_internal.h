@@ -82,7 +82,7 @@ struct AttnParams {
   WsHeader* header;
   float scale_log2;     // log2(e) * k_scale / sqrt(head_dim)
   float v_scale;
-  uint64_t wait_limit_ns;
+  uint64_t wait_limit_cycles;  // wait bound in SM clock cycles (the limit in ns at the peak clock)
 };
 
 struct MergeParams {
