@@ -11,6 +11,7 @@
 // change any row's arithmetic.
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -52,6 +53,7 @@ struct bip_plan_s {
   int32_t num_units = 0, num_split_units = 0, grid = 0;
   int64_t partial_rows = 0, kv_blocks = 0;
   bool need_scratch = false;
+  uint64_t wait_limit_cycles = 0;  // in-kernel wait bound, SM cycles at the peak clock
   size_t off_items = 0, off_merges = 0, off_partials = 0, off_scratch = 0;
   size_t partial_bytes = 0, scratch_bytes = 0, ws_bytes = 0, upload_bytes = 0;
   uint8_t* upload = nullptr;  // header + items + merges, as copied to the workspace
@@ -114,14 +116,25 @@ int query_sm_count() {
   return n;
 }
 
-// Peak SM clock of the current device in kHz (2.07 GHz if it cannot be read).
+// Peak SM clock of the current device in kHz (2.07 GHz if it cannot be
+// read).  The attribute query is slow (hundreds of microseconds), so each
+// device's answer is kept.
 uint64_t query_clock_khz() {
+  static std::atomic<uint64_t> cache[64];
   int dev = 0, khz = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return 2070000;
   }
+  if (dev >= 0 && dev < 64) {
+    const uint64_t v = cache[dev].load(std::memory_order_relaxed);
+    if (v) return v;
+  }
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0) {
+    cudaGetLastError();
+    return 2070000;
+  }
+  if (dev >= 0 && dev < 64) cache[dev].store(uint64_t(khz), std::memory_order_relaxed);
   return uint64_t(khz);
 }
 
@@ -251,6 +264,14 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   // ---- split decision (numerically neutral; see the header)
   int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
   num_sms = std::min(num_sms, bip::kMaxCtas);
+  // In-kernel waits count SM cycles (the global timer ticks too coarsely for
+  // short limits); at any clock up to the peak, the cycle count takes at
+  // least the requested time.  The clock query is slow, so it runs here once.
+  uint64_t wait_limit_cycles;
+  {
+    const uint64_t ns = opts.wait_limit_ns, khz = query_clock_khz();
+    wait_limit_cycles = ns > (~0ull / khz) ? ~0ull : std::max<uint64_t>(1, ns * khz / 1000000ull);
+  }
   std::vector<char> split(units.size(), 0);
   size_t partial_bytes = 0;
   int64_t n_items = int64_t(units.size());
@@ -368,6 +389,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->partial_rows = part_rows;
   p->partial_bytes = size_t(part_rows) * partial_row_bytes(head_dim);
   p->grid = int32_t(std::min<int64_t>(int64_t(p->items.size()), num_sms));
+  p->wait_limit_cycles = wait_limit_cycles;
   p->scratch_bytes =
       p->need_scratch ? size_t(p->grid) * NT * bip::kTileRows * head_dim * sizeof(float) : 0;
   p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->partial_bytes, p->scratch_bytes, &p->off_items,
@@ -541,13 +563,7 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   ap.header = reinterpret_cast<bip::WsHeader*>(ws);
   ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
   ap.v_scale = v_scale;
-  // In-kernel waits count SM cycles (the global timer ticks too coarsely for
-  // short limits); at any clock up to the peak, the cycle count takes at
-  // least the requested time.
-  {
-    const uint64_t ns = p->opts.wait_limit_ns, khz = query_clock_khz();
-    ap.wait_limit_cycles = ns > (~0ull / khz) ? ~0ull : std::max<uint64_t>(1, ns * khz / 1000000ull);
-  }
+  ap.wait_limit_cycles = p->wait_limit_cycles;
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;
 
