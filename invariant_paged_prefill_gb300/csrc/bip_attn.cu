@@ -123,7 +123,8 @@ enum Bar {
   B_S_FULL = 18, B_P_FULL = 22, B_O_DONE = 26,
   B_DRAIN = 30,
   B_K8_FULL = 31, B_K8_FREE = 33, B_V8_FULL = 35, B_V8_FREE = 37,  // FP8 staging, up to 2 stages
-  B_COUNT = 39
+  B_V_TX = 39,  // bf16 V blocks that end past kv_len land here first (the V producer zeroes the tail)
+  B_COUNT = 40
 };
 constexpr int OFF_TMEM_SLOT = 8 * B_COUNT;    // u32: TMEM base address
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;  // u32: a wait expired somewhere in this CTA
@@ -238,12 +239,15 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
   const uint32_t ring0 = sbase + (KV8 ? (is_v ? C::OFF_V8 : C::OFF_K8) : (is_v ? C::OFF_V : C::OFF_K));
   const uint32_t ring_bytes = KV8 ? uint32_t(C::KV8_BYTES) : uint32_t(C::KV_BYTES);
   const uint32_t page_bytes = uint32_t(p.page_size * D * (KV8 ? 1 : 2));
-  uint32_t b = 0;  // blocks started by this CTA
-  int n = 0;       // items started by this CTA
+  uint32_t b = 0;      // blocks started by this CTA
+  int n = 0;           // items started by this CTA
+  uint32_t n_tail = 0;  // bf16 V blocks routed through B_V_TX (issued)
+  uint32_t n_q = 0;     // q tile loads issued
   bool ok = true;
 
   auto load_q = [&](const WorkItem& w, const Geom& g) -> bool {
     if (n > 0 && !wait_warp(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) return false;
+    ++n_q;
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(c, B_Q_FULL), q_slot_bytes * __popc(g.mask));
 #pragma unroll
@@ -280,26 +284,49 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
       }
       if (blk < g.blk_hi) id_next = lane_page_id(p, w, blk + 1, pages_per_blk, npages_req, lane, nid);
       if (use > 0 && !wait_warp(c, bar(c, free0 + slot), (use - 1) & 1, is_v ? 3 : 2)) { ok = false; break; }
-      if (lane == 0) mbar_arrive_expect_tx(bar(c, full0 + slot), uint32_t(ncur) * page_bytes);
+      // A bf16 V block that ends past kv_len lands on B_V_TX; once it is in,
+      // this warp zeroes the rows at or past kv_len (the tail of the last
+      // page, and pages the request does not have) so that p = 0 meets a
+      // finite value, then completes the slot's V_FULL phase itself.  (FP8:
+      // the dequant warps write those zeros.)
+      const int valid_rows = w.kv_len - blk * C::BN;
+      const bool tail = !KV8 && is_v && valid_rows < C::BN;
+      const uint32_t land = tail ? bar(c, B_V_TX) : bar(c, full0 + slot);
+      if (lane == 0) mbar_arrive_expect_tx(land, uint32_t(ncur) * page_bytes);
+      n_tail += tail ? 1u : 0u;
       __syncwarp();
       if (lane < ncur) {
         if constexpr (KV8) {
-          tma_load_4d(ring0 + slot * ring_bytes + lane * page_bytes, tkv, bar(c, full0 + slot), 0, w.kv_head, 0,
-                      id);
+          tma_load_4d(ring0 + slot * ring_bytes + lane * page_bytes, tkv, land, 0, w.kv_head, 0, id);
         } else {
           for (int ch = 0; ch < C::DCH; ++ch)
-            tma_load_4d(ring0 + slot * ring_bytes + ch * C::KV_CHUNK + lane * p.page_size * 128, tkv,
-                        bar(c, full0 + slot), ch * 64, w.kv_head, 0, id);
+            tma_load_4d(ring0 + slot * ring_bytes + ch * C::KV_CHUNK + lane * p.page_size * 128, tkv, land,
+                        ch * 64, w.kv_head, 0, id);
         }
+      }
+      if (tail) {
+        if (!wait_warp(c, land, (n_tail - 1) & 1, 4)) { ok = false; break; }
+        const uint32_t vbase = ring0 + slot * ring_bytes;
+        const int per_chunk = (C::BN - valid_rows) * 8;  // 16-byte units per chunk
+        for (int u = lane; u < per_chunk * C::DCH; u += 32) {
+          const int ch = u / per_chunk, rem = u % per_chunk;
+          const uint32_t addr = vbase + ch * C::KV_CHUNK + (valid_rows + rem / 8) * 128 + (rem % 8) * 16;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(c, full0 + slot));
+        __syncwarp();
       }
     }
     if (ok && !q_done && !load_q(w, g)) ok = false;  // items shorter than the ring
   }
   // Drain: the last load on every barrier must have landed before exit (on
   // the normal path these phases completed long ago).  Phases issued: one
-  // per item for Q (K stream only), and blocks started / RING per slot.
+  // per q load (K stream only), and blocks started / RING per slot.
   if (lane == 0) {
-    if (!is_v && n > 0) drain_wait(bar(c, B_Q_FULL), (n - 1) & 1);
+    if (n_q) drain_wait(bar(c, B_Q_FULL), (n_q - 1) & 1);
+    if (n_tail) drain_wait(bar(c, B_V_TX), (n_tail - 1) & 1);
 #pragma unroll
     for (int slot = 0; slot < RING; ++slot) {
       const uint32_t issued = b / RING + (uint32_t(slot) < b % RING ? 1u : 0u);
@@ -309,14 +336,18 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
   __syncwarp();
 }
 
+// The tcgen05 issuer: one thread.  The tensor pipe queues only a few MMAs,
+// so every cycle spent between two groups of MMAs (barrier probes, warp
+// votes) shows up as pipe idle time; a single thread with plain probes keeps
+// that gap short.
 template <int D, int NT, int ST, bool KV8>
 __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const AttnParams& p) {
   using C = Cfg<D, NT, ST, KV8>;
-  const int lane = threadIdx.x & 31;
   const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);  // S = Q K^T, both K-major
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);       // O += P V, V MN-major
   uint32_t gb = 0;                       // KV blocks consumed by this CTA (ring position)
+  uint32_t k_seen = 0;                   // K blocks known to have landed
   uint32_t s_cnt[NT] = {}, pv_cnt[NT] = {};  // blocks whose S / PV was issued, per slot
   int n = 0;
   bool ok = true;
@@ -324,36 +355,36 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int nb = g.blk_hi - g.blk_lo + 1;
-    if (!wait_warp(c, bar(c, B_Q_FULL), n & 1, 10)) { ok = false; break; }
+    if (!wait_phase(c, bar(c, B_Q_FULL), n & 1, 10)) { ok = false; break; }
     tc_fence_after();
 
     // S_t for item-local block j into the slot's next S buffer.
     auto issue_s = [&](int t, int j) -> bool {
       const uint32_t kb = gb + j;
       const int kslot = kb % ST;
-      if (!wait_warp(c, bar(c, B_K_FULL + kslot), (kb / ST) & 1, 11)) return false;
-      tc_fence_after();
-      const int sbuf = s_cnt[t] % C::NS;
-      if (lane == 0) {
-        const uint32_t d_tmem = tmem + C::tm_s(t, sbuf);
-        // K step k: 32 bytes along a 128-byte row, 64 columns per chunk.  The
-        // start address sits in the descriptor's low bits (16-byte units), so
-        // a step is an add; a rolled loop keeps this issue path small.
-        const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
-        const uint64_t dk = sdesc_sw128(sK + kslot * C::KV_BYTES, 16, 1024);
-#pragma unroll 1
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t cq = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
-          const uint32_t ck = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
-          tc_mma_ss(d_tmem, dq + cq, dk + ck, kIdescS, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(c, B_S_FULL + 2 * t + sbuf));
-        if (t == g.last_slot) {
-          tc_commit(bar(c, B_K_FREE + kslot));                // last reader of this K block
-          if (j == nb - 1) tc_commit(bar(c, B_Q_FREE));       // last reader of the q tiles
-        }
+      if (kb >= k_seen) {  // the other slot's S may already have seen this K block land
+        if (!wait_phase(c, bar(c, B_K_FULL + kslot), (kb / ST) & 1, 11)) return false;
+        k_seen = kb + 1;
+        tc_fence_after();
       }
-      __syncwarp();
+      const int sbuf = s_cnt[t] % C::NS;
+      const uint32_t d_tmem = tmem + C::tm_s(t, sbuf);
+      // K step k: 32 bytes along a 128-byte row, 64 columns per chunk.  The
+      // start address sits in the descriptor's low bits (16-byte units), so
+      // a step is an add; a rolled loop keeps this issue path small.
+      const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+      const uint64_t dk = sdesc_sw128(sK + kslot * C::KV_BYTES, 16, 1024);
+#pragma unroll 1
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t cq = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
+        const uint32_t ck = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
+        tc_mma_ss(d_tmem, dq + cq, dk + ck, kIdescS, k > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(c, B_S_FULL + 2 * t + sbuf));
+      if (t == g.last_slot) {
+        tc_commit(bar(c, B_K_FREE + kslot));                // last reader of this K block
+        if (j == nb - 1) tc_commit(bar(c, B_Q_FREE));       // last reader of the q tiles
+      }
       ++s_cnt[t];
       return true;
     };
@@ -374,54 +405,33 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
       for (int t = 0; t < NT; ++t) {
         if (!(g.mask >> t & 1)) continue;
         const int pbuf = pv_cnt[t] % C::NS;
-        if (!wait_warp(c, bar(c, B_P_FULL + 2 * t + pbuf), (pv_cnt[t] / C::NS) & 1, 13)) { ok = false; break; }
+        if (!wait_phase(c, bar(c, B_P_FULL + 2 * t + pbuf), (pv_cnt[t] / C::NS) & 1, 13)) { ok = false; break; }
         if (!v_ready) {
-          if (!wait_warp(c, bar(c, B_V_FULL + vslot), (vb / ST) & 1, 14)) { ok = false; break; }
-          tc_fence_after();
-          // Rows of V at or past kv_len (the tail of the last page, and pages the
-          // request does not have) are zeroed so that p = 0 meets a finite value.
-          const int valid_rows = w.kv_len - blk * C::BN;
-          if (!KV8 && valid_rows < C::BN) {  // (FP8: the dequant warps wrote these zeros)
-            const uint32_t vbase = sV + vslot * C::KV_BYTES;
-            const int per_chunk = (C::BN - valid_rows) * 8;  // 16-byte units per chunk
-            for (int u = lane; u < per_chunk * C::DCH; u += 32) {
-              const int ch = u / per_chunk, rem = u % per_chunk;
-              const uint32_t addr = vbase + ch * C::KV_CHUNK + (valid_rows + rem / 8) * 128 + (rem % 8) * 16;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
+          // V rows at or past kv_len were zeroed before this phase completed.
+          if (!wait_phase(c, bar(c, B_V_FULL + vslot), (vb / ST) & 1, 14)) { ok = false; break; }
           v_ready = true;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t p_tmem = tmem + C::tm_s(t, pbuf);  // P_t (bf16) over its S buffer
-          const uint64_t dv = sdesc_sw128(sV + vslot * C::KV_BYTES, C::KV_CHUNK, 1024);
+        const uint32_t p_tmem = tmem + C::tm_s(t, pbuf);  // P_t (bf16) over its S buffer
+        const uint64_t dv = sdesc_sw128(sV + vslot * C::KV_BYTES, C::KV_CHUNK, 1024);
 #pragma unroll 1
-          for (int k = 0; k < C::BN / 16; ++k)  // K step k: 16 V rows (2048 bytes), 8 TMEM columns of P
-            tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, dv + uint32_t(k * 128), kIdescO,
-                      (k > 0 || !first_in_seg) ? 1u : 0u);
-          tc_commit(bar(c, B_O_DONE + 2 * t + pbuf));
-        }
-        __syncwarp();
+        for (int k = 0; k < C::BN / 16; ++k)  // K step k: 16 V rows (2048 bytes), 8 TMEM columns of P
+          tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, dv + uint32_t(k * 128), kIdescO,
+                    (k > 0 || !first_in_seg) ? 1u : 0u);
+        tc_commit(bar(c, B_O_DONE + 2 * t + pbuf));
         ++pv_cnt[t];
         // The slot's next S goes into the buffer this PV has just been queued
         // to read; tcgen05 MMAs of one thread execute in issue order.
         if (j + C::NS < nb && !issue_s(t, j + C::NS)) { ok = false; break; }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(bar(c, B_V_FREE + vslot));
-      __syncwarp();
+      tc_commit(bar(c, B_V_FREE + vslot));
     }
     gb += nb;
   }
   // Drain: every MMA this thread issued has completed before TMEM is freed.
-  if (lane == 0) {
-    tc_commit(bar(c, B_DRAIN));
-    drain_wait(bar(c, B_DRAIN), 0);
-  }
-  __syncwarp();
+  tc_commit(bar(c, B_DRAIN));
+  drain_wait(bar(c, B_DRAIN), 0);
 }
 
 template <int D, int NT, int ST, bool KV8>
@@ -773,6 +783,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
         mbar_init(bar(c, B_O_DONE + 2 * t + s), 1);
       }
     mbar_init(bar(c, B_DRAIN), 1);
+    mbar_init(bar(c, B_V_TX), 1);
     *c.abort = 0u;
     fence_mbar_init();
   }
@@ -801,7 +812,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
       }
       producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, p, false);
     } else if (role == 1) {
-      mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
+      if (lane == 0) mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
     } else if (role == 2) {
       if (lane == 0) prefetch_tmap(&tm_v);
       producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_v, p, true);

@@ -56,7 +56,7 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
     for t in range(NT):
         for s in range(NS):
             bar(f"S_FULL{t}{s}"), bar(f"P_FULL{t}{s}", 32 * warps), bar(f"O_DONE{t}{s}")
-    bar("Q_FULL"), bar("Q_FREE")
+    bar("Q_FULL"), bar("Q_FREE"), bar("V_TX")
     clock, pending, last_mma = [0], [], [0]
 
     def later(name, lo=1, hi=8):
@@ -70,11 +70,13 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
         return ("wait", name, idx)
 
     def producer(is_v):
-        """Lane 0 streams the q tiles and K, lane 1 streams V; an item's first
-        ring-depth K blocks go out before its q tiles."""
+        """One warp streams the q tiles and K, another streams V; an item's
+        first ring-depth K blocks go out before its q tiles.  A bf16 V block
+        that ends past kv_len (here: every item's last block) lands on V_TX;
+        the V warp waits for it, zeroes the tail and completes V_FULL."""
         ring = SS if SS else ST
         kv = ("V8" if SS else "V") if is_v else ("K8" if SS else "K")
-        b = 0
+        b, n_tail = 0, 0
         for n, (nb, mask) in enumerate(items):
             q_done = is_v
 
@@ -90,7 +92,13 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
                 slot, use = b % ring, b // ring
                 if use > 0:
                     yield wait(f"{kv}_FREE{slot}", use - 1)
-                later(f"{kv}_FULL{slot}")
+                if is_v and not SS and j == nb - 1:
+                    later("V_TX")
+                    yield wait("V_TX", n_tail)
+                    n_tail += 1
+                    B[f"V_FULL{slot}"].arrive()
+                else:
+                    later(f"{kv}_FULL{slot}")
                 b += 1
                 yield None
             if not q_done:
@@ -112,14 +120,16 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
                 yield None
 
     def issuer():
-        gb, s_cnt, pv_cnt = 0, [0] * NT, [0] * NT
+        gb, s_cnt, pv_cnt, k_seen = 0, [0] * NT, [0] * NT, [0]
         for n, (nb, mask) in enumerate(items):
             yield wait("Q_FULL", n)
             last = max(t for t in range(NT) if mask >> t & 1)
 
             def issue_s(t, j):
                 kb = gb + j
-                yield wait(f"K_FULL{kb % ST}", kb // ST)
+                if kb >= k_seen[0]:  # another slot's S may already have seen it land
+                    yield wait(f"K_FULL{kb % ST}", kb // ST)
+                    k_seen[0] = kb + 1
                 commit(f"S_FULL{t}{s_cnt[t] % NS}")
                 if t == last:
                     commit(f"K_FREE{kb % ST}")
