@@ -478,12 +478,17 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         const uint32_t sa = t_lane + C::tm_s(t, sbuf);
         const int lim = valid ? pos - blk * C::BN : -1;  // columns 0..lim are visible
 
-        // Blocks wholly visible to every row of the warp skip the per-column
-        // mask (same values, fewer instructions).  A warp with no visible
-        // column in this block skips the arithmetic but still stores P = 0:
-        // its rows may be valid rows past whose position the block lies, and
-        // their O keeps accumulating P V.
-        const bool whole = __all_sync(0xffffffffu, lim >= C::BN - 1);
+        // Blocks wholly visible to every valid row of the warp skip the
+        // per-column mask (same values for those rows, fewer instructions).
+        // Rows that are not valid (before the first q row of an extend, past
+        // the tile's end) are never written out; on the whole-block path they
+        // compute on whatever scores their q rows give, which touches no other
+        // row (each row of P V depends only on that row of P) and never asks
+        // for a rescale.  A warp with no visible column in this block skips
+        // the arithmetic but still stores P = 0: its rows may be valid rows
+        // past whose position the block lies, and their O keeps accumulating
+        // P V.
+        const bool whole = __all_sync(0xffffffffu, !valid || lim >= C::BN - 1);
         const bool live = __any_sync(0xffffffffu, lim >= 0);
 
         // Block max.  One TMEM round trip for the whole S row; with fewer than
@@ -586,7 +591,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // Rescale O where the running max moved (alpha is exactly 1 elsewhere);
         // the first block of a segment overwrites O instead.  With one S
         // buffer the S_FULL phase already implies the previous PV completed.
-        if ((blk % C::BPS) != 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if ((blk % C::BPS) != 0 && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
           if (C::NS == 2 && !wait_pv(cnt - 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
