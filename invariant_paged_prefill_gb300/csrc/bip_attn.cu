@@ -91,7 +91,7 @@ struct Cfg {
   // launch count.  The sum never exceeds what the launch holds.
   static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;
   static constexpr bool SPLIT_REGS = THREADS > 256;
-  static constexpr int CTL_REGS = 56;
+  static constexpr int CTL_REGS = KV8 ? 80 : 56;  // FP8: softmax is capped at 240 anyway
   static constexpr int SM_REGS_FREE =
       ((LAUNCH_REGS * THREADS - CTL_REGS * 128 - (KV8 ? LAUNCH_REGS * 128 : 0)) / (32 * SM_WARPS)) & ~7;
   static constexpr int SM_REGS = SPLIT_REGS ? (SM_REGS_FREE < 240 ? SM_REGS_FREE : 240) : 255;
@@ -99,6 +99,11 @@ struct Cfg {
                                    LAUNCH_REGS * THREADS, "register split exceeds the launch's registers");
   static_assert(!SPLIT_REGS || SM_REGS >= LAUNCH_REGS, "softmax warps must not lose registers");
   static constexpr int TM_COLS = 512;
+  // Unroll factor of the MMA issue loops.  The tensor pipe queues only a few
+  // MMAs, so the issuing thread's per-MMA instructions show up as pipe time;
+  // measured on GB300, full unrolling is best with one q-tile slot and 4
+  // with two (whose larger issue path slows down when fully unrolled).
+  static constexpr int ISSUE_UNROLL = NT == 1 ? 16 : 4;
   static constexpr int BPS = kSplitLen / BN;         // blocks per segment
   // TMEM columns: two slots use [0,256) and [256,512), each S (BN) then O (D);
   // one slot keeps two S buffers at [0, 2 BN) and O at [256, 256 + D).
@@ -371,10 +376,10 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
       const uint32_t d_tmem = tmem + C::tm_s(t, sbuf);
       // K step k: 32 bytes along a 128-byte row, 64 columns per chunk.  The
       // start address sits in the descriptor's low bits (16-byte units), so
-      // a step is an add; a rolled loop keeps this issue path small.
+      // a step is an add.
       const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
       const uint64_t dk = sdesc_sw128(sK + kslot * C::KV_BYTES, 16, 1024);
-#pragma unroll 1
+#pragma unroll (C::ISSUE_UNROLL)
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t cq = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
         const uint32_t ck = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
@@ -414,7 +419,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
         tc_fence_after();
         const uint32_t p_tmem = tmem + C::tm_s(t, pbuf);  // P_t (bf16) over its S buffer
         const uint64_t dv = sdesc_sw128(sV + vslot * C::KV_BYTES, C::KV_CHUNK, 1024);
-#pragma unroll 1
+#pragma unroll (C::ISSUE_UNROLL)
         for (int k = 0; k < C::BN / 16; ++k)  // K step k: 16 V rows (2048 bytes), 8 TMEM columns of P
           tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, dv + uint32_t(k * 128), kIdescO,
                     (k > 0 || !first_in_seg) ? 1u : 0u);
@@ -543,9 +548,10 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // absolute position (blocks start at multiples of 16).  Masked columns
         // are computed and then replaced by exact zeros, so a row gets the
         // same bits through the whole-block and the masked path.
-        // Row-sum partials: acc01 holds columns 0, 1 (mod 4), acc23 columns
-        // 2, 3 (mod 4), each pair summed with one packed add.
-        uint64_t acc01 = 0ull, acc23 = 0ull;
+        // Row-sum partials: acc[i] holds columns 2i, 2i + 1 (mod 8), each
+        // pair summed with one packed add (four chains, so that the adds do
+        // not wait on each other); they are combined pairwise at the end.
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         const uint64_t sc2 = f2_splat(scale), nm2 = f2_splat(-ms);
 #pragma unroll
         for (int h = 0; h < C::BN / HW; ++h) {
@@ -555,23 +561,17 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
             auto exp_pass = [&](auto whole_c) {
               constexpr bool kWhole = decltype(whole_c)::value;
 #pragma unroll
-              for (int j = 0; j < HW; j += 4) {
-                const int col = h * HW + j;
-                uint64_t e[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int cu = col + 2 * u;
-                  const uint64_t x = ffma2(
-                      f2_bits(__uint_as_float(hv[j + 2 * u]), __uint_as_float(hv[j + 2 * u + 1])), sc2, nm2);
-                  const int pair = (cu >> 1) & 7;
-                  if (kFmaPairs >> pair & 1) e[u] = ex2_fma2(x);
-                  else e[u] = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
-                  if (!kWhole) e[u] = f2_bits(cu <= lim ? f2_lo(e[u]) : 0.f, cu + 1 <= lim ? f2_hi(e[u]) : 0.f);
-                }
-                acc01 = fadd2(acc01, e[0]);
-                acc23 = fadd2(acc23, e[1]);
-                hv[j / 2] = pack_bf16x2(f2_lo(e[0]), f2_hi(e[0]));
-                hv[j / 2 + 1] = pack_bf16x2(f2_lo(e[1]), f2_hi(e[1]));
+              for (int j = 0; j < HW; j += 2) {
+                const int cu = h * HW + j;
+                const uint64_t x =
+                    ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
+                const int pair = (cu >> 1) & 7;
+                uint64_t e;
+                if (kFmaPairs >> pair & 1) e = ex2_fma2(x);
+                else e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
+                if (!kWhole) e = f2_bits(cu <= lim ? f2_lo(e) : 0.f, cu + 1 <= lim ? f2_hi(e) : 0.f);
+                acc[pair & 3] = fadd2(acc[pair & 3], e);
+                hv[j / 2] = pack_bf16x2(f2_lo(e), f2_hi(e));
               }
             };
             if (whole) exp_pass(std::true_type{});
@@ -584,8 +584,8 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           else tmem_st_x32_p(sa + h * (HW / 2), hv);
         }
         if (valid) {
-          const float rowsum =
-              __fadd_rn(__fadd_rn(f2_lo(acc01), f2_hi(acc01)), __fadd_rn(f2_lo(acc23), f2_hi(acc23)));
+          const uint64_t a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+          const float rowsum = __fadd_rn(f2_lo(a), f2_hi(a));
           l = __fadd_rn(__fmul_rn(l, alpha), rowsum);
         }
         // Rescale O where the running max moved (alpha is exactly 1 elsewhere);
