@@ -13,6 +13,9 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Both decoders are written from those definitions, element by element, with
 no library conversion routine; the tests compare them against library casts.
+The E4M3 encoder (used to quantise K/V rows appended to an FP8 cache) is
+written from the same definition: nearest representable value, ties to the
+even code, magnitudes beyond 448 saturated to 448.
 """
 
 from __future__ import annotations
@@ -47,3 +50,35 @@ def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Decode raw FP8 E4M3 storage (uint8 codes) to float64."""
     codes = np.asarray(bits).astype(np.int64) & 0xFF
     return _E4M3_TABLE[codes]
+
+
+# Non-negative finite E4M3 values in code order (codes 0x00 .. 0x7E); the
+# order of the codes is the order of the values.
+_E4M3_POS = _E4M3_TABLE[:0x7F]
+
+
+def f64_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Encode values as FP8 E4M3 codes (uint8).
+
+    Round to the nearest representable value; a value exactly halfway
+    between two takes the code whose mantissa is even (lowest bit 0);
+    magnitudes above 448 saturate to +-448 (no infinities exist); NaN becomes
+    the positive NaN code 0x7F.  The sign of zero is kept.
+    """
+    v = np.asarray(x, dtype=np.float64)
+    flat = v.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    mag = np.abs(flat)
+    sign = np.signbit(flat).astype(np.uint8) << 7
+    nan = np.isnan(flat)
+    m = np.where(nan, 0.0, np.minimum(mag, 448.0))
+    hi = np.searchsorted(_E4M3_POS, m, side="left")   # first code with value >= m
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E4M3_POS[hi] - m
+    d_lo = m - _E4M3_POS[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(pick_lo, lo, hi).astype(np.uint8)
+    out[:] = code | sign
+    out[nan] = 0x7F
+    return out.reshape(v.shape)
