@@ -366,6 +366,33 @@ def workload_config(name):
             "l2": "inputs larger than L2 (129 MB) between timed iterations"}
 
 
+def time_append(b, device, steps: int, warmup: int):
+    """Paged KV append of every q row's K/V into b's pools (overwrites them):
+    (ms per call, bytes moved per call).  Bytes: the bf16 rows read plus the
+    pool slots written."""
+    import invariant_paged_prefill_gb300 as bip
+    plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=b.num_qo_heads,
+                    num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size, kv_dtype=b.kv_dtype)
+    g = torch.Generator(device=device).manual_seed(77)
+    shape = (plan.total_q, b.num_kv_heads, b.head_dim)
+    k_new = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    v_new = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    for _ in range(warmup):
+        bip.append_kv(plan, k_new, v_new, b.k_pages, b.v_pages, b.kv_indices, workspace=ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        bip.append_kv(plan, k_new, v_new, b.k_pages, b.v_pages, b.kv_indices, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    elem = 2 if b.kv_dtype == "bf16" else 1
+    moved = 2 * k_new.numel() * (2 + elem)
+    return e0.elapsed_time(e1) / steps, moved
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -444,6 +471,18 @@ def run_ours(args):
                            "max_abs_out": float(np.abs(got - ro).max()), "max_abs_lse": float(np.abs(gl - rl).max())},
                 "bit_exact_repeat": repeat_exact, "workspace_bytes": run.plan.workspace_bytes,
                 "source_hash": source_hash()}
+        # the paged KV append (the step before attention), timed last: it
+        # overwrites the pools of both batches
+        a_ms, a_bytes = time_append(b, device, args.steps, args.warmup)
+        sa_ms, _ = time_append(sb, device, args.steps, args.warmup)
+        a_gbs = a_bytes / (a_ms * 1e-3) / 1e9
+        line["append"] = {
+            "workload": f"paged KV append of {batch} x {q_len} new rows (bf16 K and V, heads "
+                        f"{heads[1]} x {heads[2]}) into the long_q pools",
+            "value": a_gbs, "unit": "GB/s", "ms_per_step": a_ms,
+            "roofline": {"bound": "hbm", "achieved": a_gbs, "peak": hbm, "unit": "GB/s", "frac": a_gbs / hbm,
+                         "peak_source": f"hbm_gbs of {peak_kind}"},
+            "short_extend_us": sa_ms * 1e3}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -170,6 +170,34 @@ bip_status bip_prefill(bip_plan_t plan, const void* q, int64_t num_q_rows, const
                        const int32_t* kv_indices, float k_scale, float v_scale, void* out,
                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Write each request's new K/V rows into its pages: the paged KV append that
+ * precedes the attention of an extend: on a radix-cache prefix hit only the
+ * uncached tail is computed and its K/V join the cached pages (sglang PR 46351,
+ * "Motivation"); the FP8 E4M3 cache is the --kv-cache-dtype fp8_e4m3 setup of
+ * the model-serving-minefield issue 73 report, "What were you serving".
+ * The plan supplies the batch: request r's rows [qo_indptr[r], qo_indptr[r+1])
+ * of k_new / v_new go to sequence positions kv_len_r - q_len_r .. kv_len_r - 1,
+ * position p in page kv_indices[kv_indptr[r] + p / page_size], slot
+ * p % page_size.  DEVICE pointers:
+ *   k_new, v_new  bf16 [num_new_rows, num_kv_heads, head_dim], contiguous;
+ *            num_new_rows must equal qo_indptr[batch]
+ *   k_pages, v_pages  the pools bip_prefill reads (NHD, page stride as there),
+ *            written in place; only the new rows' slots are touched
+ *   kv_indices int32 page ids, each in [0, num_pages); others are counted
+ *            (bip_read_device_status reports BIP_ERR_BAD_PAGE_INDEX) and skipped
+ *   workspace  any buffer good for bip_prefill (only its first bytes are used);
+ *            its first bytes receive the plan's tables and a status word.
+ * bf16 pages receive the bits unchanged (k_scale and v_scale must be 1.0).
+ * E4M3 pages receive e4m3(x / scale): x widened to float32, divided by the
+ * scale with IEEE rounding, rounded to the nearest E4M3 value (ties to even)
+ * and saturated at +-448; scales must be positive and finite.  Rows, pages
+ * and the workspace must be 16-byte aligned.  Enqueued on `stream`; never
+ * synchronizes.  Calls sharing a workspace must be ordered on the GPU. */
+bip_status bip_append_kv(bip_plan_t plan, const void* k_new, const void* v_new, int64_t num_new_rows,
+                         void* k_pages, void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                         const int32_t* kv_indices, float k_scale, float v_scale, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the device array that bip_prefill_no_alloc uses as its workspace. */
 #define BIP_NO_ALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
 

@@ -21,7 +21,7 @@ import numpy as np
 
 from . import _lib
 
-__all__ = ["BipError", "Plan", "prefill", "workspace_bound", "read_device_status", "STATUS"]
+__all__ = ["BipError", "Plan", "prefill", "append_kv", "workspace_bound", "read_device_status", "STATUS"]
 
 STATUS = {
     0: "BIP_OK", 1: "BIP_ERR_INVALID_ARG", 2: "BIP_ERR_UNSUPPORTED", 3: "BIP_ERR_WORKSPACE_TOO_SMALL",
@@ -158,6 +158,46 @@ def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, 
                                  _dev_ptr(out, "out"), _dev_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
                                  workspace.numel() * workspace.element_size(), sptr), "bip_prefill")
     return out, lse
+
+
+def append_kv(plan: Plan, k_new, v_new, k_pages, v_pages, kv_indices, *, workspace=None,
+              k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+    """Enqueue the paged KV append on ``stream`` (default: torch's current stream).
+
+    k_new / v_new bf16 [total_q, Hkv, d]: request r's new rows, in the plan's
+    row order, go to its positions kv_len - q_len .. kv_len - 1.  The pools
+    (the same tensors ``prefill`` reads) are written in place: bf16 bits
+    unchanged, or e4m3(x / scale) for uint8 (E4M3) pools.
+    """
+    import torch
+    dev = k_new.device
+    if workspace is None:
+        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise BipError(1, f"{name} must be contiguous bf16")
+        if tuple(t.shape) != (plan.total_q, plan.num_kv_heads, plan.head_dim):
+            raise BipError(1, f"{name} must be [total_q, Hkv, d] of the plan")
+    if kv_indices.dtype != torch.int32:
+        raise BipError(1, "kv_indices must be int32")
+    want = torch.bfloat16 if plan.kv_dtype == "bf16" else torch.uint8
+    for name, pg in (("k_pages", k_pages), ("v_pages", v_pages)):
+        if pg.dtype != want or pg.dim() != 4 or tuple(pg.shape[1:]) != (plan.page_size, plan.num_kv_heads,
+                                                                        plan.head_dim):
+            raise BipError(1, f"{name} must be [num_pages, page_size, Hkv, d] of {want}")
+        if pg.stride()[1:] != (plan.num_kv_heads * plan.head_dim, plan.head_dim, 1):
+            raise BipError(1, f"{name}: slots and heads must be contiguous inside a page")
+    if k_pages.shape[0] != v_pages.shape[0] or k_pages.stride(0) != v_pages.stride(0):
+        raise BipError(1, "k_pages and v_pages must share page count and stride")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    _check(plan._lib.bip_append_kv(plan._h, _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"), k_new.shape[0],
+                                   _dev_ptr(k_pages, "k_pages"), _dev_ptr(v_pages, "v_pages"), k_pages.shape[0],
+                                   k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"), float(k_scale),
+                                   float(v_scale), _dev_ptr(workspace, "workspace"),
+                                   workspace.numel() * workspace.element_size(),
+                                   ctypes.c_void_p(stream.cuda_stream)), "bip_append_kv")
+    return k_pages, v_pages
 
 
 def read_device_status(workspace, stream=None) -> int:

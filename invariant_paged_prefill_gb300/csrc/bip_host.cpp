@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -50,11 +51,13 @@ struct bip_plan_s {
   std::vector<WorkItem> items;
   std::vector<MergeUnit> merges;
   std::vector<int32_t> item_desc;  // 8 int32 per item, see bip_plan_get_items
+  std::vector<bip::AppendRow> reqs;  // requests with new rows, for bip_append_kv
   int32_t num_units = 0, num_split_units = 0, grid = 0;
   int64_t partial_rows = 0, kv_blocks = 0;
   bool need_scratch = false;
   uint64_t wait_limit_cycles = 0;  // in-kernel wait bound, SM cycles at the peak clock
-  size_t off_items = 0, off_merges = 0, off_partials = 0, off_scratch = 0;
+  int32_t sms = 0;                 // CTAs to fill (the planned device's SM count, capped)
+  size_t off_items = 0, off_merges = 0, off_reqs = 0, off_partials = 0, off_scratch = 0;
   size_t partial_bytes = 0, scratch_bytes = 0, ws_bytes = 0, upload_bytes = 0;
   uint8_t* upload = nullptr;  // header + items + merges, as copied to the workspace
   bool pinned = false;
@@ -86,10 +89,15 @@ bip_status check_heads(int32_t hq, int32_t hkv, int32_t d) {
 
 size_t partial_row_bytes(int32_t d) { return size_t(d + 4) * sizeof(float); }
 
-size_t layout_bytes(size_t n_items, size_t n_merges, size_t partial_bytes, size_t scratch_bytes,
-                    size_t* off_items, size_t* off_merges, size_t* off_partials, size_t* off_scratch,
-                    size_t* upload_bytes) {
+size_t layout_bytes(size_t n_items, size_t n_merges, size_t n_reqs, size_t partial_bytes, size_t scratch_bytes,
+                    size_t* off_items, size_t* off_merges, size_t* off_reqs, size_t* off_partials,
+                    size_t* off_scratch, size_t* upload_bytes) {
+  // header | request rows | work items | merge units: the append uploads only
+  // the prefix before the work items.
   size_t o = bip::kHeaderBytes;
+  *off_reqs = o;
+  o += n_reqs * sizeof(bip::AppendRow);
+  o = align_up(o, 16);
   *off_items = o;
   o += n_items * sizeof(WorkItem);
   *off_merges = o;
@@ -152,8 +160,9 @@ extern "C" size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, in
   const int64_t extra = int64_t(split_budget_bytes / (size_t(group) * partial_row_bytes(head_dim)));
   const size_t scratch =
       size_t(bip::kMaxCtas) * bip::max_tiles_per_unit_for(head_dim) * bip::kTileRows * head_dim * sizeof(float);
-  size_t a, b, c, e, u;
-  return layout_bytes(size_t(units + extra), size_t(units), split_budget_bytes, scratch, &a, &b, &c, &e, &u);
+  size_t a, b, c, e, u, rq;
+  return layout_bytes(size_t(units + extra), size_t(units), size_t(max_batch), split_budget_bytes, scratch, &a, &b,
+                      &rq, &c, &e, &u);
 }
 
 extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, const int32_t* kv_indptr,
@@ -314,6 +323,15 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->total_q = qo_indptr[batch];
   p->opts = opts;
   p->num_units = int32_t(units.size());
+  for (int32_t r = 0; r < batch; ++r) {
+    if (q_len[r] == 0) continue;
+    bip::AppendRow row;
+    row.tok0 = qo_indptr[r];
+    row.q_len = q_len[r];
+    row.pos0 = kv_len[r] - q_len[r];
+    row.page_base = kv_indptr[r];
+    p->reqs.push_back(row);
+  }
 
   struct Pending {
     WorkItem w;
@@ -390,10 +408,12 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->partial_bytes = size_t(part_rows) * partial_row_bytes(head_dim);
   p->grid = int32_t(std::min<int64_t>(int64_t(p->items.size()), num_sms));
   p->wait_limit_cycles = wait_limit_cycles;
+  p->sms = num_sms;
   p->scratch_bytes =
       p->need_scratch ? size_t(p->grid) * NT * bip::kTileRows * head_dim * sizeof(float) : 0;
-  p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->partial_bytes, p->scratch_bytes, &p->off_items,
-                             &p->off_merges, &p->off_partials, &p->off_scratch, &p->upload_bytes);
+  p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->reqs.size(), p->partial_bytes, p->scratch_bytes,
+                             &p->off_items, &p->off_merges, &p->off_reqs, &p->off_partials, &p->off_scratch,
+                             &p->upload_bytes);
 
   // ---- host image of what each call uploads: header + items + merge units
   void* buf = nullptr;
@@ -413,6 +433,8 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     std::memcpy(p->upload + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem));
   if (!p->merges.empty())
     std::memcpy(p->upload + p->off_merges, p->merges.data(), p->merges.size() * sizeof(MergeUnit));
+  if (!p->reqs.empty())
+    std::memcpy(p->upload + p->off_reqs, p->reqs.data(), p->reqs.size() * sizeof(bip::AppendRow));
 
   *plan_out = p;
   if (workspace_bytes) *workspace_bytes = p->ws_bytes;
@@ -580,6 +602,54 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
     mp.v_scale = v_scale;
     if (bip::launch_merge(p->d, mp, stream) != cudaSuccess) return BIP_ERR_CUDA;
   }
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_append_kv(bip_plan_t p, const void* k_new, const void* v_new, int64_t num_new_rows,
+                                    void* k_pages, void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                                    const int32_t* kv_indices, float k_scale, float v_scale, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+  if (!p) return BIP_ERR_INVALID_ARG;
+  if (num_new_rows != p->total_q) return BIP_ERR_INVALID_ARG;
+  if (p->total_q == 0) return BIP_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !kv_indices || !workspace) return BIP_ERR_INVALID_ARG;
+  if (num_pages <= 0 || num_pages > INT32_MAX || page_stride_elems <= 0) return BIP_ERR_INVALID_ARG;
+  const bool fp8 = p->kv_dtype == BIP_KV_FP8_E4M3;
+  const int64_t elem = fp8 ? 1 : 2;
+  if (page_stride_elems < int64_t(p->page_size) * p->hkv * p->d) return BIP_ERR_INVALID_ARG;
+  if ((page_stride_elems * elem) % 16 != 0) return BIP_ERR_INVALID_ARG;
+  auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (misaligned(k_new) || misaligned(v_new) || misaligned(k_pages) || misaligned(v_pages) || misaligned(workspace))
+    return BIP_ERR_INVALID_ARG;
+  if (fp8) {
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+      return BIP_ERR_INVALID_ARG;
+  } else if (k_scale != 1.f || v_scale != 1.f) {
+    return BIP_ERR_INVALID_ARG;  // bf16 pages store the rows unchanged
+  }
+  if (workspace_bytes < p->off_items) return BIP_ERR_WORKSPACE_TOO_SMALL;
+
+  // header (status word cleared) and request rows only
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemcpyAsync(ws, p->upload, p->off_items, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return BIP_ERR_CUDA;
+  bip::AppendParams ap;
+  ap.rows = reinterpret_cast<const bip::AppendRow*>(ws + p->off_reqs);
+  ap.n_rows = int32_t(p->reqs.size());
+  ap.total_q = p->total_q;
+  ap.num_kv_heads = p->hkv;
+  ap.page_size = p->page_size;
+  ap.num_pages = int32_t(num_pages);
+  ap.page_stride = page_stride_elems;
+  ap.kv_indices = kv_indices;
+  ap.k_new = static_cast<const uint16_t*>(k_new);
+  ap.v_new = static_cast<const uint16_t*>(v_new);
+  ap.k_pages = k_pages;
+  ap.v_pages = v_pages;
+  ap.k_scale = k_scale;
+  ap.v_scale = v_scale;
+  ap.header = reinterpret_cast<bip::WsHeader*>(ws);
+  if (bip::launch_append(p->d, fp8, ap, p->sms, stream) != cudaSuccess) return BIP_ERR_CUDA;
   return BIP_OK;
 }
 

@@ -97,10 +97,40 @@ struct MergeParams {
   float v_scale;
 };
 
-// Kernel launchers (bip_attn.cu / bip_merge.cu).
+// One request with new rows, for the KV append: its rows of k_new / v_new
+// are [tok0, tok0 + q_len) and go to positions pos0 .. pos0 + q_len - 1
+// (pos0 = kv_len - q_len) of the page table starting at kv_indices[page_base].
+// Only requests with q_len > 0, in row order.  16 bytes.
+struct AppendRow {
+  int32_t tok0;
+  int32_t q_len;
+  int32_t pos0;
+  int32_t page_base;
+};
+static_assert(sizeof(AppendRow) == 16, "append row size");
+
+struct AppendParams {
+  const AppendRow* rows;
+  int32_t n_rows;           // entries of rows
+  int32_t total_q;          // new rows
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int32_t num_pages;
+  int64_t page_stride;      // elements (bf16) or bytes (E4M3) between pages
+  const int32_t* kv_indices;
+  const uint16_t* k_new;    // bf16 [total_q, num_kv_heads, head_dim]
+  const uint16_t* v_new;
+  void* k_pages;
+  void* v_pages;
+  float k_scale, v_scale;   // E4M3 pages store e4m3(x / scale)
+  WsHeader* header;
+};
+
+// Kernel launchers (bip_attn.cu / bip_merge.cu / bip_append.cu).
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
                              cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_append(int head_dim, bool kv_fp8, const AppendParams& p, int num_sms, cudaStream_t stream);
 
 }  // namespace bip

@@ -91,6 +91,25 @@ def test_prefill_rejects_before_touching_memory(lib):
     assert lib.bip_prefill(empty._h, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, None, None, 0, None) == 0
 
 
+def test_append_rejects_before_touching_memory(lib):
+    plan = bip.Plan([0, 3], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    fake = ctypes.c_void_p(1 << 20)
+    args = lambda rows, stride=16 * 8 * 128, ks=1.0, vs=1.0, ws=plan.workspace_bytes, kn=fake: (
+        plan._h, kn, fake, rows, fake, fake, 1, stride, fake, ks, vs, fake, ws, None)
+    assert lib.bip_append_kv(*args(4)) == 1                      # row count != qo_indptr[-1]
+    assert lib.bip_append_kv(*args(3, ks=0.5)) == 1              # bf16 pages take no scale
+    assert lib.bip_append_kv(*args(3, stride=16 * 8 * 128 - 8)) == 1
+    assert lib.bip_append_kv(*args(3, kn=ctypes.c_void_p((1 << 20) + 4))) == 1  # misaligned rows
+    assert lib.bip_append_kv(*args(3, ws=64)) == 3               # workspace smaller than the upload
+    f8 = bip.Plan([0, 3], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="fp8_e4m3")
+    for ks in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.bip_append_kv(f8._h, fake, fake, 3, fake, fake, 1, 16 * 8 * 128, fake, ks, 1.0, fake,
+                                 f8.workspace_bytes, None) == 1
+    # nothing to append
+    empty = bip.Plan([0, 0], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    assert lib.bip_append_kv(empty._h, None, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, 0, None) == 0
+
+
 def random_batch(rng, batch, max_kv, ps=16):
     kv_len = rng.integers(1, max_kv + 1, size=batch)
     q_len = np.minimum(kv_len, rng.integers(0, max_kv + 1, size=batch))
