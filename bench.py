@@ -393,6 +393,45 @@ def time_append(b, device, steps: int, warmup: int):
     return e0.elapsed_time(e1) / steps, moved
 
 
+def time_graph(b, device, steps: int, warmup: int):
+    """Device-planned prefill captured in a CUDA graph (buffers sized to b):
+    ms per replay, and whether the replay matches the host-planned result."""
+    import invariant_paged_prefill_gb300 as bip
+    plan = bip.GraphPlan(len(b.q_lens), b.q.shape[0], num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                         head_dim=b.head_dim, page_size=b.page_size, kv_dtype=b.kv_dtype)
+    i32 = dict(dtype=torch.int32, device=device)
+    qo = torch.as_tensor(np.asarray(b.qo_indptr), **i32)
+    kv = torch.as_tensor(np.asarray(b.kv_indptr), **i32)
+    last = torch.as_tensor(np.asarray(b.kv_last_page_len), **i32)
+    out = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[0], b.q.shape[1], dtype=torch.float32, device=device)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=device)
+
+    def launch():
+        bip.prefill_graph(plan, len(b.q_lens), qo, kv, last, b.q, b.k_pages, b.v_pages, b.kv_indices, out, lse, ws)
+
+    launch()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            launch()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, out, lse
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -471,6 +510,15 @@ def run_ours(args):
                            "max_abs_out": float(np.abs(got - ro).max()), "max_abs_lse": float(np.abs(gl - rl).max())},
                 "bit_exact_repeat": repeat_exact, "workspace_bytes": run.plan.workspace_bytes,
                 "source_hash": source_hash()}
+        # device-planned launches replayed from a CUDA graph (fold only, no split)
+        g_ms, g_out, g_lse = time_graph(b, device, args.steps, args.warmup)
+        sg_ms, sg_out, sg_lse = time_graph(sb, device, args.steps, args.warmup)
+        line["graph"] = {
+            "what": "device-planned prefill replayed from a captured CUDA graph (every unit folded in one CTA)",
+            "long_q_tflops": fl / (g_ms * 1e-3) / 1e12,
+            "short_extend_kv_gbs": kvb / (sg_ms * 1e-3) / 1e9,
+            "bit_exact_vs_host_planned": bool(torch.equal(g_out, run.out) and torch.equal(g_lse, run.lse) and
+                                              torch.equal(sg_out, srun.out) and torch.equal(sg_lse, srun.lse))}
         # the paged KV append (the step before attention), timed last: it
         # overwrites the pools of both batches
         a_ms, a_bytes = time_append(b, device, args.steps, args.warmup)

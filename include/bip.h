@@ -198,6 +198,53 @@ bip_status bip_append_kv(bip_plan_t plan, const void* k_new, const void* v_new, 
                          const int32_t* kv_indices, float k_scale, float v_scale, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
+/* ---- graph-replayable launches
+ * A captured CUDA graph fixes its kernels' arguments, so the batch must come
+ * from device memory and the work list must be built on the device (sglang
+ * PR 46351: the full prefill CUDA graph keeps a static q buffer for the
+ * captured token count, Woody-Hu's follow-up; a radix hit and the full
+ * recompute of a prompt usually land in different captured buckets,
+ * jbymy2000's correction).  A graph plan fixes only capacities and shapes;
+ * bip_prefill_graph plans on the device from the indptr arrays each launch
+ * and folds every unit in one CTA.  Since no plan choice enters a row's
+ * arithmetic, the results are the bits of bip_prefill for the same batch,
+ * in any bucket. */
+typedef struct bip_graph_plan_s* bip_graph_plan_t;
+
+/* Capacities: batches of at most max_batch requests with at most
+ * max_total_q q rows in all.  Heads, head_dim, page_size, kv_dtype as for
+ * bip_plan; opts: num_sms, wait_limit_ns and tiles_per_unit apply,
+ * split_policy must not be BIP_SPLIT_ALWAYS.  *workspace_bytes receives the
+ * fixed workspace size.  Host only; no device work. */
+bip_status bip_graph_plan(bip_graph_plan_t* plan, int32_t max_batch, int32_t max_total_q, int32_t num_qo_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t page_size, bip_kv_dtype kv_dtype,
+                          const bip_plan_options* opts, size_t* workspace_bytes);
+
+/* Enqueue a device-planned prefill on `stream` with no host-to-device copy
+ * and no synchronisation: safe to capture in a CUDA graph and replay with
+ * new contents in the same buffers.  DEVICE pointers:
+ *   qo_indptr [batch + 1], kv_indptr [batch + 1], kv_last_page_len [batch]
+ *            int32, read when the launch runs; batch <= max_batch is the
+ *            launch's (host) request count, padding requests may have q_len 0
+ *   q, out   [max_total_q, num_qo_heads, head_dim] bf16 buffers; rows past
+ *            qo_indptr[batch] are not written
+ *   lse      fp32 [max_total_q, num_qo_heads]
+ *   pages, kv_indices, scales as for bip_prefill
+ *   workspace >= the graph plan's workspace_bytes, 256-byte aligned.
+ * Arguments checked on the device (indptr monotone from 0, last-page lengths,
+ * q_len <= kv_len, qo_indptr[batch] <= max_total_q) set the status word to
+ * BIP_ERR_INVALID_ARG and the launch computes nothing; read it with
+ * bip_read_device_status.  The first launch per variant may set a kernel
+ * attribute: make one before capturing. */
+bip_status bip_prefill_graph(bip_graph_plan_t plan, int32_t batch, const int32_t* qo_indptr,
+                             const int32_t* kv_indptr, const int32_t* kv_last_page_len, const void* q,
+                             const void* k_pages, const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                             const int32_t* kv_indices, float k_scale, float v_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Release a graph plan (host memory only). */
+bip_status bip_graph_plan_destroy(bip_graph_plan_t plan);
+
 /* Size of the device array that bip_prefill_no_alloc uses as its workspace. */
 #define BIP_NO_ALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
 

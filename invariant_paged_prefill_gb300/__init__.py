@@ -21,7 +21,8 @@ import numpy as np
 
 from . import _lib
 
-__all__ = ["BipError", "Plan", "prefill", "append_kv", "workspace_bound", "read_device_status", "STATUS"]
+__all__ = ["BipError", "Plan", "prefill", "append_kv", "GraphPlan", "prefill_graph", "workspace_bound",
+           "read_device_status", "STATUS"]
 
 STATUS = {
     0: "BIP_OK", 1: "BIP_ERR_INVALID_ARG", 2: "BIP_ERR_UNSUPPORTED", 3: "BIP_ERR_WORKSPACE_TOO_SMALL",
@@ -198,6 +199,81 @@ def append_kv(plan: Plan, k_new, v_new, k_pages, v_pages, kv_indices, *, workspa
                                    workspace.numel() * workspace.element_size(),
                                    ctypes.c_void_p(stream.cuda_stream)), "bip_append_kv")
     return k_pages, v_pages
+
+
+class GraphPlan:
+    """Capacities and shapes for device-planned, graph-replayable prefills."""
+
+    def __init__(self, max_batch: int, max_total_q: int, *, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                 page_size: int = 16, kv_dtype: str = "bf16", num_sms: int = 0, wait_limit_ns: int = 0,
+                 tiles_per_unit: int = 0):
+        self._lib = _lib.load()
+        self._h = ctypes.c_void_p()
+        opts = _lib.PlanOptions(_POLICY["auto"], 256 << 20, int(num_sms), int(wait_limit_ns), int(tiles_per_unit))
+        ws = ctypes.c_size_t()
+        _check(self._lib.bip_graph_plan(ctypes.byref(self._h), int(max_batch), int(max_total_q), num_qo_heads,
+                                        num_kv_heads, head_dim, page_size, _KV[kv_dtype], ctypes.byref(opts),
+                                        ctypes.byref(ws)), "bip_graph_plan")
+        self.workspace_bytes = int(ws.value)
+        self.max_batch, self.max_total_q = int(max_batch), int(max_total_q)
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+        self.page_size, self.kv_dtype = page_size, kv_dtype
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.bip_graph_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def prefill_graph(plan: GraphPlan, batch: int, qo_indptr, kv_indptr, kv_last_page_len, q, k_pages, v_pages,
+                  kv_indices, out, lse, workspace, *, k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+    """Enqueue a device-planned prefill (capturable in a CUDA graph).
+
+    The indptr arrays are int32 device tensors read when the launch runs;
+    q/out [max_total_q, Hq, d] bf16 and lse [max_total_q, Hq] fp32 are the
+    graph's static buffers.  Results equal ``prefill`` on the same batch.
+    """
+    import torch
+    for name, t, n in (("qo_indptr", qo_indptr, batch + 1), ("kv_indptr", kv_indptr, batch + 1),
+                       ("kv_last_page_len", kv_last_page_len, batch)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n:
+            raise BipError(1, f"{name} must be a contiguous int32 device tensor of at least {n} entries")
+    rows = (plan.max_total_q, plan.num_qo_heads, plan.head_dim)
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or tuple(q.shape) != rows or out.shape != q.shape:
+        raise BipError(1, "q and out must be bf16 [max_total_q, Hq, d]")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != rows[:2]:
+        raise BipError(1, "lse must be fp32 [max_total_q, Hq]")
+    if not (q.is_contiguous() and out.is_contiguous() and lse.is_contiguous()):
+        raise BipError(1, "q, out and lse must be contiguous")
+    if kv_indices.dtype != torch.int32:
+        raise BipError(1, "kv_indices must be int32")
+    want = torch.bfloat16 if plan.kv_dtype == "bf16" else torch.uint8
+    for name, pg in (("k_pages", k_pages), ("v_pages", v_pages)):
+        if pg.dtype != want or pg.dim() != 4 or tuple(pg.shape[1:]) != (plan.page_size, plan.num_kv_heads,
+                                                                        plan.head_dim):
+            raise BipError(1, f"{name} must be [num_pages, page_size, Hkv, d] of {want}")
+        if pg.stride()[1:] != (plan.num_kv_heads * plan.head_dim, plan.head_dim, 1):
+            raise BipError(1, f"{name}: slots and heads must be contiguous inside a page")
+    if k_pages.shape[0] != v_pages.shape[0] or k_pages.stride(0) != v_pages.stride(0):
+        raise BipError(1, "k_pages and v_pages must share page count and stride")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    _check(plan._lib.bip_prefill_graph(plan._h, int(batch), _dev_ptr(qo_indptr, "qo_indptr"),
+                                       _dev_ptr(kv_indptr, "kv_indptr"), _dev_ptr(kv_last_page_len,
+                                                                                  "kv_last_page_len"),
+                                       _dev_ptr(q, "q"), _dev_ptr(k_pages, "k_pages"), _dev_ptr(v_pages, "v_pages"),
+                                       k_pages.shape[0], k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"),
+                                       float(k_scale), float(v_scale), _dev_ptr(out, "out"), _dev_ptr(lse, "lse"),
+                                       _dev_ptr(workspace, "workspace"),
+                                       workspace.numel() * workspace.element_size(),
+                                       ctypes.c_void_p(stream.cuda_stream)), "bip_prefill_graph")
+    return out, lse
 
 
 def read_device_status(workspace, stream=None) -> int:

@@ -208,6 +208,12 @@ __device__ __forceinline__ Geom geom_of(const WorkItem& w, int T) {
   return g;
 }
 
+// Work items of this launch: fixed by the host plan, or counted on the
+// device by the planner kernel that ran before (graph-replayable launches).
+__device__ __forceinline__ int item_count(const AttnParams& p) {
+  return p.n_items_dev ? int(*p.n_items_dev) : p.n_items;
+}
+
 // ------------------------------------------------------------------ roles
 
 // Page id of page `lane` of KV block `blk` (0 for lanes past the block's
@@ -267,7 +273,7 @@ __device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, co
     return true;
   };
 
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x, ++n) {
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int npages_req = (w.kv_len + p.page_size - 1) / p.page_size;
@@ -356,7 +362,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
   uint32_t s_cnt[NT] = {}, pv_cnt[NT] = {};  // blocks whose S / PV was issued, per slot
   int n = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x, ++n) {
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int nb = g.blk_hi - g.blk_lo + 1;
@@ -459,7 +465,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
     return true;
   };
 
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x) {
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     if (!(g.mask >> t & 1)) continue;
@@ -701,7 +707,7 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) 
     constexpr int GROUPS = D / 16;                          // 16-code groups per row
     uint32_t b = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x) {
       const WorkItem w = p.items[it];
       const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
       for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {

@@ -514,6 +514,42 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
+// TMA descriptors of one launch.  q: [rows, Hq, d] as dims (d, Hq, rows); box
+// (64, group, T) = one tile chunk.  pages: [pages, slot, Hkv, d] as dims (d,
+// Hkv, slot, page).  bf16: box (64, 1, page_size, 1), one 128-byte-swizzled
+// chunk of a page.  FP8: box (d, 1, page_size, 1), a whole page row-major,
+// unswizzled (the dequant warps lay out the bf16 operand).
+bool encode_maps(int32_t d, int32_t hq, int32_t hkv, int32_t group, int32_t T, int32_t page_size, bool fp8,
+                 const void* q, int64_t q_rows, const void* k_pages, const void* v_pages, int64_t num_pages,
+                 int64_t page_stride_elems, CUtensorMap* tm_q, CUtensorMap* tm_k, CUtensorMap* tm_v) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  {
+    cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(hq), cuuint64_t(q_rows)};
+    cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(hq) * d * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(T)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const int64_t elem = fp8 ? 1 : 2;
+  for (int which = 0; which < 2; ++which) {
+    const void* base = which == 0 ? k_pages : v_pages;
+    cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(page_size), cuuint64_t(num_pages)};
+    cuuint64_t strides[3] = {cuuint64_t(d) * elem, cuuint64_t(hkv) * d * elem, cuuint64_t(page_stride_elems) * elem};
+    cuuint32_t box[4] = {fp8 ? cuuint32_t(d) : 64u, 1, cuuint32_t(page_size), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (encode(which == 0 ? tm_k : tm_v, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const void* k_pages,
                                   const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
                                   const int32_t* kv_indices, float k_scale, float v_scale, void* out, float* lse,
@@ -532,38 +568,11 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
     return BIP_ERR_INVALID_ARG;
   if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return BIP_ERR_INVALID_ARG;
 
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (!encode) return BIP_ERR_CUDA;
-
-  // q: [rows, Hq, d] as dims (d, Hq, rows); box (64, group, T) = one tile chunk.
-  CUtensorMap tm_q, tm_k, tm_v;
-  {
-    cuuint64_t dims[3] = {cuuint64_t(p->d), cuuint64_t(p->hq), cuuint64_t(num_q_rows)};
-    cuuint64_t strides[2] = {cuuint64_t(p->d) * 2, cuuint64_t(p->hq) * p->d * 2};
-    cuuint32_t box[3] = {64, cuuint32_t(p->group), cuuint32_t(p->T)};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return BIP_ERR_CUDA;
-  }
-  // pages: [pages, slot, Hkv, d] as dims (d, Hkv, slot, page).  bf16: box (64, 1, page_size, 1), one
-  // 128-byte-swizzled chunk of a page.  FP8: box (d, 1, page_size, 1), a whole page row-major, unswizzled
-  // (the dequant warps lay out the bf16 operand).
   const bool fp8 = p->kv_dtype == BIP_KV_FP8_E4M3;
-  for (int which = 0; which < 2; ++which) {
-    const void* base = which == 0 ? k_pages : v_pages;
-    cuuint64_t dims[4] = {cuuint64_t(p->d), cuuint64_t(p->hkv), cuuint64_t(p->page_size), cuuint64_t(num_pages)};
-    cuuint64_t strides[3] = {cuuint64_t(p->d) * elem, cuuint64_t(p->hkv) * p->d * elem,
-                             cuuint64_t(page_stride_elems) * elem};
-    cuuint32_t box[4] = {fp8 ? cuuint32_t(p->d) : 64u, 1, cuuint32_t(p->page_size), 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    if (encode(which == 0 ? &tm_k : &tm_v, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-               4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return BIP_ERR_CUDA;
-  }
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_maps(p->d, p->hq, p->hkv, p->group, p->T, p->page_size, fp8, q, num_q_rows, k_pages, v_pages,
+                   num_pages, page_stride_elems, &tm_q, &tm_k, &tm_v))
+    return BIP_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemcpyAsync(ws, p->upload, p->upload_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
@@ -572,6 +581,7 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   bip::AttnParams ap;
   ap.items = reinterpret_cast<const WorkItem*>(ws + p->off_items);
   ap.n_items = int32_t(p->items.size());
+  ap.n_items_dev = nullptr;
   ap.num_qo_heads = p->hq;
   ap.group = p->group;
   ap.tile_pos = p->T;
@@ -650,6 +660,154 @@ extern "C" bip_status bip_append_kv(bip_plan_t p, const void* k_new, const void*
   ap.v_scale = v_scale;
   ap.header = reinterpret_cast<bip::WsHeader*>(ws);
   if (bip::launch_append(p->d, fp8, ap, p->sms, stream) != cudaSuccess) return BIP_ERR_CUDA;
+  return BIP_OK;
+}
+
+// ------------------------------------------------------------ graph plans
+
+struct bip_graph_plan_s {
+  int32_t max_batch = 0, max_total_q = 0, hq = 0, hkv = 0, d = 0, page_size = 0, group = 0, T = 0, nt = 1;
+  int32_t grid = 0, capacity = 0;
+  bip_kv_dtype kv_dtype = BIP_KV_BF16;
+  uint64_t wait_limit_cycles = 0;
+  size_t off_items = 0, off_scratch = 0, ws_bytes = 0;
+};
+
+extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_batch, int32_t max_total_q,
+                                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                     bip_kv_dtype kv_dtype, const bip_plan_options* opts_in,
+                                     size_t* workspace_bytes) {
+  if (!plan_out) return BIP_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  if (max_batch < 0 || max_total_q < 0) return BIP_ERR_INVALID_ARG;
+  bip_status st = check_heads(num_qo_heads, num_kv_heads, head_dim);
+  if (st != BIP_OK) return st;
+  if (kv_dtype != BIP_KV_BF16 && kv_dtype != BIP_KV_FP8_E4M3) return BIP_ERR_INVALID_ARG;
+  const int32_t bn = bip::kv_block_for(head_dim);
+  if (page_size <= 0) return BIP_ERR_INVALID_ARG;
+  if ((page_size & (page_size - 1)) != 0 || page_size < 8 || page_size > bn) return BIP_ERR_UNSUPPORTED;
+  bip_plan_options opts;
+  opts.split_policy = BIP_SPLIT_AUTO;
+  opts.split_budget_bytes = kDefaultSplitBudget;
+  opts.num_sms = 0;
+  opts.wait_limit_ns = 0;
+  opts.tiles_per_unit = 0;
+  if (opts_in) opts = *opts_in;
+  if (opts.split_policy == BIP_SPLIT_ALWAYS) return BIP_ERR_UNSUPPORTED;  // graph launches fold every unit
+  if (opts.split_policy != BIP_SPLIT_AUTO && opts.split_policy != BIP_SPLIT_NEVER) return BIP_ERR_INVALID_ARG;
+  if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
+  if (opts.tiles_per_unit < 0 || opts.tiles_per_unit > bip::max_tiles_per_unit_for(head_dim))
+    return BIP_ERR_INVALID_ARG;
+  if (kv_dtype == BIP_KV_FP8_E4M3 && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
+  if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
+
+  bip_graph_plan_s* p = new (std::nothrow) bip_graph_plan_s;
+  if (!p) return BIP_ERR_OUT_OF_MEMORY;
+  p->max_batch = max_batch;
+  p->max_total_q = max_total_q;
+  p->hq = num_qo_heads;
+  p->hkv = num_kv_heads;
+  p->d = head_dim;
+  p->page_size = page_size;
+  p->kv_dtype = kv_dtype;
+  p->group = num_qo_heads / num_kv_heads;
+  p->T = bip::kTileRows / p->group;
+  // No batch statistics at capture time: two tiles per CTA wherever the
+  // variant exists (numerically neutral, like every plan choice).
+  p->nt = opts.tiles_per_unit ? opts.tiles_per_unit
+                              : (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 ? 2 : 1);
+  int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
+  p->grid = std::min(num_sms, bip::kMaxCtas);
+  {
+    const uint64_t ns = opts.wait_limit_ns, khz = query_clock_khz();
+    p->wait_limit_cycles = ns > (~0ull / khz) ? ~0ull : std::max<uint64_t>(1, ns * khz / 1000000ull);
+  }
+  // A request with q_len rows touches at most ceil(q_len / T) + 1 tiles.
+  const int64_t cap = int64_t(num_kv_heads) * ((int64_t(max_total_q) + p->T - 1) / p->T + 2 * int64_t(max_batch));
+  if (cap > INT32_MAX) {
+    delete p;
+    return BIP_ERR_UNSUPPORTED;
+  }
+  p->capacity = int32_t(cap);
+  p->off_items = bip::kHeaderBytes;
+  p->off_scratch = align_up(p->off_items + size_t(cap) * sizeof(WorkItem), 256);
+  p->ws_bytes = align_up(p->off_scratch + size_t(p->grid) * p->nt * bip::kTileRows * head_dim * sizeof(float), 256);
+  *plan_out = p;
+  if (workspace_bytes) *workspace_bytes = p->ws_bytes;
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_graph_plan_destroy(bip_graph_plan_t p) {
+  delete p;
+  return BIP_OK;
+}
+
+extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t* qo_indptr,
+                                        const int32_t* kv_indptr, const int32_t* kv_last_page_len, const void* q,
+                                        const void* k_pages, const void* v_pages, int64_t num_pages,
+                                        int64_t page_stride_elems, const int32_t* kv_indices, float k_scale,
+                                        float v_scale, void* out, float* lse, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  if (!p) return BIP_ERR_INVALID_ARG;
+  if (batch < 0 || batch > p->max_batch) return BIP_ERR_INVALID_ARG;
+  if (!qo_indptr || !kv_indptr || !kv_last_page_len || !q || !k_pages || !v_pages || !kv_indices || !out || !lse ||
+      !workspace)
+    return BIP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return BIP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return BIP_ERR_INVALID_ARG;
+  if (workspace_bytes < p->ws_bytes) return BIP_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t page_elems = int64_t(p->page_size) * p->hkv * p->d;
+  const bool fp8 = p->kv_dtype == BIP_KV_FP8_E4M3;
+  const int64_t elem = fp8 ? 1 : 2;
+  if (num_pages <= 0 || num_pages > INT32_MAX || page_stride_elems < page_elems ||
+      (page_stride_elems * elem) % 16 != 0)
+    return BIP_ERR_INVALID_ARG;
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return BIP_ERR_INVALID_ARG;
+  if (p->max_total_q == 0) return BIP_OK;  // no buffer rows: nothing can ever run
+
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_maps(p->d, p->hq, p->hkv, p->group, p->T, p->page_size, fp8, q, p->max_total_q, k_pages, v_pages,
+                   num_pages, page_stride_elems, &tm_q, &tm_k, &tm_v))
+    return BIP_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  bip::WsHeader* header = reinterpret_cast<bip::WsHeader*>(ws);
+  bip::DevPlanParams dp;
+  dp.batch = batch;
+  dp.max_total_q = p->max_total_q;
+  dp.page_size = p->page_size;
+  dp.group = p->group;
+  dp.tile_pos = p->T;
+  dp.tiles_per_unit = p->nt;
+  dp.num_kv_heads = p->hkv;
+  dp.capacity = p->capacity;
+  dp.qo_indptr = qo_indptr;
+  dp.kv_indptr = kv_indptr;
+  dp.kv_last_page_len = kv_last_page_len;
+  dp.items = reinterpret_cast<WorkItem*>(ws + p->off_items);
+  dp.header = header;
+  if (bip::launch_device_plan(dp, stream) != cudaSuccess) return BIP_ERR_CUDA;
+
+  bip::AttnParams ap;
+  ap.items = dp.items;
+  ap.n_items = p->capacity;
+  ap.n_items_dev = &header->n_items;
+  ap.num_qo_heads = p->hq;
+  ap.group = p->group;
+  ap.tile_pos = p->T;
+  ap.page_size = p->page_size;
+  ap.num_pages = int32_t(num_pages);
+  ap.kv_indices = kv_indices;
+  ap.out = static_cast<uint16_t*>(out);
+  ap.lse = lse;
+  ap.partials = nullptr;  // every item folds its segments
+  ap.scratch = reinterpret_cast<float*>(ws + p->off_scratch);
+  ap.header = header;
+  ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
+  ap.v_scale = v_scale;
+  ap.wait_limit_cycles = p->wait_limit_cycles;
+  if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
+    return BIP_ERR_CUDA;
   return BIP_OK;
 }
 

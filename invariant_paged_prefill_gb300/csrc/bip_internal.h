@@ -24,7 +24,8 @@ struct WsHeader {
   uint32_t status;          // 0 = ok, else a bip_status code
   uint32_t where;           // which wait expired (diagnostics)
   uint32_t bad_pages;       // count of out-of-range page ids seen
-  uint32_t reserved[61];
+  uint32_t n_items;         // work items, when the device planner wrote them
+  uint32_t reserved[60];
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
 
@@ -69,6 +70,7 @@ static_assert(sizeof(MergeUnit) == 32, "merge unit size");
 struct AttnParams {
   const WorkItem* items;
   int32_t n_items;
+  const uint32_t* n_items_dev;  // if set, the item count is read here (device-planned launches)
   int32_t num_qo_heads;
   int32_t group;        // q heads per kv head
   int32_t tile_pos;     // T = floor(128 / group)
@@ -126,11 +128,33 @@ struct AppendParams {
   WsHeader* header;
 };
 
-// Kernel launchers (bip_attn.cu / bip_merge.cu / bip_append.cu).
+// Device-side planner for graph-replayable launches: reads the batch's
+// indptr arrays on the device and writes the fold-only work list (every
+// unit one item over all its segments; no partials, no merge kernel) and
+// its count into the workspace header.  Validation failures set the header
+// status and leave zero items.
+struct DevPlanParams {
+  int32_t batch;
+  int32_t max_total_q;   // q rows the buffers hold
+  int32_t page_size;
+  int32_t group;         // q heads per kv head
+  int32_t tile_pos;      // T
+  int32_t tiles_per_unit;
+  int32_t num_kv_heads;
+  int32_t capacity;      // work items the workspace holds
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* kv_last_page_len;
+  WorkItem* items;
+  WsHeader* header;
+};
+
+// Kernel launchers (bip_attn.cu / bip_merge.cu / bip_append.cu / bip_plan_dev.cu).
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
                              cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int head_dim, bool kv_fp8, const AppendParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_device_plan(const DevPlanParams& p, cudaStream_t stream);
 
 }  // namespace bip

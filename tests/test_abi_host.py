@@ -110,6 +110,26 @@ def test_append_rejects_before_touching_memory(lib):
     assert lib.bip_append_kv(empty._h, None, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, 0, None) == 0
 
 
+def test_graph_plan_validation_and_sizes(lib):
+    gp = bip.GraphPlan(8, 4096, num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    # the fixed workspace holds the worst-case work list and every CTA's fold state
+    assert gp.workspace_bytes >= 256 + 8 * (4096 // 32 + 16) * 48
+    fake = ctypes.c_void_p(1 << 20)
+    args = lambda batch, ws=gp.workspace_bytes, q=fake: (gp._h, batch, fake, fake, fake, q, fake, fake, 1,
+                                                         16 * 8 * 128, fake, 1.0, 1.0, fake, fake, fake, ws, None)
+    assert lib.bip_prefill_graph(*args(9)) == 1                     # more requests than the capacity
+    assert lib.bip_prefill_graph(*args(-1)) == 1
+    assert lib.bip_prefill_graph(*args(8, ws=gp.workspace_bytes - 1)) == 3
+    assert lib.bip_prefill_graph(*args(8, q=ctypes.c_void_p((1 << 20) + 2))) == 1
+    with pytest.raises(bip.BipError):
+        bip.GraphPlan(8, 4096, num_qo_heads=32, num_kv_heads=8, head_dim=96)
+    opts = _lib.PlanOptions(2, 1 << 20, 0, 0, 0)   # BIP_SPLIT_ALWAYS: graph launches fold
+    h = ctypes.c_void_p()
+    assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 0, ctypes.byref(opts), None) == 2
+    opts = _lib.PlanOptions(0, 1 << 20, 0, 0, 2)   # FP8 pages use the one-tile variant
+    assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 1, ctypes.byref(opts), None) == 2
+
+
 def random_batch(rng, batch, max_kv, ps=16):
     kv_len = rng.integers(1, max_kv + 1, size=batch)
     q_len = np.minimum(kv_len, rng.integers(0, max_kv + 1, size=batch))
