@@ -529,7 +529,7 @@ def run_ours(args):
                         f"{heads[1]} x {heads[2]}) into the long_q pools",
             "value": a_gbs, "unit": "GB/s", "ms_per_step": a_ms,
             "roofline": {"bound": "hbm", "achieved": a_gbs, "peak": hbm, "unit": "GB/s", "frac": a_gbs / hbm,
-                         "peak_source": f"hbm_gbs of {peak_kind}"},
+                         "peak_source": f"hbm_gbs of {peak_kind}", "traffic": recorded_traffic("append")},
             "short_extend_us": sa_ms * 1e3}
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -543,6 +543,14 @@ def run_profile(args):
     from invariant_paged_prefill_gb300 import build as B
     B.ensure_built()
     device = torch.device("cuda:0")
+    if args.workload == "append":  # the paged KV append of every long_q row
+        heads, batch, q_len, kv_len = WORKLOADS["long_q"]
+        batch = args.batch or batch
+        b = make_batch(heads, batch, q_len, kv_len, device)
+        ms, moved = time_append(b, device, args.steps, args.warmup)
+        print(json.dumps({"profile": "append", "batch": batch, "ms": ms, "gbs": moved / ms / 1e6,
+                          "source_hash": source_hash()}), flush=True)
+        return
     heads, batch, q_len, kv_len = WORKLOADS[args.workload]
     batch = args.batch or batch
     b = make_batch(heads, batch, q_len, kv_len, device)
@@ -589,7 +597,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long_q")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["append"], default="long_q",
+                    help="append: with --profile only, the paged KV append of the long_q rows")
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--profile", action="store_true", help="time only the main step (for ncu captures)")
