@@ -81,6 +81,18 @@ def visible_keys(position: int) -> int:
     return position + 1
 
 
+def first_visible_key(position: int, window_left: int = 0) -> int:
+    """First key a row at ``position`` attends to.
+
+    Without a window (``window_left`` 0) every earlier key is visible.  With
+    a sliding window of ``window_left`` keys to the left of the diagonal,
+    the row sees keys ``position - window_left .. position`` (sliding-window
+    KV pools are among the cases the padding skips, sglang PR 46351, "Fix"),
+    clipped at 0.
+    """
+    return 0 if window_left <= 0 else max(0, position - window_left)
+
+
 def gather_request_kv(pages: np.ndarray, kv_indices: Sequence[int], page_lo: int, kv_len: int,
                       page_size: int) -> np.ndarray:
     """Keys (or values) ``[kv_len, num_kv_heads, head_dim]`` of one request, token order.
@@ -99,8 +111,8 @@ def gather_request_kv(pages: np.ndarray, kv_indices: Sequence[int], page_lo: int
 
 
 def attend_rows(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, positions: np.ndarray,
-                sm_scale: float) -> tuple[np.ndarray, np.ndarray]:
-    """Causal softmax attention of some rows against one head's keys.
+                sm_scale: float, window_left: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """Causal (optionally sliding-window) softmax attention of some rows against one head's keys.
 
     q_rows ``[n, d]``, keys/values ``[kv_len, d]``, positions ``[n]``.
     Returns out ``[n, d]`` and natural-log lse ``[n]`` in float64.
@@ -108,6 +120,7 @@ def attend_rows(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, positi
     scores = (q_rows @ keys.T) * sm_scale                       # [n, kv_len]
     kv_idx = np.arange(keys.shape[0])[None, :]
     visible = kv_idx < np.array([visible_keys(int(p)) for p in positions])[:, None]
+    visible &= kv_idx >= np.array([first_visible_key(int(p), window_left) for p in positions])[:, None]
     scores = np.where(visible, scores, -np.inf)
     m = scores.max(axis=1, keepdims=True)
     w = np.exp(scores - m)                                       # masked entries -> 0
@@ -132,7 +145,7 @@ def paged_prefill(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, kv_last
                   num_qo_heads: int, num_kv_heads: int, page_size: int, *,
                   q_kind: str = "f64", kv_kind: str = "f64", k_scale: float = 1.0,
                   v_scale: float = 1.0, sm_scale: float | None = None,
-                  rows: Iterable[int] | None = None, row_chunk: int = 512):
+                  rows: Iterable[int] | None = None, row_chunk: int = 512, window_left: int = 0):
     """Reference output and lse of paged causal GQA prefill.
 
     q ``[total_tokens, num_qo_heads, head_dim]``; k_pages/v_pages
@@ -141,6 +154,7 @@ def paged_prefill(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, kv_last
 
     ``rows`` restricts the computation to the listed token rows (all rows when
     None); the returned arrays then hold those rows in the order given.
+    ``window_left`` > 0 restricts each row to its last window_left + 1 keys.
     Returns ``(out [n, num_qo_heads, head_dim], lse [n, num_qo_heads])``.
     """
     q_raw = np.asarray(q)
@@ -178,7 +192,8 @@ def paged_prefill(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, kv_last
             q_rows = _as_f64(q_raw[toks], q_kind)          # decode only the rows used
             for h in range(hq):
                 hk = kv_head_of(h, num_qo_heads, num_kv_heads)
-                o, s = attend_rows(q_rows[:, h, :], keys[:last, hk, :], vals[:last, hk, :], pos, sm_scale)
+                o, s = attend_rows(q_rows[:, h, :], keys[:last, hk, :], vals[:last, hk, :], pos, sm_scale,
+                                   window_left)
                 idx = [order[t] for t in toks]
                 out[idx, h, :] = o
                 lse[idx, h] = s

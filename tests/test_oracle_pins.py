@@ -294,7 +294,7 @@ def test_planted_mistake_is_caught(name, monkeypatch):
         monkeypatch.setattr(pa, "gather_request_kv", _wrong_gather)
     elif name == "scale_squared":
         real = pa.attend_rows
-        monkeypatch.setattr(pa, "attend_rows", lambda q, k, v, p, s: real(q, k, v, p, s * s))
+        monkeypatch.setattr(pa, "attend_rows", lambda q, k, v, p, s, *rest: real(q, k, v, p, s * s, *rest))
     else:
         attr, fn = MUTATIONS[name]
         monkeypatch.setattr(pa, attr, fn)
@@ -303,3 +303,89 @@ def test_planted_mistake_is_caught(name, monkeypatch):
     except (ValueError, IndexError):
         caught = True  # a mistake that breaks the shapes is caught as well
     assert caught, f"planted mistake {name} went unnoticed"
+
+
+# --------------------------------------------------------------------------
+# sliding window
+# --------------------------------------------------------------------------
+
+def sdpa_window_reference(q, k, v, q_len, window_left):
+    """Library attention with a banded mask: row at position p sees keys p - W .. p."""
+    kv_len = k.shape[0]
+    pos = torch.arange(q_len)[:, None] + (kv_len - q_len)
+    key = torch.arange(kv_len)[None, :]
+    mask = (key <= pos) & (key >= pos - window_left)
+    qt = torch.from_numpy(q).permute(1, 0, 2)[None]
+    kt = torch.from_numpy(k).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(v).permute(1, 0, 2)[None]
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, enable_gqa=True)
+    g = q.shape[1] // k.shape[1]
+    kr = kt.repeat_interleave(g, dim=1)
+    scores = (qt @ kr.transpose(-1, -2)) / math.sqrt(q.shape[2])
+    lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1)
+    return out[0].permute(1, 0, 2).numpy(), lse[0].permute(1, 0).numpy()
+
+
+@pytest.mark.parametrize("window", [1, 3, 8, 40])
+def test_oracle_window_matches_library_banded_mask(window):
+    specs, hq, hkv, d, ps = [(7, 7), (3, 11), (1, 5), (5, 30), (12, 50)], 8, 2, 16, 4
+    qs, ks, vs = random_requests(specs, hq, hkv, d, seed=77)
+    args = paged_from_dense(qs, ks, vs, page_size=ps, seed=5)
+    out, lse = pa.paged_prefill(**args, window_left=window)
+    row = 0
+    for q, k, v, (ql, kl) in zip(qs, ks, vs, specs):
+        ro, rl = sdpa_window_reference(q, k, v, ql, window)
+        assert _err(out[row:row + ql] - ro) < TOL and _err(lse[row:row + ql] - rl) < TOL
+        row += ql
+
+
+def test_oracle_window_closed_forms():
+    # window 1 over keys of one value channel: a row sees exactly keys p-1 and p;
+    # with q = 0 the output is their mean and lse = ln 2 (one key at p = 0: lse 0).
+    hq, hkv, d, n = 4, 1, 8, 9
+    q = np.zeros((n, hq, d))
+    k = np.random.default_rng(1).standard_normal((n, hkv, d))
+    v = np.zeros((n, hkv, d))
+    v[:, 0, 0] = np.arange(n, dtype=np.float64)
+    args = paged_from_dense([q], [k], [v], page_size=4, seed=2)
+    out, lse = pa.paged_prefill(**args, window_left=1)
+    want = np.array([0.0] + [p - 0.5 for p in range(1, n)])
+    assert _err(out[:, 0, 0] - want) < TOL
+    assert _err(lse[0]) < TOL and _err(lse[1:] - math.log(2)) < TOL
+    # a window at least as long as the sequence is plain causal attention
+    o2, l2 = pa.paged_prefill(**args, window_left=n)
+    o3, l3 = pa.paged_prefill(**args)
+    assert np.array_equal(o2, o3) and np.array_equal(l2, l3)
+
+
+def test_oracle_window_extend_rows_equal_full_rows():
+    specs, hq, hkv, d = [(40, 40)], 4, 2, 8
+    qs, ks, vs = random_requests(specs, hq, hkv, d, seed=9)
+    full = paged_from_dense(qs, ks, vs, page_size=4, seed=1)
+    ext = paged_from_dense([qs[0][30:]], ks, vs, page_size=4, seed=1)
+    fo, fl = pa.paged_prefill(**full, window_left=6)
+    eo, el = pa.paged_prefill(**ext, window_left=6)
+    assert np.array_equal(eo, fo[30:]) and np.array_equal(el, fl[30:])
+
+
+def window_sdpa_error(window: int) -> float:
+    specs, hq, hkv, d, ps = [(7, 7), (3, 11), (5, 30), (12, 50)], 8, 2, 16, 4
+    qs, ks, vs = random_requests(specs, hq, hkv, d, seed=78)
+    args = paged_from_dense(qs, ks, vs, page_size=ps, seed=6)
+    out, lse = pa.paged_prefill(**args, window_left=window)
+    worst, row = 0.0, 0
+    for q, k, v, (ql, kl) in zip(qs, ks, vs, specs):
+        ro, rl = sdpa_window_reference(q, k, v, ql, window)
+        worst = max(worst, _err(out[row:row + ql] - ro), _err(lse[row:row + ql] - rl))
+        row += ql
+    return worst
+
+
+@pytest.mark.parametrize("mistake", ["one_short", "one_long", "ignored"])
+def test_planted_window_mistake_is_caught(mistake, monkeypatch):
+    real = pa.first_visible_key
+    wrong = {"one_short": lambda p, w=0: real(p, w) + (1 if w > 0 and p - w >= 0 else 0),
+             "one_long": lambda p, w=0: max(0, real(p, w) - 1),
+             "ignored": lambda p, w=0: 0}[mistake]
+    monkeypatch.setattr(pa, "first_visible_key", wrong)
+    assert window_sdpa_error(5) > TOL, f"planted window mistake {mistake} went unnoticed"
