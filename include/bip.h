@@ -82,6 +82,9 @@ typedef struct bip_plan_options {
                                     runs proportionally longer before it gives up */
   int32_t tiles_per_unit;        /* q tiles per CTA: 0 = auto, 1, or 2 (head_dim 128 only);
                                     numerically neutral (tested) */
+  int32_t window_left;           /* sliding window: 0 = none (every earlier key is visible);
+                                    W > 0: the row at position p sees keys p - W .. p only
+                                    (sliding-window KV, a mask case of sglang PR 46351, "Fix") */
 } bip_plan_options;
 
 typedef struct bip_plan_info {

@@ -66,7 +66,7 @@ class Plan:
     def __init__(self, qo_indptr, kv_indptr, kv_last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                  head_dim: int, page_size: int = 16, kv_dtype: str = "bf16", split_policy: str = "auto",
                  split_budget_bytes: int = 256 << 20, num_sms: int = 0, wait_limit_ns: int = 0,
-                 tiles_per_unit: int = 0):
+                 tiles_per_unit: int = 0, window_left: int = 0):
         self._lib = _lib.load()
         self._h = ctypes.c_void_p()
         qo, kv, last = _i32_array(qo_indptr), _i32_array(kv_indptr), _i32_array(kv_last_page_len)
@@ -74,7 +74,7 @@ class Plan:
         if batch < 0 or len(kv) != batch + 1 or len(last) != batch:
             raise BipError(1, "indptr lengths disagree")
         opts = _lib.PlanOptions(_POLICY[split_policy], int(split_budget_bytes), int(num_sms), int(wait_limit_ns),
-                                int(tiles_per_unit))
+                                int(tiles_per_unit), int(window_left))
         ws = ctypes.c_size_t()
         _check(self._lib.bip_plan(ctypes.byref(self._h), _ptr(qo), _ptr(kv), _ptr(last) if batch else None,
                                   batch, num_qo_heads, num_kv_heads, head_dim, page_size, _KV[kv_dtype],
@@ -206,10 +206,11 @@ class GraphPlan:
 
     def __init__(self, max_batch: int, max_total_q: int, *, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                  page_size: int = 16, kv_dtype: str = "bf16", num_sms: int = 0, wait_limit_ns: int = 0,
-                 tiles_per_unit: int = 0):
+                 tiles_per_unit: int = 0, window_left: int = 0):
         self._lib = _lib.load()
         self._h = ctypes.c_void_p()
-        opts = _lib.PlanOptions(_POLICY["auto"], 256 << 20, int(num_sms), int(wait_limit_ns), int(tiles_per_unit))
+        opts = _lib.PlanOptions(_POLICY["auto"], 256 << 20, int(num_sms), int(wait_limit_ns), int(tiles_per_unit),
+                                int(window_left))
         ws = ctypes.c_size_t()
         _check(self._lib.bip_graph_plan(ctypes.byref(self._h), int(max_batch), int(max_total_q), num_qo_heads,
                                         num_kv_heads, head_dim, page_size, _KV[kv_dtype], ctypes.byref(opts),

@@ -21,7 +21,7 @@ P_i32 = ctypes.POINTER(ctypes.c_int32)
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("split_policy", ctypes.c_int), ("split_budget_bytes", c_size), ("num_sms", c_i32),
-                ("wait_limit_ns", c_u64), ("tiles_per_unit", c_i32)]
+                ("wait_limit_ns", c_u64), ("tiles_per_unit", c_i32), ("window_left", c_i32)]
 
 
 class PlanInfo(ctypes.Structure):

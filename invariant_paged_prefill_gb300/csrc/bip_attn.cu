@@ -38,6 +38,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <type_traits>
 
 #include "bip_internal.h"
@@ -203,7 +204,7 @@ __device__ __forceinline__ Geom geom_of(const WorkItem& w, int T) {
       unit_end = g.tile_end[t];
     }
   }
-  g.blk_lo = w.seg_lo * (kSplitLen / BN);
+  g.blk_lo = max(int(w.seg_lo) * (kSplitLen / BN), w.blk_min);  // a sliding window starts mid-segment
   g.blk_hi = min((int(w.seg_hi) + 1) * kSplitLen - 1, unit_end) / BN;
   return g;
 }
@@ -410,7 +411,9 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
       const uint32_t vb = gb + j;
       const int vslot = vb % ST;
       const int blk = g.blk_lo + j;
-      const bool first_in_seg = (blk % C::BPS) == 0;
+      // O starts afresh at a segment's first visited block (a block boundary
+      // of the segment grid, or the item's first block under a window)
+      const bool first_in_seg = (blk % C::BPS) == 0 || j == 0;
       bool v_ready = false;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
@@ -445,7 +448,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
   drain_wait(bar(c, B_DRAIN), 0);
 }
 
-template <int D, int NT, int ST, bool KV8>
+template <int D, int NT, int ST, bool KV8, bool WIN>
 __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t) {
   using C = Cfg<D, NT, ST, KV8>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -479,15 +482,19 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
     const uint32_t o_addr = t_lane + C::tm_o(t);
 
     for (int s = w.seg_lo; s <= w.seg_hi && ok; ++s) {
-      const int sb_lo = s * C::BPS;
+      const int sb_lo = max(s * C::BPS, g.blk_lo);
       const int sb_hi = min((s + 1) * C::BPS - 1, g.blk_hi);
       float m = -INFINITY, l = 0.f;  // running raw-score max (possibly stale) and sum over this segment
-      for (int blk = sb_lo; blk <= sb_hi; ++blk, ++cnt) {
+      bool seg_first = true;  // first block of this segment: O is overwritten, never rescaled
+      for (int blk = sb_lo; blk <= sb_hi; ++blk, ++cnt, seg_first = false) {
         const int sbuf = cnt % C::NS;
         if (!wait_warp(c, bar(c, B_S_FULL + 2 * t + sbuf), (cnt / C::NS) & 1, 21)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = t_lane + C::tm_s(t, sbuf);
-        const int lim = valid ? pos - blk * C::BN : -1;  // columns 0..lim are visible
+        // Columns lo..lim are visible: keys up to the row's position, and
+        // with a sliding window none before position - window_left.
+        const int lim = valid ? pos - blk * C::BN : -1;
+        const int lo = WIN ? pos - p.window_left - blk * C::BN : INT_MIN / 2;
 
         // Blocks wholly visible to every valid row of the warp skip the
         // per-column mask (same values for those rows, fewer instructions).
@@ -499,13 +506,13 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // the arithmetic but still stores P = 0: its rows may be valid rows
         // past whose position the block lies, and their O keeps accumulating
         // P V.
-        const bool whole = __all_sync(0xffffffffu, !valid || lim >= C::BN - 1);
-        const bool live = __any_sync(0xffffffffu, lim >= 0);
+        const bool whole = __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (!WIN || lo <= 0)));
+        const bool live = __any_sync(0xffffffffu, lim >= 0 && (!WIN || lo < C::BN));
 
-        // Block max.  One TMEM round trip for the whole S row; with fewer than
-        // 248 registers a thread S is then reread in two halves for the
-        // exponentials instead of keeping the row live (which would spill).
-        constexpr bool kHalves = C::SM_REGS < 248 && C::BN == 128;
+        // Block max.  One TMEM round trip for the whole S row; a 128-column
+        // row is then reread in two halves for the exponentials instead of
+        // being kept live (which spills even at 255 registers a thread).
+        constexpr bool kHalves = C::BN == 128;
         constexpr int HW = kHalves ? C::BN / 2 : C::BN;  // columns per exp pass
         float mx = -INFINITY;
         uint32_t sv[C::BN];
@@ -521,8 +528,8 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           for (int j = 0; j < C::BN; j += 2) {
             float a = __uint_as_float(sv[j]), b = __uint_as_float(sv[j + 1]);
             if (!kWhole) {
-              a = j <= lim ? a : -INFINITY;
-              b = j + 1 <= lim ? b : -INFINITY;
+              a = (j <= lim && (!WIN || j >= lo)) ? a : -INFINITY;
+              b = (j + 1 <= lim && (!WIN || j + 1 >= lo)) ? b : -INFINITY;
             }
             m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], a, b);
           }
@@ -575,7 +582,9 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                 uint64_t e;
                 if (kFmaPairs >> pair & 1) e = ex2_fma2(x);
                 else e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
-                if (!kWhole) e = f2_bits(cu <= lim ? f2_lo(e) : 0.f, cu + 1 <= lim ? f2_hi(e) : 0.f);
+                if (!kWhole)
+                  e = f2_bits((cu <= lim && (!WIN || cu >= lo)) ? f2_lo(e) : 0.f,
+                              (cu + 1 <= lim && (!WIN || cu + 1 >= lo)) ? f2_hi(e) : 0.f);
                 acc[pair & 3] = fadd2(acc[pair & 3], e);
                 hv[j / 2] = pack_bf16x2(f2_lo(e), f2_hi(e));
               }
@@ -597,7 +606,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // Rescale O where the running max moved (alpha is exactly 1 elsewhere);
         // the first block of a segment overwrites O instead.  With one S
         // buffer the S_FULL phase already implies the previous PV completed.
-        if ((blk % C::BPS) != 0 && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
+        if (!seg_first && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
           if (C::NS == 2 && !wait_pv(cnt - 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
@@ -753,7 +762,7 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) 
   }
 }
 
-template <int D, int NT, int ST, bool KV8>
+template <int D, int NT, int ST, bool KV8, bool WIN>
 __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
     bip_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -810,7 +819,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   if (warp < C::SM_WARPS) {
     if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
-    softmax_role<D, NT, ST, KV8>(c, tmem, p, warp / 4);
+    softmax_role<D, NT, ST, KV8, WIN>(c, tmem, p, warp / 4);
   } else if (warp < C::CTL_WARP0) {
     dequant_role<D, NT, ST, KV8>(c, sbase, p);
   } else {
@@ -836,19 +845,28 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
   if (warp == C::CTL_WARP0 + 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-template <int D, int NT, int ST, bool KV8>
-cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                   int grid, cudaStream_t stream) {
+// The sliding-window mask is a separate instantiation, so that the plain
+// causal kernel carries none of its arithmetic.
+template <int D, int NT, int ST, bool KV8, bool WIN>
+cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                       int grid, cudaStream_t stream) {
   using C = Cfg<D, NT, ST, KV8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D, NT, ST, KV8>,
+    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D, NT, ST, KV8, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  bip_attn_kernel<D, NT, ST, KV8><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  bip_attn_kernel<D, NT, ST, KV8, WIN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+template <int D, int NT, int ST, bool KV8>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                   int grid, cudaStream_t stream) {
+  return p.window_left > 0 ? launch_one<D, NT, ST, KV8, true>(tq, tk, tv, p, grid, stream)
+                           : launch_one<D, NT, ST, KV8, false>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace

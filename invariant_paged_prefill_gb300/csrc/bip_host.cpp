@@ -38,8 +38,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct UnitDesc {
   int32_t request, kv_head, tile;  // tile = absolute tile of slot 0
   int32_t mask;                    // slots present
-  int32_t rows[bip::kMaxTilesPerUnit], nseg[bip::kMaxTilesPerUnit];
-  int32_t nseg_unit, blocks;       // over the union of the slots' keys
+  int32_t rows[bip::kMaxTilesPerUnit], nseg[bip::kMaxTilesPerUnit];  // nseg: segments 0 .. tile_end / L
+  int32_t blk_min, seg_lo, seg_hi;  // first block, first and last segment the unit visits
+  int32_t blocks;                   // blocks visited (union of the slots' keys, window applied)
 };
 
 }  // namespace
@@ -186,7 +187,9 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   opts.num_sms = 0;
   opts.wait_limit_ns = 0;
   opts.tiles_per_unit = 0;
+  opts.window_left = 0;
   if (opts_in) opts = *opts_in;
+  if (opts.window_left < 0) return BIP_ERR_INVALID_ARG;
   if (opts.split_policy != BIP_SPLIT_AUTO && opts.split_policy != BIP_SPLIT_NEVER &&
       opts.split_policy != BIP_SPLIT_ALWAYS)
     return BIP_ERR_INVALID_ARG;
@@ -243,7 +246,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
       u.request = r;
       u.tile = g0;
       u.mask = 0;
-      int32_t unit_end = -1;
+      int32_t unit_end = -1, unit_first = INT32_MAX;
       for (int32_t t = 0; t < NT; ++t) {
         const int32_t tile = g0 + t;
         u.rows[t] = 0;
@@ -255,9 +258,15 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
         u.rows[t] = (tile_end - first_valid + 1) * group;
         u.nseg[t] = tile_end / bip::kSplitLen + 1;
         unit_end = std::max(unit_end, tile_end);
+        unit_first = std::min(unit_first, first_valid);
       }
-      u.nseg_unit = unit_end / bip::kSplitLen + 1;
-      u.blocks = unit_end / bn + 1;
+      // With a sliding window the unit's earliest row sees keys from
+      // first - window on; blocks and segments before that are skipped.
+      const int32_t key_lo = opts.window_left > 0 ? std::max(0, unit_first - opts.window_left) : 0;
+      u.blk_min = key_lo / bn;
+      u.seg_lo = key_lo / bip::kSplitLen;
+      u.seg_hi = unit_end / bip::kSplitLen;
+      u.blocks = unit_end / bn + 1 - u.blk_min;
       for (int32_t h = 0; h < num_kv_heads; ++h) {
         u.kv_head = h;
         units.push_back(u);
@@ -266,7 +275,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   }
   auto split_need = [&](const UnitDesc& u) {
     size_t rows = 0;
-    for (int t = 0; t < NT; ++t) rows += size_t(u.nseg[t]) * u.rows[t];
+    for (int t = 0; t < NT; ++t) rows += size_t(std::max(0, u.nseg[t] - u.seg_lo)) * u.rows[t];
     return rows * partial_row_bytes(head_dim);
   };
 
@@ -287,7 +296,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   if (opts.split_policy != BIP_SPLIT_NEVER) {
     std::vector<size_t> cand;
     for (size_t i = 0; i < units.size(); ++i)
-      if (units[i].nseg_unit > 1) cand.push_back(i);
+      if (units[i].seg_hi > units[i].seg_lo) cand.push_back(i);
     std::stable_sort(cand.begin(), cand.end(),
                      [&](size_t a, size_t b) { return units[a].blocks > units[b].blocks; });
     // AUTO: split by segment when there are too few units to balance a
@@ -303,7 +312,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
       if (partial_bytes + need > opts.split_budget_bytes) continue;
       split[i] = 1;
       partial_bytes += need;
-      n_items += units[i].nseg_unit - 1;
+      n_items += units[i].seg_hi - units[i].seg_lo;
     }
   }
 
@@ -354,11 +363,12 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     w.kv_head = int16_t(u.kv_head);
     w.flags = int16_t(u.mask * bip::kSlotPresent);
     for (int t = 0; t < NT; ++t) w.nseg[t] = int16_t(u.nseg[t]);
+    w.blk_min = u.blk_min;
     const int32_t bps = bip::kSplitLen / bn;
     if (!split[i]) {
-      w.seg_lo = 0;
-      w.seg_hi = int16_t(u.nseg_unit - 1);
-      pend.push_back({w, {r, u.kv_head, u.tile, 0, u.nseg_unit - 1, 0, u.blocks, u.mask}, u.blocks});
+      w.seg_lo = int16_t(u.seg_lo);
+      w.seg_hi = int16_t(u.seg_hi);
+      pend.push_back({w, {r, u.kv_head, u.tile, u.seg_lo, u.seg_hi, 0, u.blocks, u.mask}, u.blocks});
     } else {
       int64_t base[bip::kMaxTilesPerUnit] = {0, 0};
       for (int t = 0; t < NT; ++t) {
@@ -371,17 +381,18 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
         m.part_base = int32_t(part_rows);
         m.rows = u.rows[t];
         m.kv_head = int16_t(u.kv_head);
-        m.nseg = int16_t(u.nseg[t]);
+        m.nseg = int16_t(u.nseg[t] - u.seg_lo);  // partials of segments seg_lo .. nseg - 1
         p->merges.push_back(m);
         base[t] = part_rows;
-        part_rows += int64_t(u.nseg[t]) * u.rows[t];
+        part_rows += int64_t(u.nseg[t] - u.seg_lo) * u.rows[t];
       }
-      for (int32_t sg = 0; sg < u.nseg_unit; ++sg) {
+      const int32_t blk_end = u.blk_min + u.blocks;  // one past the last block
+      for (int32_t sg = u.seg_lo; sg <= u.seg_hi; ++sg) {
         WorkItem ws = w;
         ws.seg_lo = ws.seg_hi = int16_t(sg);
         ws.flags = int16_t(w.flags | bip::kItemSplit);
-        for (int t = 0; t < NT; ++t) ws.part_base[t] = int32_t(base[t] + int64_t(sg) * u.rows[t]);
-        const int32_t blocks = std::min(u.blocks, (sg + 1) * bps) - sg * bps;
+        for (int t = 0; t < NT; ++t) ws.part_base[t] = int32_t(base[t] + int64_t(sg - u.seg_lo) * u.rows[t]);
+        const int32_t blocks = std::min(blk_end, (sg + 1) * bps) - std::max(u.blk_min, sg * bps);
         pend.push_back({ws, {r, u.kv_head, u.tile, sg, sg, 1, blocks, u.mask}, blocks});
       }
       p->num_split_units++;
@@ -596,6 +607,7 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
   ap.v_scale = v_scale;
   ap.wait_limit_cycles = p->wait_limit_cycles;
+  ap.window_left = p->opts.window_left;
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;
 
@@ -670,6 +682,7 @@ struct bip_graph_plan_s {
   int32_t grid = 0, capacity = 0;
   bip_kv_dtype kv_dtype = BIP_KV_BF16;
   uint64_t wait_limit_cycles = 0;
+  int32_t window_left = 0;
   size_t off_items = 0, off_scratch = 0, ws_bytes = 0;
 };
 
@@ -692,7 +705,9 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   opts.num_sms = 0;
   opts.wait_limit_ns = 0;
   opts.tiles_per_unit = 0;
+  opts.window_left = 0;
   if (opts_in) opts = *opts_in;
+  if (opts.window_left < 0) return BIP_ERR_INVALID_ARG;
   if (opts.split_policy == BIP_SPLIT_ALWAYS) return BIP_ERR_UNSUPPORTED;  // graph launches fold every unit
   if (opts.split_policy != BIP_SPLIT_AUTO && opts.split_policy != BIP_SPLIT_NEVER) return BIP_ERR_INVALID_ARG;
   if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
@@ -705,6 +720,7 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   if (!p) return BIP_ERR_OUT_OF_MEMORY;
   p->max_batch = max_batch;
   p->max_total_q = max_total_q;
+  p->window_left = opts.window_left;
   p->hq = num_qo_heads;
   p->hkv = num_kv_heads;
   p->d = head_dim;
@@ -780,7 +796,9 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
   dp.tile_pos = p->T;
   dp.tiles_per_unit = p->nt;
   dp.num_kv_heads = p->hkv;
+  dp.kv_block = bip::kv_block_for(p->d);
   dp.capacity = p->capacity;
+  dp.window_left = p->window_left;
   dp.qo_indptr = qo_indptr;
   dp.kv_indptr = kv_indptr;
   dp.kv_last_page_len = kv_last_page_len;
@@ -806,6 +824,7 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
   ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
   ap.v_scale = v_scale;
   ap.wait_limit_cycles = p->wait_limit_cycles;
+  ap.window_left = p->window_left;
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;
   return BIP_OK;

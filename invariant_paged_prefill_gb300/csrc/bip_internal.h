@@ -43,7 +43,8 @@ struct WorkItem {
   int16_t flags;       // kItemSplit | tile-present bits (kSlotPresent << t)
   int32_t part_base[2];  // split: partial row of slot t's first valid row in this segment
   int16_t nseg[2];       // segments that hold slot t's rows (tile_end / 4096 + 1)
-  int32_t pad[2];
+  int32_t blk_min;       // first KV block any row of the item sees (0 without a sliding window)
+  int32_t pad;
 };
 static_assert(sizeof(WorkItem) == 48, "work item size");
 constexpr int16_t kItemSplit = 1;
@@ -85,6 +86,7 @@ struct AttnParams {
   float scale_log2;     // log2(e) * k_scale / sqrt(head_dim)
   float v_scale;
   uint64_t wait_limit_cycles;  // wait bound in SM clock cycles (the limit in ns at the peak clock)
+  int32_t window_left;         // > 0: a row at position p sees keys p - window_left .. p only
 };
 
 struct MergeParams {
@@ -141,7 +143,9 @@ struct DevPlanParams {
   int32_t tile_pos;      // T
   int32_t tiles_per_unit;
   int32_t num_kv_heads;
+  int32_t kv_block;      // BN
   int32_t capacity;      // work items the workspace holds
+  int32_t window_left;   // > 0: sliding window of this many keys left of the diagonal
   const int32_t* qo_indptr;
   const int32_t* kv_indptr;
   const int32_t* kv_last_page_len;

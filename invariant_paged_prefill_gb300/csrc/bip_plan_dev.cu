@@ -9,6 +9,8 @@
 // Because a row's arithmetic depends on no property of the plan, results are
 // the bits of the host-planned launch.
 
+#include <climits>
+
 #include <cuda_runtime.h>
 
 #include "bip_internal.h"
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kPlanThreads) bip_device_plan_kernel(const Dev
         w.q_lo = q_lo;
         w.tile = g.g0 + gi * p.tiles_per_unit;
         w.kv_head = int16_t(h);
-        int mask = 0, unit_end = -1;
+        int mask = 0, unit_end = -1, unit_first = INT_MAX;
         w.nseg[0] = w.nseg[1] = 0;
         for (int t = 0; t < p.tiles_per_unit; ++t) {
           const int32_t tile = w.tile + t;
@@ -112,12 +114,16 @@ __global__ void __launch_bounds__(kPlanThreads) bip_device_plan_kernel(const Dev
           mask |= 1 << t;
           w.nseg[t] = int16_t(tile_end / kSplitLen + 1);
           unit_end = max(unit_end, tile_end);
+          unit_first = min(unit_first, max(tile * p.tile_pos, q_lo));
         }
+        // with a sliding window, keys before first - window are skipped
+        const int32_t key_lo = p.window_left > 0 ? max(0, unit_first - p.window_left) : 0;
         w.flags = int16_t(mask * kSlotPresent);
-        w.seg_lo = 0;
+        w.seg_lo = int16_t(key_lo / kSplitLen);
         w.seg_hi = int16_t(unit_end / kSplitLen);
         w.part_base[0] = w.part_base[1] = 0;
-        w.pad[0] = w.pad[1] = 0;
+        w.blk_min = key_lo / p.kv_block;
+        w.pad = 0;
         p.items[o++] = w;
       }
     }

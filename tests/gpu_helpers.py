@@ -27,13 +27,13 @@ def to_device(b: W.PagedBatch, device) -> W.PagedBatch:
 
 def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 << 20, num_sms: int = 0,
             wait_limit_ns: int = 0, check_status: bool = True, k_scale: float = 1.0, v_scale: float = 1.0,
-            tiles_per_unit: int = 0):
+            tiles_per_unit: int = 0, window_left: int = 0):
     """Plan + prefill on the device; returns (out, lse, plan) on the host."""
     d = b if b.q.is_cuda else to_device(b, device)
     plan = bip.Plan(d.qo_indptr, d.kv_indptr, d.kv_last_page_len, num_qo_heads=d.num_qo_heads,
                     num_kv_heads=d.num_kv_heads, head_dim=d.head_dim, page_size=d.page_size, kv_dtype=d.kv_dtype,
                     split_policy=policy, split_budget_bytes=budget, num_sms=num_sms, wait_limit_ns=wait_limit_ns,
-                    tiles_per_unit=tiles_per_unit)
+                    tiles_per_unit=tiles_per_unit, window_left=window_left)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     out = torch.full_like(d.q, float("nan"))
     lse = torch.full((d.q.shape[0], d.q.shape[1]), float("nan"), dtype=torch.float32, device=device)
@@ -46,7 +46,7 @@ def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 
     return out.cpu(), lse.cpu(), plan
 
 
-def oracle(b: W.PagedBatch, rows=None):
+def oracle(b: W.PagedBatch, rows=None, window_left: int = 0):
     kind = "bf16" if b.kv_dtype == "bf16" else "e4m3"
     kp = b.k_pages.cpu() if b.k_pages.is_cuda else b.k_pages
     vp = b.v_pages.cpu() if b.v_pages.is_cuda else b.v_pages
@@ -55,7 +55,7 @@ def oracle(b: W.PagedBatch, rows=None):
     return pa.paged_prefill(b.q.cpu().view(torch.int16).numpy(), kview.numpy(), vview.numpy(),
                             b.qo_indptr.tolist(), b.kv_indptr.tolist(), b.kv_indices.cpu().tolist(),
                             b.kv_last_page_len.tolist(), b.num_qo_heads, b.num_kv_heads, b.page_size,
-                            q_kind="bf16", kv_kind=kind, rows=rows)
+                            q_kind="bf16", kv_kind=kind, rows=rows, window_left=window_left)
 
 
 def assert_close_to_oracle(out, lse, ref_out, ref_lse, rows=None):

@@ -130,6 +130,19 @@ def test_graph_plan_validation_and_sizes(lib):
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 1, ctypes.byref(opts), None) == 2
 
 
+def test_window_plans_skip_keys_and_reject_negative_windows(lib):
+    qo, kv, last = [0, 9000], [0, 563], [9000 - 16 * 562]  # one 9000-token fresh prefill
+    plain = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_policy="never")
+    win = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_policy="never",
+                   window_left=1000)
+    assert win.info["kv_blocks"] < plain.info["kv_blocks"] / 3
+    items = win.items()
+    # the last tile group's item starts in segment 1 (its rows see keys from ~8000 - 1000 on)
+    assert items[:, 3].max() >= 1 and (items[:, 3] <= items[:, 4]).all()
+    with pytest.raises(bip.BipError):
+        bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, window_left=-1)
+
+
 def random_batch(rng, batch, max_kv, ps=16):
     kv_len = rng.integers(1, max_kv + 1, size=batch)
     q_len = np.minimum(kv_len, rng.integers(0, max_kv + 1, size=batch))
