@@ -151,12 +151,12 @@ def make_batch(heads, batch, q_len, kv_len, device, kv_dtype="bf16", seed=0):
 class Runner:
     """One workload resident on the device, with its plan and buffers."""
 
-    def __init__(self, b, device):
+    def __init__(self, b, device, window_left: int = 0):
         import invariant_paged_prefill_gb300 as bip
         self.bip, self.b, self.device = bip, b, device
         self.plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=b.num_qo_heads,
                              num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
-                             kv_dtype=b.kv_dtype)
+                             kv_dtype=b.kv_dtype, window_left=window_left)
         self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty_like(b.q)
         self.lse = torch.empty(b.q.shape[0], b.q.shape[1], dtype=torch.float32, device=device)
@@ -393,6 +393,18 @@ def time_append(b, device, steps: int, warmup: int):
     return e0.elapsed_time(e1) / steps, moved
 
 
+def windowed_work(heads, q_lens, kv_lens, window: int):
+    """(FLOP, KV bytes) of sliding-window attention: row at position p sees
+    min(p + 1, window + 1) keys; a request reads its last q + window keys."""
+    hq, hkv, d = heads
+    pairs, keys = 0, 0
+    for q, kv in zip(q_lens, kv_lens):
+        for p in range(kv - q, kv):
+            pairs += min(p + 1, window + 1)
+        keys += min(kv, q + window)
+    return 4 * d * hq * pairs, keys * 2 * hkv * d * 2
+
+
 def time_graph(b, device, steps: int, warmup: int):
     """Device-planned prefill captured in a CUDA graph (buffers sized to b):
     ms per replay, and whether the replay matches the host-planned result."""
@@ -510,6 +522,19 @@ def run_ours(args):
                            "max_abs_out": float(np.abs(got - ro).max()), "max_abs_lse": float(np.abs(gl - rl).max())},
                 "bit_exact_repeat": repeat_exact, "workspace_bytes": run.plan.workspace_bytes,
                 "source_hash": source_hash()}
+        # sliding window: long_q with a 1024-key window, the short extend with 4096
+        wl = Runner(b, device, window_left=1024)
+        wl_total, _ = wl.timed(args.steps, args.warmup)
+        ws_ = Runner(sb, device, window_left=4096)
+        ws_total, _ = ws_.timed(args.steps, args.warmup)
+        wfl, _ = windowed_work(heads, b.q_lens, b.kv_lens, 1024)
+        _, wkvb = windowed_work(sheads, sb.q_lens, sb.kv_lens, 4096)
+        line["window"] = {
+            "long_q_window_1024_tflops": wfl / (wl_total / args.steps * 1e-3) / 1e12,
+            "short_extend_window_4096_kv_gbs": wkvb / (ws_total / args.steps * 1e-3) / 1e9,
+            "short_extend_window_4096_ms": ws_total / args.steps,
+            "note": "algorithmic work of the window only (pairs within the window, keys the window reads)"}
+        del wl, ws_
         # device-planned launches replayed from a CUDA graph (fold only, no split)
         g_ms, g_out, g_lse = time_graph(b, device, args.steps, args.warmup)
         sg_ms, sg_out, sg_lse = time_graph(sb, device, args.steps, args.warmup)
