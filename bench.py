@@ -143,9 +143,10 @@ WORKLOADS = {
 }
 
 
-def make_batch(heads, batch, q_len, kv_len, device, kv_dtype="bf16", seed=0):
+def make_batch(heads, batch, q_len, kv_len, device, kv_dtype="bf16", seed=0, page_size=16):
     from invariant_paged_prefill_gb300 import workloads as W
-    return W.sweep_point(heads, q_len, kv_len, batch=batch, kv_dtype=kv_dtype, device=device, seed_data=seed)
+    return W.sweep_point(heads, q_len, kv_len, batch=batch, kv_dtype=kv_dtype, device=device, seed_data=seed,
+                         page_size=page_size)
 
 
 class Runner:
@@ -535,6 +536,20 @@ def run_ours(args):
             "short_extend_window_4096_ms": ws_total / args.steps,
             "note": "algorithmic work of the window only (pairs within the window, keys the window reads)"}
         del wl, ws_
+        # token-granular pools (page size 1, every row of a block gathered on
+        # its own): the same prompts, so the same bits as the 16-slot pages
+        b1 = make_batch(heads, batch, q_len, kv_len, device, seed=rank_seed(rank), page_size=1)
+        sb1 = make_batch(sheads, sbatch, sq, skv, device, seed=rank_seed(rank, 100), page_size=1)
+        r1, sr1 = Runner(b1, device), Runner(sb1, device)
+        p1_total, _ = r1.timed(args.steps, args.warmup)
+        sp1_total, _ = sr1.timed(args.steps, args.warmup)
+        line["page_size_1"] = {
+            "long_q_tflops": fl / (p1_total / args.steps * 1e-3) / 1e12,
+            "short_extend_kv_gbs": kvb / (sp1_total / args.steps * 1e-3) / 1e9,
+            "short_extend_ms": sp1_total / args.steps,
+            "bit_exact_vs_page_16": bool(torch.equal(r1.out, run.out) and torch.equal(r1.lse, run.lse) and
+                                         torch.equal(sr1.out, srun.out) and torch.equal(sr1.lse, srun.lse))}
+        del r1, sr1, b1, sb1
         # device-planned launches replayed from a CUDA graph (fold only, no split)
         g_ms, g_out, g_lse = time_graph(b, device, args.steps, args.warmup)
         sg_ms, sg_out, sg_lse = time_graph(sb, device, args.steps, args.warmup)

@@ -127,8 +127,10 @@ size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, int32_t num_q
  * kv_len = (pages - 1) * page_size + last_page_len (0 with no pages);
  * 0 <= q_len <= kv_len is required; q_len = 0 is legal and yields no rows.
  * Supported now: head_dim 128 or 256, gqa_group <= 128, page_size a power of
- * two in [8, BN], kv_dtype BIP_KV_BF16 or BIP_KV_FP8_E4M3 (FP8 runs one q tile
- * per CTA; tiles_per_unit = 2 with FP8 returns BIP_ERR_UNSUPPORTED).
+ * two in [1, BN] (1 = a token-granular pool; below 8 the kernel gathers
+ * token rows instead of whole pages, with the same bits), kv_dtype
+ * BIP_KV_BF16 or BIP_KV_FP8_E4M3 (FP8 runs one q tile per CTA;
+ * tiles_per_unit = 2 with FP8 returns BIP_ERR_UNSUPPORTED).
  * opts may be NULL (defaults).  On success *plan owns the result and
  * *workspace_bytes (if not NULL) receives the exact workspace size, never
  * above bip_workspace_bound for the same shapes.  No device work except a
@@ -164,7 +166,8 @@ bip_status bip_plan_destroy(bip_plan_t plan);
  *            bytes receive this call's work list (one host->device copy on
  *            `stream`) and a status word.
  * q, pages and out must be 16-byte aligned; page_stride_elems * element size
- * must be a multiple of 16 bytes.  k_scale multiplies the logits (folded
+ * must be a multiple of 16 bytes (and, for page sizes below 8, below 2^31
+ * bytes, else BIP_ERR_UNSUPPORTED).  k_scale multiplies the logits (folded
  * into the softmax scale) and v_scale the output; use 1.0 for bf16 pages.
  * Page slots at or beyond a request's kv_len may hold anything (NaN too).
  * Calls sharing one workspace must be ordered on the GPU. */

@@ -1,887 +1,27 @@
-// Persistent paged prefill attention for sm_103a: TMA page loads, tcgen05
-// MMAs with TMEM accumulators, an fp32 online softmax with one thread per
-// row, P kept in TMEM, and a fixed-order segment merge.
-//
-// One CTA (one per SM) walks work items: a unit = (request, KV head, NT
-// consecutive absolute q tiles that share the same keys) over some of its
-// 4096-key segments.  Roles:
-//   warp 0          TMA producer: the unit's q tiles once, then K blocks page
-//                   by page through an ST-deep ring.
-//   last warp       TMA producer of the V blocks (its own ST-deep ring).
-//   warp 1          tcgen05 issuer: S_t = Q_t K^T into TMEM, then
-//                   O_t += P_t V with P_t read from TMEM; zeroes V rows past
-//                   kv_len before they enter a product.
-//   warps 2..       one softmax warpgroup per q tile slot t: thread i owns
-//                   packed row i (TMEM lane i); masks, keeps the row's running
-//                   max and sum, writes P_t (bf16) over S_t in TMEM, rescales
-//                   O_t when needed, and at each segment end folds or writes
-//                   the segment.
-//   (FP8 pages)     a dequant warpgroup converts staged E4M3 blocks to bf16.
-// With two slots (head_dim 128) the softmax of one tile overlaps the MMAs of
-// the other.  Slots and ring depth only decide scheduling; every row's
-// arithmetic is the same in every variant.
-//
-// Packed rows (GQA group inside the 128-row tile, sglang PR 46351 "Root
-// cause": packed q length = q_len * group): row = local_pos * group + head
-// within the KV head's group, local_pos in [0, T), T = floor(128 / group).
-//
-// Invariance: a row's arithmetic depends only on its own q row, on keys at
-// positions <= its own, and on the compile-time block/segment lengths.  MMA
-// rows never mix; blocks beyond a row's position contribute exact zeros
-// (p = 0 against finite V: rows of V past kv_len are zeroed in shared
-// memory), and segments wholly beyond it are empty and skipped by the merge.
-// The running max is moved (and O rescaled) only when a row's block max
-// exceeds it by more than kLazyRescale in log2 units: a per-row decision.
+// Attention launches for pools whose pages hold 8 or more token slots:
+// every page lands in shared memory as TMA boxes (kernel templates in
+// bip_attn_impl.cuh).  Smaller pages go to the row-gather variants.
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-#include <cuda_runtime.h>
-
-#include <climits>
-#include <type_traits>
-
-#include "bip_internal.h"
-#include "bip_numerics.cuh"
-#include "bip_ptx.cuh"
+#include "bip_attn_impl.cuh"
 
 namespace bip {
-namespace {
-
-// A row keeps a stale running max until a block raises it by more than this
-// (log2 units): probabilities then stay below 2^8 and O is rescaled rarely.
-constexpr float kLazyRescale = 8.0f;
-
-// Column pairs (mod 8) whose exponentials run on the FMA pipe instead of
-// MUFU.  Measured on GB300: every pair moved to the polynomial made the
-// softmax slower (the exp pass is latency- and register-bound, not MUFU
-// throughput-bound), so none is.
-constexpr uint32_t kFmaPairs = 0x00;
-
-template <int D, int NT, int ST, bool KV8 = false>
-struct Cfg {
-  static constexpr int BN = kv_block_for(D);        // keys per block
-  static constexpr int NS = NT == 1 ? 2 : 1;        // S buffers per tile slot
-  static constexpr int DCH = D / 64;                // 64-column (128-byte) chunks of a d-row
-  static constexpr int Q_CHUNK = kTileRows * 128;   // bytes of one q chunk (128 rows)
-  static constexpr int Q_BYTES = DCH * Q_CHUNK;     // one tile slot
-  static constexpr int KV_CHUNK = BN * 128;         // bytes of one K/V chunk (BN rows)
-  static constexpr int KV_BYTES = DCH * KV_CHUNK;   // one K or V block
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NT * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + ST * KV_BYTES;
-  // FP8 pages land raw (BN rows x D bytes, unswizzled) in a staging ring and
-  // are converted to the bf16 operand layout by the dequant warpgroup.
-  static constexpr int SS = KV8 ? (D == 128 ? 2 : 1) : 0;  // staging stages
-  static constexpr int KV8_BYTES = BN * D;
-  static constexpr int OFF_K8 = OFF_V + ST * KV_BYTES;
-  static constexpr int OFF_V8 = OFF_K8 + SS * KV8_BYTES;
-  static constexpr int OFF_BAR = OFF_V8 + SS * KV8_BYTES;
-  static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
-  // Warp roles, whole warpgroups each: softmax warps 0 .. 4 NT - 1 (slot
-  // t = warp / 4, TMEM lane quarter = warp % 4), then the FP8 dequant
-  // warpgroup, then the control warpgroup: q/K producer, MMA issuer, V
-  // producer and one spare warp.
-  static constexpr int SM_WARPS = 4 * NT;
-  static constexpr int DQ_WARP0 = SM_WARPS;
-  static constexpr int CTL_WARP0 = SM_WARPS + (KV8 ? 4 : 0);
-  static constexpr int THREADS = 32 * (CTL_WARP0 + 4);
-  // Register split: launches of more than 256 threads start at LAUNCH_REGS
-  // a thread; the control warpgroup then gives registers back (setmaxnreg)
-  // and the softmax warpgroups take them.  The dequant warpgroup keeps its
-  // launch count.  The sum never exceeds what the launch holds.
-  static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;
-  static constexpr bool SPLIT_REGS = THREADS > 256;
-  static constexpr int CTL_REGS = KV8 ? 80 : 56;  // FP8: softmax is capped at 240 anyway
-  static constexpr int SM_REGS_FREE =
-      ((LAUNCH_REGS * THREADS - CTL_REGS * 128 - (KV8 ? LAUNCH_REGS * 128 : 0)) / (32 * SM_WARPS)) & ~7;
-  static constexpr int SM_REGS = SPLIT_REGS ? (SM_REGS_FREE < 240 ? SM_REGS_FREE : 240) : 255;
-  static_assert(!SPLIT_REGS || SM_REGS * 32 * SM_WARPS + CTL_REGS * 128 + (KV8 ? LAUNCH_REGS * 128 : 0) <=
-                                   LAUNCH_REGS * THREADS, "register split exceeds the launch's registers");
-  static_assert(!SPLIT_REGS || SM_REGS >= LAUNCH_REGS, "softmax warps must not lose registers");
-  static constexpr int TM_COLS = 512;
-  // Unroll factor of the MMA issue loops.  The tensor pipe queues only a few
-  // MMAs, so the issuing thread's per-MMA instructions show up as pipe time;
-  // measured on GB300, full unrolling is best with one q-tile slot and 4
-  // with two (whose larger issue path slows down when fully unrolled).
-  static constexpr int ISSUE_UNROLL = NT == 1 ? 16 : 4;
-  static constexpr int BPS = kSplitLen / BN;         // blocks per segment
-  // TMEM columns: two slots use [0,256) and [256,512), each S (BN) then O (D);
-  // one slot keeps two S buffers at [0, 2 BN) and O at [256, 256 + D).
-  __host__ __device__ static constexpr uint32_t tm_s(int t, int s) {
-    return NT == 2 ? uint32_t(t * 256) : uint32_t(s * BN);
-  }
-  __host__ __device__ static constexpr uint32_t tm_o(int t) { return NT == 2 ? uint32_t(t * 256 + BN) : 256u; }
-  static_assert(NT == 1 || (BN + D <= 256), "two slots need S and O in 256 columns each");
-  static_assert(NT == 2 || (2 * BN <= 256 && 256 + D <= TM_COLS), "TMEM budget");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  static_assert(!KV8 || NT == 1, "FP8 pages use the one-tile variant");
-};
-
-// Barrier slots (8 bytes each) at OFF_BAR.
-enum Bar {
-  B_Q_FULL = 0, B_Q_FREE = 1,
-  B_K_FULL = 2, B_K_FREE = 6, B_V_FULL = 10, B_V_FREE = 14,  // up to 4 ring stages
-  // Per slot and per S buffer (index 2 slot + buffer).  P_FULL and O_DONE
-  // are kept per buffer too: with two S buffers the softmax may finish two
-  // blocks before the issuer waits on the first, and a single barrier two
-  // phases ahead of its waiter reads as zero under a parity wait.
-  B_S_FULL = 18, B_P_FULL = 22, B_O_DONE = 26,
-  B_DRAIN = 30,
-  B_K8_FULL = 31, B_K8_FREE = 33, B_V8_FULL = 35, B_V8_FREE = 37,  // FP8 staging, up to 2 stages
-  B_V_TX = 39,  // bf16 V blocks that end past kv_len land here first (the V producer zeroes the tail)
-  B_COUNT = 40
-};
-constexpr int OFF_TMEM_SLOT = 8 * B_COUNT;    // u32: TMEM base address
-constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;  // u32: a wait expired somewhere in this CTA
-static_assert(OFF_ABORT + 4 <= 512, "barrier area");
-
-struct Ctx {
-  uint32_t bar0;
-  volatile uint32_t* abort;
-  WsHeader* header;
-  uint64_t limit_cycles;
-};
-
-__device__ __forceinline__ uint32_t bar(const Ctx& c, int i) { return c.bar0 + 8u * i; }
-
-// Bounded wait on an mbarrier phase.  On expiry the CTA is marked aborted,
-// the workspace status records a timeout, and false is returned; any wait
-// that sees the abort mark also returns false.  The first probe answers at
-// once; after it the clock is checked before every (suspending) probe, so a
-// wait that is not already complete always meets the limit check.  (Inlined:
-// an out-of-line call cannot be shared by warpgroups running with different
-// register budgets.)
-__device__ __forceinline__ bool wait_phase(const Ctx& c, uint32_t b, uint32_t parity, uint32_t where) {
-  const uint64_t t0 = clock64();
-  if (mbar_ready(b, parity)) return true;
-  while (true) {
-    if (uint64_t(clock64()) - t0 > c.limit_cycles) {
-      *c.abort = 1u;
-      atomicCAS(&c.header->status, 0u, 5u /* BIP_ERR_DEVICE_TIMEOUT */);
-      atomicExch(&c.header->where, where);
-      return false;
-    }
-    if (mbar_test(b, parity)) return true;
-    if (*c.abort) return false;
-  }
-}
-
-// Same, with the result made uniform across the warp.
-__device__ __forceinline__ bool wait_warp(const Ctx& c, uint32_t b, uint32_t parity, uint32_t where) {
-  const bool ok = wait_phase(c, b, parity, where);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Bounded wait used only while draining at exit (ignores the abort mark).
-__device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_test(b, parity))
-    if (globaltimer_ns() - t0 > 2000000000ull) break;
-}
-
-struct Geom {
-  int tile_start[kMaxTilesPerUnit];  // first position of each slot's tile
-  int tile_end[kMaxTilesPerUnit];    // last position with a q row or key in each slot's tile
-  int first_valid[kMaxTilesPerUnit];
-  int mask, last_slot;
-  int blk_lo, blk_hi;  // inclusive block range of the item (union of the slots' keys)
-};
-
-template <int NT, int BN>
-__device__ __forceinline__ Geom geom_of(const WorkItem& w, int T) {
-  Geom g;
-  g.mask = (w.flags / kSlotPresent) & ((1 << NT) - 1);
-  g.last_slot = 0;
-  int unit_end = 0;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    g.tile_start[t] = (w.tile + t) * T;
-    g.tile_end[t] = min(g.tile_start[t] + T - 1, w.kv_len - 1);
-    g.first_valid[t] = max(g.tile_start[t], w.q_lo);
-    if (g.mask >> t & 1) {
-      g.last_slot = t;
-      unit_end = g.tile_end[t];
-    }
-  }
-  g.blk_lo = max(int(w.seg_lo) * (kSplitLen / BN), w.blk_min);  // a sliding window starts mid-segment
-  g.blk_hi = min((int(w.seg_hi) + 1) * kSplitLen - 1, unit_end) / BN;
-  return g;
-}
-
-// Work items of this launch: fixed by the host plan, or counted on the
-// device by the planner kernel that ran before (graph-replayable launches).
-__device__ __forceinline__ int item_count(const AttnParams& p) {
-  return p.n_items_dev ? int(*p.n_items_dev) : p.n_items;
-}
-
-// ------------------------------------------------------------------ roles
-
-// Page id of page `lane` of KV block `blk` (0 for lanes past the block's
-// pages), and the block's page count.  Pages per block <= 16 <= warp size.
-__device__ __forceinline__ int lane_page_id(const AttnParams& p, const WorkItem& w, int blk, int pages_per_blk,
-                                            int npages_req, int lane, int& n) {
-  const int p0 = blk * pages_per_blk;
-  n = min(p0 + pages_per_blk, npages_req) - p0;
-  return lane < n ? __ldg(p.kv_indices + w.page_base + p0 + lane) : 0;
-}
-
-// One TMA stream, run by a whole warp: the control warpgroup's first warp
-// loads the q tiles and K, its third warp loads V, so a V slot still in use
-// never holds back K loads (or the reverse).  Lane i holds the page id of
-// page i of the next block (fetched one block ahead) and issues that page's
-// loads; lane 0 posts the expected bytes first.  Each item's first
-// ring-depth K blocks are issued before its q tiles, whose load waits for
-// the previous item's last S, so the ring keeps streaming across item
-// boundaries.
-template <int D, int NT, int ST, bool KV8>
-__device__ void producer(const Ctx& c, uint32_t sbase, const CUtensorMap* tq, const CUtensorMap* tkv,
-                         const AttnParams& p, const bool is_v) {
-  using C = Cfg<D, NT, ST, KV8>;
-  static_assert(C::BN / 8 <= 32, "one lane per page");
-  const int lane = threadIdx.x & 31;
-  const uint32_t sQ = sbase + C::OFF_Q;
-  const int pages_per_blk = C::BN / p.page_size;
-  const uint32_t q_slot_bytes = uint32_t(C::DCH * 128 * p.group * p.tile_pos);
-  // bf16: TMA fills the ring slot; FP8: TMA fills the staging ring, the
-  // dequant warps fill the slot.
-  constexpr int RING = KV8 ? C::SS : ST;
-  const int full0 = KV8 ? (is_v ? B_V8_FULL : B_K8_FULL) : (is_v ? B_V_FULL : B_K_FULL);
-  const int free0 = KV8 ? (is_v ? B_V8_FREE : B_K8_FREE) : (is_v ? B_V_FREE : B_K_FREE);
-  const uint32_t ring0 = sbase + (KV8 ? (is_v ? C::OFF_V8 : C::OFF_K8) : (is_v ? C::OFF_V : C::OFF_K));
-  const uint32_t ring_bytes = KV8 ? uint32_t(C::KV8_BYTES) : uint32_t(C::KV_BYTES);
-  const uint32_t page_bytes = uint32_t(p.page_size * D * (KV8 ? 1 : 2));
-  uint32_t b = 0;      // blocks started by this CTA
-  int n = 0;           // items started by this CTA
-  uint32_t n_tail = 0;  // bf16 V blocks routed through B_V_TX (issued)
-  uint32_t n_q = 0;     // q tile loads issued
-  bool ok = true;
-
-  auto load_q = [&](const WorkItem& w, const Geom& g) -> bool {
-    if (n > 0 && !wait_warp(c, bar(c, B_Q_FREE), (n - 1) & 1, 1)) return false;
-    ++n_q;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(c, B_Q_FULL), q_slot_bytes * __popc(g.mask));
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (!(g.mask >> t & 1)) continue;
-        for (int ch = 0; ch < C::DCH; ++ch)
-          tma_load_3d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tq, bar(c, B_Q_FULL), ch * 64, w.kv_head * p.group,
-                      w.q_tok0 + g.tile_start[t]);
-      }
-    }
-    __syncwarp();
-    return true;
-  };
-
-  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x, ++n) {
-    const WorkItem w = p.items[it];
-    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
-    const int npages_req = (w.kv_len + p.page_size - 1) / p.page_size;
-    int nid;
-    int id_next = lane_page_id(p, w, g.blk_lo, pages_per_blk, npages_req, lane, nid);
-    bool q_done = is_v;
-    for (int blk = g.blk_lo; blk <= g.blk_hi; ++blk, ++b) {
-      if (!q_done && blk - g.blk_lo == min(RING, g.blk_hi - g.blk_lo + 1)) {
-        if (!load_q(w, g)) { ok = false; break; }
-        q_done = true;
-      }
-      const int slot = b % RING;
-      const uint32_t use = b / RING;
-      const int ncur = nid;
-      int id = id_next;
-      if (lane < ncur && (id < 0 || id >= p.num_pages)) {  // counted once, by the K stream
-        if (!is_v) atomicAdd(&c.header->bad_pages, 1u);
-        id = 0;
-      }
-      if (blk < g.blk_hi) id_next = lane_page_id(p, w, blk + 1, pages_per_blk, npages_req, lane, nid);
-      if (use > 0 && !wait_warp(c, bar(c, free0 + slot), (use - 1) & 1, is_v ? 3 : 2)) { ok = false; break; }
-      // A bf16 V block that ends past kv_len lands on B_V_TX; once it is in,
-      // this warp zeroes the rows at or past kv_len (the tail of the last
-      // page, and pages the request does not have) so that p = 0 meets a
-      // finite value, then completes the slot's V_FULL phase itself.  (FP8:
-      // the dequant warps write those zeros.)
-      const int valid_rows = w.kv_len - blk * C::BN;
-      const bool tail = !KV8 && is_v && valid_rows < C::BN;
-      const uint32_t land = tail ? bar(c, B_V_TX) : bar(c, full0 + slot);
-      if (lane == 0) mbar_arrive_expect_tx(land, uint32_t(ncur) * page_bytes);
-      n_tail += tail ? 1u : 0u;
-      __syncwarp();
-      if (lane < ncur) {
-        if constexpr (KV8) {
-          tma_load_4d(ring0 + slot * ring_bytes + lane * page_bytes, tkv, land, 0, w.kv_head, 0, id);
-        } else {
-          for (int ch = 0; ch < C::DCH; ++ch)
-            tma_load_4d(ring0 + slot * ring_bytes + ch * C::KV_CHUNK + lane * p.page_size * 128, tkv, land,
-                        ch * 64, w.kv_head, 0, id);
-        }
-      }
-      if (tail) {
-        if (!wait_warp(c, land, (n_tail - 1) & 1, 4)) { ok = false; break; }
-        const uint32_t vbase = ring0 + slot * ring_bytes;
-        const int per_chunk = (C::BN - valid_rows) * 8;  // 16-byte units per chunk
-        for (int u = lane; u < per_chunk * C::DCH; u += 32) {
-          const int ch = u / per_chunk, rem = u % per_chunk;
-          const uint32_t addr = vbase + ch * C::KV_CHUNK + (valid_rows + rem / 8) * 128 + (rem % 8) * 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(c, full0 + slot));
-        __syncwarp();
-      }
-    }
-    if (ok && !q_done && !load_q(w, g)) ok = false;  // items shorter than the ring
-  }
-  // Drain: the last load on every barrier must have landed before exit (on
-  // the normal path these phases completed long ago).  Phases issued: one
-  // per q load (K stream only), and blocks started / RING per slot.
-  if (lane == 0) {
-    if (n_q) drain_wait(bar(c, B_Q_FULL), (n_q - 1) & 1);
-    if (n_tail) drain_wait(bar(c, B_V_TX), (n_tail - 1) & 1);
-#pragma unroll
-    for (int slot = 0; slot < RING; ++slot) {
-      const uint32_t issued = b / RING + (uint32_t(slot) < b % RING ? 1u : 0u);
-      if (issued) drain_wait(bar(c, full0 + slot), (issued - 1) & 1);
-    }
-  }
-  __syncwarp();
-}
-
-// The tcgen05 issuer: one thread.  The tensor pipe queues only a few MMAs,
-// so every cycle spent between two groups of MMAs (barrier probes, warp
-// votes) shows up as pipe idle time; a single thread with plain probes keeps
-// that gap short.
-template <int D, int NT, int ST, bool KV8>
-__device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const AttnParams& p) {
-  using C = Cfg<D, NT, ST, KV8>;
-  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);  // S = Q K^T, both K-major
-  constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);       // O += P V, V MN-major
-  uint32_t gb = 0;                       // KV blocks consumed by this CTA (ring position)
-  uint32_t k_seen = 0;                   // K blocks known to have landed
-  uint32_t s_cnt[NT] = {}, pv_cnt[NT] = {};  // blocks whose S / PV was issued, per slot
-  int n = 0;
-  bool ok = true;
-  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x, ++n) {
-    const WorkItem w = p.items[it];
-    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
-    const int nb = g.blk_hi - g.blk_lo + 1;
-    if (!wait_phase(c, bar(c, B_Q_FULL), n & 1, 10)) { ok = false; break; }
-    tc_fence_after();
-
-    // S_t for item-local block j into the slot's next S buffer.
-    auto issue_s = [&](int t, int j) -> bool {
-      const uint32_t kb = gb + j;
-      const int kslot = kb % ST;
-      if (kb >= k_seen) {  // the other slot's S may already have seen this K block land
-        if (!wait_phase(c, bar(c, B_K_FULL + kslot), (kb / ST) & 1, 11)) return false;
-        k_seen = kb + 1;
-        tc_fence_after();
-      }
-      const int sbuf = s_cnt[t] % C::NS;
-      const uint32_t d_tmem = tmem + C::tm_s(t, sbuf);
-      // K step k: 32 bytes along a 128-byte row, 64 columns per chunk.  The
-      // start address sits in the descriptor's low bits (16-byte units), so
-      // a step is an add.
-      const uint64_t dq = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
-      const uint64_t dk = sdesc_sw128(sK + kslot * C::KV_BYTES, 16, 1024);
-#pragma unroll (C::ISSUE_UNROLL)
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t cq = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
-        const uint32_t ck = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
-        tc_mma_ss(d_tmem, dq + cq, dk + ck, kIdescS, k > 0 ? 1u : 0u);
-      }
-      tc_commit(bar(c, B_S_FULL + 2 * t + sbuf));
-      if (t == g.last_slot) {
-        tc_commit(bar(c, B_K_FREE + kslot));                // last reader of this K block
-        if (j == nb - 1) tc_commit(bar(c, B_Q_FREE));       // last reader of the q tiles
-      }
-      ++s_cnt[t];
-      return true;
-    };
-
-    for (int j = 0; j < C::NS && j < nb && ok; ++j)
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if ((g.mask >> t & 1) && !issue_s(t, j)) { ok = false; break; }
-    if (!ok) break;
-
-    for (int j = 0; j < nb && ok; ++j) {
-      const uint32_t vb = gb + j;
-      const int vslot = vb % ST;
-      const int blk = g.blk_lo + j;
-      // O starts afresh at a segment's first visited block (a block boundary
-      // of the segment grid, or the item's first block under a window)
-      const bool first_in_seg = (blk % C::BPS) == 0 || j == 0;
-      bool v_ready = false;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (!(g.mask >> t & 1)) continue;
-        const int pbuf = pv_cnt[t] % C::NS;
-        if (!wait_phase(c, bar(c, B_P_FULL + 2 * t + pbuf), (pv_cnt[t] / C::NS) & 1, 13)) { ok = false; break; }
-        if (!v_ready) {
-          // V rows at or past kv_len were zeroed before this phase completed.
-          if (!wait_phase(c, bar(c, B_V_FULL + vslot), (vb / ST) & 1, 14)) { ok = false; break; }
-          v_ready = true;
-        }
-        tc_fence_after();
-        const uint32_t p_tmem = tmem + C::tm_s(t, pbuf);  // P_t (bf16) over its S buffer
-        const uint64_t dv = sdesc_sw128(sV + vslot * C::KV_BYTES, C::KV_CHUNK, 1024);
-#pragma unroll (C::ISSUE_UNROLL)
-        for (int k = 0; k < C::BN / 16; ++k)  // K step k: 16 V rows (2048 bytes), 8 TMEM columns of P
-          tc_mma_ts(tmem + C::tm_o(t), p_tmem + k * 8, dv + uint32_t(k * 128), kIdescO,
-                    (k > 0 || !first_in_seg) ? 1u : 0u);
-        tc_commit(bar(c, B_O_DONE + 2 * t + pbuf));
-        ++pv_cnt[t];
-        // The slot's next S goes into the buffer this PV has just been queued
-        // to read; tcgen05 MMAs of one thread execute in issue order.
-        if (j + C::NS < nb && !issue_s(t, j + C::NS)) { ok = false; break; }
-      }
-      if (!ok) break;
-      tc_commit(bar(c, B_V_FREE + vslot));
-    }
-    gb += nb;
-  }
-  // Drain: every MMA this thread issued has completed before TMEM is freed.
-  tc_commit(bar(c, B_DRAIN));
-  drain_wait(bar(c, B_DRAIN), 0);
-}
-
-template <int D, int NT, int ST, bool KV8, bool WIN>
-__device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t) {
-  using C = Cfg<D, NT, ST, KV8>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quarter = warp & 3;          // TMEM lanes this warp may access
-  const int row = quarter * 32 + lane;   // packed tile row == TMEM lane
-  const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16);
-  const float scale = p.scale_log2;
-  uint32_t cnt = 0, pv_seen = 0;  // blocks of this slot processed / PVs known complete
-  bool ok = true;
-
-  // PV of this slot's block x has completed.  PVs complete in order, so
-  // pv_seen only skips waits already satisfied.
-  auto wait_pv = [&](uint32_t x) -> bool {
-    if (pv_seen > x) return true;
-    if (!wait_warp(c, bar(c, B_O_DONE + 2 * t + x % C::NS), (x / C::NS) & 1, 20)) return false;
-    pv_seen = x + 1;
-    return true;
-  };
-
-  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x) {
-    const WorkItem w = p.items[it];
-    const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
-    if (!(g.mask >> t & 1)) continue;
-    const int local_pos = row / p.group;
-    const int hg = row - local_pos * p.group;
-    const int pos = g.tile_start[t] + local_pos;
-    const bool valid = row < p.tile_pos * p.group && pos >= g.first_valid[t] && pos <= g.tile_end[t];
-    const bool split = (w.flags & kItemSplit) != 0;
-    float Mrun = -INFINITY, Lrun = 0.f;  // merged state of the segments before this one
-    float* scratch_row = p.scratch + ((size_t(blockIdx.x) * NT + t) * kTileRows + row) * D;
-    const uint32_t o_addr = t_lane + C::tm_o(t);
-
-    for (int s = w.seg_lo; s <= w.seg_hi && ok; ++s) {
-      const int sb_lo = max(s * C::BPS, g.blk_lo);
-      const int sb_hi = min((s + 1) * C::BPS - 1, g.blk_hi);
-      float m = -INFINITY, l = 0.f;  // running raw-score max (possibly stale) and sum over this segment
-      bool seg_first = true;  // first block of this segment: O is overwritten, never rescaled
-      for (int blk = sb_lo; blk <= sb_hi; ++blk, ++cnt, seg_first = false) {
-        const int sbuf = cnt % C::NS;
-        if (!wait_warp(c, bar(c, B_S_FULL + 2 * t + sbuf), (cnt / C::NS) & 1, 21)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sa = t_lane + C::tm_s(t, sbuf);
-        // Columns lo..lim are visible: keys up to the row's position, and
-        // with a sliding window none before position - window_left.
-        const int lim = valid ? pos - blk * C::BN : -1;
-        const int lo = WIN ? pos - p.window_left - blk * C::BN : INT_MIN / 2;
-
-        // Blocks wholly visible to every valid row of the warp skip the
-        // per-column mask (same values for those rows, fewer instructions).
-        // Rows that are not valid (before the first q row of an extend, past
-        // the tile's end) are never written out; on the whole-block path they
-        // compute on whatever scores their q rows give, which touches no other
-        // row (each row of P V depends only on that row of P) and never asks
-        // for a rescale.  A warp with no visible column in this block skips
-        // the arithmetic but still stores P = 0: its rows may be valid rows
-        // past whose position the block lies, and their O keeps accumulating
-        // P V.
-        const bool whole = __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (!WIN || lo <= 0)));
-        const bool live = __any_sync(0xffffffffu, lim >= 0 && (!WIN || lo < C::BN));
-
-        // Block max.  One TMEM round trip for the whole S row; a 128-column
-        // row is then reread in two halves for the exponentials instead of
-        // being kept live (which spills even at 255 registers a thread).
-        constexpr bool kHalves = C::BN == 128;
-        constexpr int HW = kHalves ? C::BN / 2 : C::BN;  // columns per exp pass
-        float mx = -INFINITY;
-        uint32_t sv[C::BN];
-        // eight independent partial maxima over column pairs (max is exact in
-        // any order); masked columns enter as -inf.  Whole blocks and masked
-        // blocks get separately compiled loops.
-        auto block_max = [&](auto whole_c) {
-          constexpr bool kWhole = decltype(whole_c)::value;
-          float m8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < C::BN; j += 2) {
-            float a = __uint_as_float(sv[j]), b = __uint_as_float(sv[j + 1]);
-            if (!kWhole) {
-              a = (j <= lim && (!WIN || j >= lo)) ? a : -INFINITY;
-              b = (j + 1 <= lim && (!WIN || j + 1 >= lo)) ? b : -INFINITY;
-            }
-            m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], a, b);
-          }
-          return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        };
-        if (live) {
-          if constexpr (C::BN == 128) tmem_ld_x128(sa, sv);
-          else tmem_ld_x64(sa, sv);
-          mx = whole ? block_max(std::true_type{}) : block_max(std::false_type{});
-        }
-        float alpha = 1.f;
-        if (mx != -INFINITY) {
-          if (m == -INFINITY) {
-            m = mx;  // first visible block of the segment: O starts fresh
-          } else {
-            const float ms_old = __fmul_rn(m, scale), ms_new = __fmul_rn(mx, scale);
-            if (__fsub_rn(ms_new, ms_old) > kLazyRescale) {
-              alpha = ex2(__fsub_rn(ms_old, ms_new));
-              m = mx;
-            }
-          }
-        }
-        const float ms = (m == -INFINITY) ? 0.f : __fmul_rn(m, scale);
-
-        // Probabilities, the row sum and P (bf16 pairs, packed in place)
-        // written back over the S columns already read.  Column pairs (2i,
-        // 2i+1) whose bit i (mod 8) is set in kFmaPairs take 2^x on the FMA
-        // pipe, the rest on MUFU; the choice depends only on the key's
-        // absolute position (blocks start at multiples of 16).  Masked columns
-        // are computed and then replaced by exact zeros, so a row gets the
-        // same bits through the whole-block and the masked path.
-        // Row-sum partials: acc[i] holds columns 2i, 2i + 1 (mod 8), each
-        // pair summed with one packed add (four chains, so that the adds do
-        // not wait on each other); they are combined pairwise at the end.
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        const uint64_t sc2 = f2_splat(scale), nm2 = f2_splat(-ms);
-#pragma unroll
-        for (int h = 0; h < C::BN / HW; ++h) {
-          uint32_t* hv = kHalves ? sv : sv + h * HW;
-          if (live) {
-            if constexpr (kHalves) tmem_ld_x64(sa + h * HW, *reinterpret_cast<uint32_t(*)[64]>(hv));
-            auto exp_pass = [&](auto whole_c) {
-              constexpr bool kWhole = decltype(whole_c)::value;
-#pragma unroll
-              for (int j = 0; j < HW; j += 2) {
-                const int cu = h * HW + j;
-                const uint64_t x =
-                    ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
-                const int pair = (cu >> 1) & 7;
-                uint64_t e;
-                if (kFmaPairs >> pair & 1) e = ex2_fma2(x);
-                else e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
-                if (!kWhole)
-                  e = f2_bits((cu <= lim && (!WIN || cu >= lo)) ? f2_lo(e) : 0.f,
-                              (cu + 1 <= lim && (!WIN || cu + 1 >= lo)) ? f2_hi(e) : 0.f);
-                acc[pair & 3] = fadd2(acc[pair & 3], e);
-                hv[j / 2] = pack_bf16x2(f2_lo(e), f2_hi(e));
-              }
-            };
-            if (whole) exp_pass(std::true_type{});
-            else exp_pass(std::false_type{});
-          } else {
-#pragma unroll
-            for (int k = 0; k < HW / 2; ++k) hv[k] = 0u;
-          }
-          if constexpr (HW == 128) tmem_st_x64(sa, hv);
-          else tmem_st_x32_p(sa + h * (HW / 2), hv);
-        }
-        if (valid) {
-          const uint64_t a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-          const float rowsum = __fadd_rn(f2_lo(a), f2_hi(a));
-          l = __fadd_rn(__fmul_rn(l, alpha), rowsum);
-        }
-        // Rescale O where the running max moved (alpha is exactly 1 elsewhere);
-        // the first block of a segment overwrites O instead.  With one S
-        // buffer the S_FULL phase already implies the previous PV completed.
-        if (!seg_first && __any_sync(0xffffffffu, valid && alpha != 1.f)) {
-          if (C::NS == 2 && !wait_pv(cnt - 1)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t ov[32];
-            tmem_ld_x32(o_addr + c0, ov);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__fmul_rn(__uint_as_float(ov[j]), alpha));
-            tmem_st_x32(o_addr + c0, ov);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar(c, B_P_FULL + 2 * t + sbuf));
-      }
-      if (!ok) break;
-
-      // ---- segment end: O of this segment is complete after the last PV
-      if (!wait_pv(cnt - 1)) { ok = false; break; }
-      tc_fence_after();
-      const float m_seg = (m == -INFINITY) ? -INFINITY : __fmul_rn(m, scale);
-      const int vr = (pos - g.first_valid[t]) * p.group + hg;  // row among the tile's valid rows
-      if (split) {
-        const bool write = valid && s < w.nseg[t];
-        float* prow = p.partials + (size_t(w.part_base[t]) + vr) * (D + 4);
-        if (write) *reinterpret_cast<float4*>(prow) = make_float4(m_seg, l, 0.f, 0.f);
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ov[32];
-          tmem_ld_x32(o_addr + c0, ov);
-          if (write) {
-            float4* dst = reinterpret_cast<float4*>(prow + 4 + c0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]),
-                                   __uint_as_float(ov[4 * j + 2]), __uint_as_float(ov[4 * j + 3]));
-          }
-        }
-      } else {
-        const MergeStep st = merge_step(Mrun, Lrun, m_seg, l);
-        const bool last = (s == w.seg_hi);
-        const bool use_scratch = (w.seg_hi > w.seg_lo);
-        const float osc = last ? out_scale(st.l, p.v_scale) : 0.f;
-        const int tok = w.q_tok0 + pos;
-        const int head = w.kv_head * p.group + hg;
-        uint16_t* orow = p.out + (size_t(tok) * p.num_qo_heads + head) * D;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ov[32];
-          tmem_ld_x32(o_addr + c0, ov);
-          if (valid) {
-            float o[32];
-            if (use_scratch && st.kind != 1) {
-              const float4* src = reinterpret_cast<const float4*>(scratch_row + c0);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 v = src[j];
-                o[4 * j] = v.x; o[4 * j + 1] = v.y; o[4 * j + 2] = v.z; o[4 * j + 3] = v.w;
-              }
-#pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = merge_elem(st, o[j], __uint_as_float(ov[j]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(ov[j]);
-            }
-            if (!last) {
-              float4* dst = reinterpret_cast<float4*>(scratch_row + c0);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                dst[j] = make_uint4(pack_bf16x2(__fmul_rn(o[8 * j + 0], osc), __fmul_rn(o[8 * j + 1], osc)),
-                                    pack_bf16x2(__fmul_rn(o[8 * j + 2], osc), __fmul_rn(o[8 * j + 3], osc)),
-                                    pack_bf16x2(__fmul_rn(o[8 * j + 4], osc), __fmul_rn(o[8 * j + 5], osc)),
-                                    pack_bf16x2(__fmul_rn(o[8 * j + 6], osc), __fmul_rn(o[8 * j + 7], osc)));
-              }
-            }
-          }
-        }
-        if (last && valid) p.lse[size_t(tok) * p.num_qo_heads + head] = final_lse(st.m, st.l);
-        Mrun = st.m;
-        Lrun = st.l;
-      }
-      tc_fence_before();
-    }
-  }
-}
-
-// Two E4M3 codes (low byte first) -> two bf16 (low half first).  Exact: every
-// E4M3 value, subnormals included, is representable in f16, f32 and bf16.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  return pack_bf16x2(f.x, f.y);
-}
-
-// FP8 pages: convert each staged block (BN rows x D codes, row-major) into the
-// bf16, 128-byte-swizzled K/V ring slot the MMAs read; V rows at or past
-// kv_len are written as zeros.  K, then V, per block; the bf16 slot is taken
-// once the MMA that last read it has completed.
-template <int D, int NT, int ST, bool KV8>
-__device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) {
-  if constexpr (KV8) {
-    using C = Cfg<D, NT, ST, KV8>;
-    const int tid = int(threadIdx.x) - C::DQ_WARP0 * 32;  // 0..127
-    constexpr int GROUPS = D / 16;                          // 16-code groups per row
-    uint32_t b = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x) {
-      const WorkItem w = p.items[it];
-      const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
-      for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {
-        const int ss = b % C::SS, slot = b % ST;
-        const uint32_t suse = b / C::SS, use = b / ST;
-        const int valid_rows = w.kv_len - blk * C::BN;
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-          const int full8 = which ? B_V8_FULL : B_K8_FULL, free8 = which ? B_V8_FREE : B_K8_FREE;
-          const int full = which ? B_V_FULL : B_K_FULL, freeb = which ? B_V_FREE : B_K_FREE;
-          if (!wait_warp(c, bar(c, full8 + ss), suse & 1, 30 + which)) { ok = false; break; }
-          if (use > 0 && !wait_warp(c, bar(c, freeb + slot), (use - 1) & 1, 32 + which)) { ok = false; break; }
-          const uint32_t src = sbase + (which ? C::OFF_V8 : C::OFF_K8) + ss * C::KV8_BYTES;
-          const uint32_t dst = sbase + (which ? C::OFF_V : C::OFF_K) + slot * C::KV_BYTES;
-          for (int u = tid; u < C::BN * GROUPS; u += 128) {
-            const int r = u / GROUPS, gi = u % GROUPS;
-            uint32_t x, y, z, q;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x), "=r"(y), "=r"(z), "=r"(q)
-                         : "r"(src + r * D + gi * 16));
-            uint32_t o[8] = {e4m3x2_to_bf16x2(x), e4m3x2_to_bf16x2(x >> 16), e4m3x2_to_bf16x2(y),
-                             e4m3x2_to_bf16x2(y >> 16), e4m3x2_to_bf16x2(z), e4m3x2_to_bf16x2(z >> 16),
-                             e4m3x2_to_bf16x2(q), e4m3x2_to_bf16x2(q >> 16)};
-            if (which == 1 && r >= valid_rows) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) o[j] = 0u;
-            }
-            const int ch = gi >> 2, u8 = (gi & 3) * 2;
-            const uint32_t rowb = dst + ch * C::KV_CHUNK + r * 128;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + ((u8 ^ (r & 7)) << 4)), "r"(o[0]),
-                         "r"(o[1]), "r"(o[2]), "r"(o[3])
-                         : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + (((u8 + 1) ^ (r & 7)) << 4)),
-                         "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(bar(c, full + slot));
-          mbar_arrive(bar(c, free8 + ss));
-        }
-      }
-    }
-  }
-}
-
-template <int D, int NT, int ST, bool KV8, bool WIN>
-__global__ void __launch_bounds__(Cfg<D, NT, ST, KV8>::THREADS, 1)
-    bip_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using C = Cfg<D, NT, ST, KV8>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  const uint32_t sbase = raw + pad;
-  const int warp = threadIdx.x >> 5;
-
-  Ctx c;
-  c.bar0 = sbase + C::OFF_BAR;
-  c.abort = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + OFF_ABORT);
-  c.header = p.header;
-  c.limit_cycles = p.wait_limit_cycles;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + OFF_TMEM_SLOT);
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(c, B_Q_FULL), 1);
-    mbar_init(bar(c, B_Q_FREE), 1);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(bar(c, B_K_FULL + s), KV8 ? 128 : 1);  // FP8: the dequant warps arrive
-      mbar_init(bar(c, B_K_FREE + s), 1);
-      mbar_init(bar(c, B_V_FULL + s), KV8 ? 128 : 1);
-      mbar_init(bar(c, B_V_FREE + s), 1);
-    }
-    for (int s = 0; s < C::SS; ++s) {
-      mbar_init(bar(c, B_K8_FULL + s), 1);
-      mbar_init(bar(c, B_K8_FREE + s), 128);
-      mbar_init(bar(c, B_V8_FULL + s), 1);
-      mbar_init(bar(c, B_V8_FREE + s), 128);
-    }
-    for (int t = 0; t < NT; ++t)
-      for (int s = 0; s < C::NS; ++s) {
-        mbar_init(bar(c, B_S_FULL + 2 * t + s), 1);
-        mbar_init(bar(c, B_P_FULL + 2 * t + s), 128);
-        mbar_init(bar(c, B_O_DONE + 2 * t + s), 1);
-      }
-    mbar_init(bar(c, B_DRAIN), 1);
-    mbar_init(bar(c, B_V_TX), 1);
-    *c.abort = 0u;
-    fence_mbar_init();
-  }
-  if (warp == C::CTL_WARP0 + 1) {
-    tmem_alloc(smem_addr(tmem_slot), C::TM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-
-  const int lane = threadIdx.x & 31;
-  if (warp < C::SM_WARPS) {
-    if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
-    softmax_role<D, NT, ST, KV8, WIN>(c, tmem, p, warp / 4);
-  } else if (warp < C::CTL_WARP0) {
-    dequant_role<D, NT, ST, KV8>(c, sbase, p);
-  } else {
-    if constexpr (C::SPLIT_REGS) reg_dealloc<C::CTL_REGS>();
-    const int role = warp - C::CTL_WARP0;
-    if (role == 0) {
-      if (lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-      }
-      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_k, p, false);
-    } else if (role == 1) {
-      if (lane == 0) mma_issuer<D, NT, ST, KV8>(c, sbase, tmem, p);
-    } else if (role == 2) {
-      if (lane == 0) prefetch_tmap(&tm_v);
-      producer<D, NT, ST, KV8>(c, sbase, &tm_q, &tm_v, p, true);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == C::CTL_WARP0 + 1) tmem_dealloc(tmem, C::TM_COLS);
-}
-
-// The sliding-window mask is a separate instantiation, so that the plain
-// causal kernel carries none of its arithmetic.
-template <int D, int NT, int ST, bool KV8, bool WIN>
-cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                       int grid, cudaStream_t stream) {
-  using C = Cfg<D, NT, ST, KV8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D, NT, ST, KV8, WIN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  bip_attn_kernel<D, NT, ST, KV8, WIN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
-}
-
-template <int D, int NT, int ST, bool KV8>
-cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                   int grid, cudaStream_t stream) {
-  return p.window_left > 0 ? launch_one<D, NT, ST, KV8, true>(tq, tk, tv, p, grid, stream)
-                           : launch_one<D, NT, ST, KV8, false>(tq, tk, tv, p, grid, stream);
-}
-
-}  // namespace
 
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
                              cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+  if (p.page_size < 8) return launch_attention_gather(head_dim, tiles_per_unit, kv_fp8, tm_q, tm_k, tm_v, p, grid,
+                                                      stream);
   if (!kv_fp8) {
-    if (head_dim == 128 && tiles_per_unit == 2) return launch<128, 2, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 128 && tiles_per_unit == 1) return launch<128, 1, 3, false>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 256 && tiles_per_unit == 1) return launch<256, 1, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128 && tiles_per_unit == 2)
+      return launch<128, 2, 2, false, false>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128 && tiles_per_unit == 1)
+      return launch<128, 1, 3, false, false>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 256 && tiles_per_unit == 1)
+      return launch<256, 1, 2, false, false>(tm_q, tm_k, tm_v, p, grid, stream);
   } else if (tiles_per_unit == 1) {
-    if (head_dim == 128) return launch<128, 1, 2, true>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 256) return launch<256, 1, 2, true>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128) return launch<128, 1, 2, true, false>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 256) return launch<256, 1, 2, true, false>(tm_q, tm_k, tm_v, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -179,7 +179,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   if (kv_dtype != BIP_KV_BF16 && kv_dtype != BIP_KV_FP8_E4M3) return BIP_ERR_INVALID_ARG;
   const int32_t bn = bip::kv_block_for(head_dim);
   if (page_size <= 0) return BIP_ERR_INVALID_ARG;
-  if ((page_size & (page_size - 1)) != 0 || page_size < 8 || page_size > bn) return BIP_ERR_UNSUPPORTED;
+  if ((page_size & (page_size - 1)) != 0 || page_size > bn) return BIP_ERR_UNSUPPORTED;
 
   bip_plan_options opts;
   opts.split_policy = BIP_SPLIT_AUTO;
@@ -196,8 +196,9 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
   if (opts.tiles_per_unit < 0 || opts.tiles_per_unit > bip::max_tiles_per_unit_for(head_dim))
     return BIP_ERR_INVALID_ARG;
-  // FP8 pages run in the one-tile variant (its dequant warpgroup needs the room).
-  if (kv_dtype == BIP_KV_FP8_E4M3 && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
+  // FP8 pages and token-granular pages (below 8 slots) run one-tile variants
+  // (their dequant and row-gather warpgroups need the room).
+  if ((kv_dtype == BIP_KV_FP8_E4M3 || page_size < 8) && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
   if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
 
   // ---- lengths and validation
@@ -232,7 +233,8 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
       ++active;
       tiles += (kv_len[r] - 1) / T - (kv_len[r] - q_len[r]) / T + 1;
     }
-    NT = (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 && tiles >= 2 * active) ? 2 : 1;
+    NT = (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 && page_size >= 8 &&
+          tiles >= 2 * active) ? 2 : 1;
   }
 
   // ---- units: (request, kv head, NT consecutive absolute q tiles sharing keys)
@@ -523,6 +525,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The pools as plain pointers: page sizes below 8 gather token rows with
+// cp.async instead of TMA boxes.
+void set_pools(bip::AttnParams& ap, const void* k_pages, const void* v_pages, int64_t page_stride_bytes,
+               int32_t slot_bytes) {
+  ap.k_pool = static_cast<const uint8_t*>(k_pages);
+  ap.v_pool = static_cast<const uint8_t*>(v_pages);
+  ap.page_stride_bytes = page_stride_bytes;
+  ap.slot_bytes = slot_bytes;
+}
+
 }  // namespace
 
 // TMA descriptors of one launch.  q: [rows, Hq, d] as dims (d, Hq, rows); box
@@ -578,6 +590,7 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
       (page_stride_elems * elem) % 16 != 0)
     return BIP_ERR_INVALID_ARG;
   if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return BIP_ERR_INVALID_ARG;
+  if (p->page_size < 8 && page_stride_elems * elem > INT32_MAX) return BIP_ERR_UNSUPPORTED;  // row gather: 32-bit
 
   const bool fp8 = p->kv_dtype == BIP_KV_FP8_E4M3;
   CUtensorMap tm_q, tm_k, tm_v;
@@ -608,6 +621,7 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   ap.v_scale = v_scale;
   ap.wait_limit_cycles = p->wait_limit_cycles;
   ap.window_left = p->opts.window_left;
+  set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;
 
@@ -698,7 +712,7 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   if (kv_dtype != BIP_KV_BF16 && kv_dtype != BIP_KV_FP8_E4M3) return BIP_ERR_INVALID_ARG;
   const int32_t bn = bip::kv_block_for(head_dim);
   if (page_size <= 0) return BIP_ERR_INVALID_ARG;
-  if ((page_size & (page_size - 1)) != 0 || page_size < 8 || page_size > bn) return BIP_ERR_UNSUPPORTED;
+  if ((page_size & (page_size - 1)) != 0 || page_size > bn) return BIP_ERR_UNSUPPORTED;
   bip_plan_options opts;
   opts.split_policy = BIP_SPLIT_AUTO;
   opts.split_budget_bytes = kDefaultSplitBudget;
@@ -713,7 +727,7 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
   if (opts.tiles_per_unit < 0 || opts.tiles_per_unit > bip::max_tiles_per_unit_for(head_dim))
     return BIP_ERR_INVALID_ARG;
-  if (kv_dtype == BIP_KV_FP8_E4M3 && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
+  if ((kv_dtype == BIP_KV_FP8_E4M3 || page_size < 8) && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
   if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
 
   bip_graph_plan_s* p = new (std::nothrow) bip_graph_plan_s;
@@ -731,7 +745,8 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   // No batch statistics at capture time: two tiles per CTA wherever the
   // variant exists (numerically neutral, like every plan choice).
   p->nt = opts.tiles_per_unit ? opts.tiles_per_unit
-                              : (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 ? 2 : 1);
+                              : (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 &&
+                                         page_size >= 8 ? 2 : 1);
   int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
   p->grid = std::min(num_sms, bip::kMaxCtas);
   {
@@ -779,6 +794,7 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
       (page_stride_elems * elem) % 16 != 0)
     return BIP_ERR_INVALID_ARG;
   if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return BIP_ERR_INVALID_ARG;
+  if (p->page_size < 8 && page_stride_elems * elem > INT32_MAX) return BIP_ERR_UNSUPPORTED;  // row gather: 32-bit
   if (p->max_total_q == 0) return BIP_OK;  // no buffer rows: nothing can ever run
 
   CUtensorMap tm_q, tm_k, tm_v;
@@ -825,6 +841,7 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
   ap.v_scale = v_scale;
   ap.wait_limit_cycles = p->wait_limit_cycles;
   ap.window_left = p->window_left;
+  set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;
   return BIP_OK;

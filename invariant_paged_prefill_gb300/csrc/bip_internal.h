@@ -1,5 +1,5 @@
 // Contract between the host planner (bip_host.cpp) and the kernels
-// (bip_attn.cu, bip_merge.cu): work-list records, workspace header and
+// (attention, merge, KV append, device planner): work-list records, workspace header and
 // launch parameters.  Host and device code include it.
 #pragma once
 
@@ -87,6 +87,12 @@ struct AttnParams {
   float v_scale;
   uint64_t wait_limit_cycles;  // wait bound in SM clock cycles (the limit in ns at the peak clock)
   int32_t window_left;         // > 0: a row at position p sees keys p - window_left .. p only
+  // Pools as plain pointers, for page sizes below 8 (rows gathered with
+  // cp.async instead of TMA boxes).
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  int64_t page_stride_bytes;
+  int32_t slot_bytes;          // one token slot: num_kv_heads * head_dim * element size
 };
 
 struct MergeParams {
@@ -153,10 +159,15 @@ struct DevPlanParams {
   WsHeader* header;
 };
 
-// Kernel launchers (bip_attn.cu / bip_merge.cu / bip_append.cu / bip_plan_dev.cu).
+// Kernel launchers (bip_attn.cu / bip_attn_gather.cu / bip_merge.cu /
+// bip_append.cu / bip_plan_dev.cu).  launch_attention hands page sizes below
+// 8 to launch_attention_gather.
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
                              cudaStream_t stream);
+cudaError_t launch_attention_gather(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
+                                    const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                                    cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int head_dim, bool kv_fp8, const AppendParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_device_plan(const DevPlanParams& p, cudaStream_t stream);

@@ -83,6 +83,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// ------------------------------------------------------------ cp.async
+// One 16-byte global -> shared copy through the LSU, cached in L2 only.
+// src_bytes 0 reads nothing and writes 16 zero bytes.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// One arrival on the barrier once every cp.async this thread has issued has
+// landed.  .noinc: the arrival counts toward the barrier's expected count.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor-core operand reads, TMA) after this fence.
 __device__ __forceinline__ void fence_proxy_async_smem() {

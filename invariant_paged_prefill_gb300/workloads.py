@@ -205,7 +205,7 @@ def tiny(q_len: int, *, seed_data: int = 0, seed_pages: int = 1, kv_dtype: str =
 
 
 def radix_burst(*, n_req: int = 16, prefix: int = 1024, seed_data: int = 0, seed_pages: int = 1,
-                seed_lengths: int = 2, kv_dtype: str = "bf16", device="cpu"):
+                seed_lengths: int = 2, kv_dtype: str = "bf16", device="cpu", page_size: int = PAGE_SIZE):
     """16 requests behind a shared 1024-token prefix, tails of 1-4 tokens.
 
     Returns ``(extend, cold)``: the extend batch sends only the tails and
@@ -218,9 +218,9 @@ def radix_burst(*, n_req: int = 16, prefix: int = 1024, seed_data: int = 0, seed
     prompts = [concat_prompts(pre, make_prompt(t, hq, hkv, d, seed=seed_data + 1000 + i,
                                                kv_dtype=kv_dtype, device=device))
                for i, t in enumerate(tails)]
-    extend = layout(prompts, tails, PAGE_SIZE, seed_pages=seed_pages, share_prefix_tokens=prefix,
+    extend = layout(prompts, tails, page_size, seed_pages=seed_pages, share_prefix_tokens=prefix,
                     kv_dtype=kv_dtype)
-    cold = layout(prompts, [p.n for p in prompts], PAGE_SIZE, seed_pages=seed_pages + 100,
+    cold = layout(prompts, [p.n for p in prompts], page_size, seed_pages=seed_pages + 100,
                   kv_dtype=kv_dtype)
     return extend, cold
 
@@ -251,13 +251,14 @@ def large_head(n_tokens: int, *, seed_data: int = 0, seed_pages: int = 1, kv_dty
 
 
 def sweep_point(heads: Sequence[int], q_len: int, kv_len: int, *, batch: int = 16, kv_dtype: str = "bf16",
-                seed_data: int = 0, seed_pages: int = 1, device="cpu", poison: bool = True) -> PagedBatch:
+                seed_data: int = 0, seed_pages: int = 1, device="cpu", poison: bool = True,
+                page_size: int = PAGE_SIZE) -> PagedBatch:
     """Batch of ``batch`` requests with private pages, each ``q_len`` rows behind ``kv_len`` keys."""
     hq, hkv, d = heads
     assert kv_len >= q_len
     prompts = [make_prompt(kv_len, hq, hkv, d, seed=seed_data + 7 * i, kv_dtype=kv_dtype, device=device)
                for i in range(batch)]
-    return layout(prompts, [q_len] * batch, PAGE_SIZE, seed_pages=seed_pages, kv_dtype=kv_dtype,
+    return layout(prompts, [q_len] * batch, page_size, seed_pages=seed_pages, kv_dtype=kv_dtype,
                   poison=poison)
 
 

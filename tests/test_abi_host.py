@@ -58,6 +58,14 @@ def plan_code(qo, kv, last, hq=32, hkv=8, d=128, ps=16, kv_dtype=0, opts=None):
     (dict(qo=[0, 1], kv=[0, 1], last=[4], hq=30), 1),     # heads do not divide
     (dict(qo=[0, 1], kv=[0, 1], last=[4], d=64), 2),      # unsupported head_dim
     (dict(qo=[0, 1], kv=[0, 1], last=[4], ps=12), 2),     # page size not a power of two
+    (dict(qo=[0, 1], kv=[0, 1], last=[3], ps=3), 2),      # nor below 8
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], ps=256), 2),    # page longer than a KV block
+    (dict(qo=[0, 3], kv=[0, 3], last=[1], ps=1), 0),      # token-granular pool
+    (dict(qo=[0, 3], kv=[0, 2], last=[2], ps=2), 0),
+    (dict(qo=[0, 3], kv=[0, 1], last=[4], ps=4), 0),
+    (dict(qo=[0, 1], kv=[0, 1], last=[2], ps=1), 1),      # last page overfull at page size 1
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], hkv=4, d=256, ps=64), 0),
+    (dict(qo=[0, 1], kv=[0, 1], last=[4], hkv=4, d=256, ps=128), 2),  # d 256 runs 64-key blocks
     (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=1), 0),  # FP8 E4M3 pages
     (dict(qo=[0, 1], kv=[0, 1], last=[4], kv_dtype=9), 1),
     (dict(qo=[0, 0, 3], kv=[0, 0, 1], last=[0, 3]), 0),   # zero-length request with no pages
@@ -86,6 +94,12 @@ def test_prefill_rejects_before_touching_memory(lib):
     rc = lib.bip_prefill(plan._h, fake, 3, fake, fake, 1, 16 * 8 * 128 - 8, fake, 1.0, 1.0, fake, fake, fake,
                          plan.workspace_bytes, None)
     assert rc == 1
+    # token-granular pools gather rows with 32-bit page offsets: a page stride
+    # of 2^31 bytes or more is refused (before any launch)
+    tok = bip.Plan([0, 3], [0, 3], [1], num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=1)
+    rc = lib.bip_prefill(tok._h, fake, 3, fake, fake, 1, 1 << 30, fake, 1.0, 1.0, fake, fake, fake,
+                         tok.workspace_bytes, None)
+    assert rc == 2
     # a plan with only q_len = 0 requests has nothing to run
     empty = bip.Plan([0, 0], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
     assert lib.bip_prefill(empty._h, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, None, None, 0, None) == 0
