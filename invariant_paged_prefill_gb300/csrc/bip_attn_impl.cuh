@@ -85,16 +85,16 @@ struct Cfg {
   static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
   // Warp roles, whole warpgroups each: softmax warps 0 .. 4 NT - 1 (slot
   // t = warp / 4, TMEM lane quarter = warp % 4), then the FP8 dequant
-  // warpgroup, then (GATHER with bf16 pages) a row-gather warpgroup, two
-  // warps for K and two for V, then the control warpgroup: q/K producer,
+  // warpgroup, then (GATHER with bf16 pages) two row-gather warpgroups,
+  // four warps for K and four for V, then the control warpgroup: q/K producer,
   // MMA issuer, V producer and one spare warp.  GATHER with FP8 pages (half
   // the bytes a row) gathers with the control warpgroup's warps 3 (K) and
   // 2 (V): a fifth warpgroup would leave too few registers at launch.
   static constexpr int SM_WARPS = 4 * NT;
   static constexpr int DQ_WARP0 = SM_WARPS;
   static constexpr int GA_WARP0 = SM_WARPS + (KV8 ? 4 : 0);
-  static constexpr int GA_WARPS = GATHER && !KV8 ? 4 : 0;
-  static constexpr int GW = GATHER ? (KV8 ? 1 : 2) : 0;  // gather warps per stream (K or V)
+  static constexpr int GA_WARPS = GATHER && !KV8 ? 8 : 0;
+  static constexpr int GW = GATHER ? (KV8 ? 1 : 4) : 0;  // gather warps per stream (K or V)
   static constexpr int CTL_WARP0 = GA_WARP0 + GA_WARPS;
   static constexpr int THREADS = 32 * (CTL_WARP0 + 4);
   // Register split: launches of more than 256 threads start at LAUNCH_REGS
@@ -104,7 +104,7 @@ struct Cfg {
   // launch holds.
   static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;
   static constexpr bool SPLIT_REGS = THREADS > 256;
-  static constexpr int CTL_REGS = KV8 ? 80 : (GATHER ? 64 : 56);  // FP8: softmax is capped at 240 anyway
+  static constexpr int CTL_REGS = KV8 ? 80 : (GATHER ? 72 : 56);  // FP8: softmax is capped at 240 anyway
   static constexpr int GA_REGS = 56;
   static constexpr int FIXED_REGS = CTL_REGS * 128 + GA_REGS * 32 * GA_WARPS + (KV8 ? LAUNCH_REGS * 128 : 0);
   static constexpr int SM_REGS_FREE = ((LAUNCH_REGS * THREADS - FIXED_REGS) / (32 * SM_WARPS)) & ~7;
@@ -588,7 +588,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
   drain_wait(bar(c, B_DRAIN), 0);
 }
 
-template <int D, int NT, int ST, bool KV8, bool WIN>
+template <int D, int NT, int ST, bool KV8, bool WIN, bool NARROW_LD>
 __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t) {
   using C = Cfg<D, NT, ST, KV8>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -676,8 +676,14 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         };
         if (live) {
-          if constexpr (C::BN == 128) tmem_ld_x128(sa, sv);
-          else tmem_ld_x64(sa, sv);
+          if constexpr (C::BN == 128 && !NARROW_LD) {
+            tmem_ld_x128(sa, sv);
+          } else if constexpr (C::BN == 128) {  // launches of 128 registers a thread: no 128-wide load
+            tmem_ld_x64(sa, *reinterpret_cast<uint32_t(*)[64]>(sv));
+            tmem_ld_x64(sa + 64, *reinterpret_cast<uint32_t(*)[64]>(sv + 64));
+          } else {
+            tmem_ld_x64(sa, sv);
+          }
           mx = whole ? block_max(std::true_type{}) : block_max(std::false_type{});
         }
         float alpha = 1.f;
@@ -963,7 +969,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   if (warp < C::SM_WARPS) {
     if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
-    softmax_role<D, NT, ST, KV8, WIN>(c, tmem, p, warp / 4);
+    softmax_role<D, NT, ST, KV8, WIN, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4);
   } else if (warp < C::GA_WARP0) {
     dequant_role<D, NT, ST, KV8>(c, sbase, p);
   } else if (warp < C::CTL_WARP0) {
