@@ -142,6 +142,19 @@ def test_graph_plan_validation_and_sizes(lib):
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 0, ctypes.byref(opts), None) == 2
     opts = _lib.PlanOptions(0, 1 << 20, 0, 0, 2)   # FP8 pages use the one-tile variant
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 1, ctypes.byref(opts), None) == 2
+    # so do token-granular pools (the row-gather warps take the second tile's room)
+    assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 4, 0, ctypes.byref(opts), None) == 2
+    assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 8, 0, ctypes.byref(opts), None) == 0
+    lib.bip_graph_plan_destroy(h)
+
+
+def test_token_granular_plans_run_one_tile_per_cta(lib):
+    qo, kv, last = [0, 8192], [0, 8192], [1]   # one 8192-token fresh prefill, one slot a page
+    p1 = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=1)
+    p16 = bip.Plan(qo, [0, 512], [16], num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    assert p16.info["tiles_per_unit"] == 2 and p1.info["tiles_per_unit"] == 1
+    assert plan_code(qo, kv, last, ps=1, opts=ctypes.byref(_lib.PlanOptions(0, 1 << 20, 0, 0, 2))) == 2
+    assert plan_code(qo, kv, last, ps=1, opts=ctypes.byref(_lib.PlanOptions(0, 1 << 20, 0, 0, 1))) == 0
 
 
 def test_window_plans_skip_keys_and_reject_negative_windows(lib):

@@ -1,11 +1,12 @@
 """Model check of the attention kernel's mbarrier schedule (CPU, no GPU).
 
-The kernel's roles (two TMA streams -- q tiles and K, and V --, optional FP8
-dequant warpgroup, tcgen05
-issuer, one softmax warpgroup per q-tile slot of 4 warps) synchronise through
+The kernel's roles (two TMA streams -- q tiles and K, and V -- or, for
+token-granular pages, a q-tile stream and row-gather warps; an optional FP8
+dequant warpgroup; the tcgen05 issuer; one softmax warpgroup per q-tile slot
+of 4 warps) synchronise through
 mbarriers waited on by phase parity.  This test replays that schedule -- the
 same waits, arrivals and commits, in the same order per role as
-csrc/bip_attn.cu -- with random completion delays for TMA loads and MMAs and
+csrc/bip_attn_impl.cuh -- with random completion delays for TMA loads and MMAs and
 random interleavings of the roles, for every kernel variant, and checks two
 properties on many schedules:
 
@@ -39,20 +40,24 @@ class _Bar:
         return (self.phase & 1) != parity
 
 
-def _simulate(NT, NS, ST, SS, items, seed, warps=4):
-    """items: list of (nb, mask); SS > 0 models FP8 staging + dequant."""
+def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0):
+    """items: list of (nb, mask); SS > 0 models FP8 staging + dequant; GW > 0
+    models token-granular pages: GW row-gather warps per stream, whose 32
+    lanes each arrive on the landing barrier when their own copies land,
+    and a q/K producer that loads q tiles only."""
     rnd = random.Random(seed)
     B = {}
 
     def bar(name, count=1):
         B.setdefault(name, _Bar(count))
 
+    land = 32 * GW if GW else 1
     for s in range(ST):
         for n in ("K_FULL", "V_FULL"):
-            bar(f"{n}{s}", 128 if SS else 1)
+            bar(f"{n}{s}", 128 if SS else land)
         bar(f"K_FREE{s}"), bar(f"V_FREE{s}")
     for s in range(SS):
-        bar(f"K8_FULL{s}"), bar(f"V8_FULL{s}"), bar(f"K8_FREE{s}", 128), bar(f"V8_FREE{s}", 128)
+        bar(f"K8_FULL{s}", land), bar(f"V8_FULL{s}", land), bar(f"K8_FREE{s}", 128), bar(f"V8_FREE{s}", 128)
     for t in range(NT):
         for s in range(NS):
             bar(f"S_FULL{t}{s}"), bar(f"P_FULL{t}{s}", 32 * warps), bar(f"O_DONE{t}{s}")
@@ -61,6 +66,30 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
 
     def later(name, lo=1, hi=8):
         pending.append((clock[0] + rnd.randint(lo, hi), name))
+
+    def gatherer(is_v):
+        """One row-gather warp: the same block schedule as the TMA producer;
+        each lane's copies land after their own delay, then that lane
+        arrives."""
+        ring = SS if SS else ST
+        kv = ("V8" if SS else "V") if is_v else ("K8" if SS else "K")
+        b = 0
+        for nb, _ in items:
+            for _ in range(nb):
+                slot, use = b % ring, b // ring
+                if use > 0:
+                    yield wait(f"{kv}_FREE{slot}", use - 1)
+                for _ in range(32):
+                    later(f"{kv}_FULL{slot}", 1, 12)
+                b += 1
+                yield None
+
+    def q_loader():
+        for n in range(len(items)):
+            if n > 0:
+                yield wait("Q_FREE", n - 1)
+            later("Q_FULL")
+            yield None
 
     def commit(name):
         last_mma[0] = max(last_mma[0], clock[0]) + rnd.randint(1, 5)
@@ -181,7 +210,11 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
                 yield None
             yield from wait_pv(cnt - 1)                            # segment end: read O
 
-    roles = [("producer_k", producer(False)), ("producer_v", producer(True)), ("issuer", issuer())]
+    if GW:
+        roles = [("q_loader", q_loader()), ("issuer", issuer())]
+        roles += [(f"gather_{kv}{w}", gatherer(kv == "v")) for kv in "kv" for w in range(GW)]
+    else:
+        roles = [("producer_k", producer(False)), ("producer_v", producer(True)), ("issuer", issuer())]
     roles += [(f"softmax{t}.{w}", softmax(t)) for t in range(NT) for w in range(warps)]
     if SS:
         roles.append(("dequant", dequant()))
@@ -215,22 +248,26 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4):
     raise AssertionError("schedule did not finish")
 
 
-VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages)
-    "d128_two_tiles": (2, 1, 2, 0),
-    "d128_one_tile": (1, 2, 3, 0),
-    "d256": (1, 2, 2, 0),
-    "d128_fp8": (1, 2, 2, 2),
-    "d256_fp8": (1, 2, 2, 1),
+VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, GW gather warps per stream)
+    "d128_two_tiles": (2, 1, 2, 0, 0),
+    "d128_one_tile": (1, 2, 3, 0, 0),
+    "d256": (1, 2, 2, 0, 0),
+    "d128_fp8": (1, 2, 2, 2, 0),
+    "d256_fp8": (1, 2, 2, 1, 0),
+    "d128_rows": (1, 2, 3, 0, 4),
+    "d256_rows": (1, 2, 2, 0, 4),
+    "d128_fp8_rows": (1, 2, 2, 2, 1),
+    "d256_fp8_rows": (1, 2, 2, 1, 1),
 }
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 def test_schedule_never_deadlocks_or_aliases(variant):
-    NT, NS, ST, SS = VARIANTS[variant]
+    NT, NS, ST, SS, GW = VARIANTS[variant]
     full = (1 << NT) - 1
     item_sets = [[(1, full)], [(9, full)], [(4, full), (1, full), (17, full)], [(3, 1), (2, full), (5, 1)]]
     if NT == 2:
         item_sets.append([(6, 2), (2, 1), (7, 3)])
     for items in item_sets:
-        for seed in range(60):
-            _simulate(NT, NS, ST, SS, items, seed)
+        for seed in range(60 if not GW else 25):
+            _simulate(NT, NS, ST, SS, items, seed, GW=GW)

@@ -104,6 +104,8 @@ SDPA_CASES = [
     ([(7, 7), (3, 11), (1, 5), (0, 4), (5, 9)], 8, 2, 16, 4),
     ([(4, 13), (13, 13)], 6, 1, 8, 16),
     ([(2, 2), (6, 21)], 12, 2, 32, 4),
+    ([(3, 9), (9, 9)], 4, 2, 16, 1),     # token-granular pools
+    ([(5, 10), (1, 7)], 4, 1, 8, 2),
 ]
 
 
