@@ -35,8 +35,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged prefill attn TFLOP/s (long q) & KV-read GB/s (short extends), bit-exact"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["bip_host.cpp", "bip_attn.cu", "bip_merge.cu", "bip_internal.h", "bip_numerics.cuh",
-                  "bip_ptx.cuh"]
+KERNEL_SOURCES = ["bip_host.cpp", "bip_attn.cu", "bip_attn_gather.cu", "bip_attn_impl.cuh", "bip_merge.cu",
+                  "bip_append.cu", "bip_plan_dev.cu", "bip_internal.h", "bip_numerics.cuh", "bip_ptx.cuh"]
 
 
 # ----------------------------------------------------------------- helpers
@@ -543,10 +543,15 @@ def run_ours(args):
         r1, sr1 = Runner(b1, device), Runner(sb1, device)
         p1_total, _ = r1.timed(args.steps, args.warmup)
         sp1_total, _ = sr1.timed(args.steps, args.warmup)
+        p1_gbs = kvb / (sp1_total / args.steps * 1e-3) / 1e9
         line["page_size_1"] = {
+            "what": "token-granular pools: K and V rows gathered by cp.async warps (one q tile per CTA)",
             "long_q_tflops": fl / (p1_total / args.steps * 1e-3) / 1e12,
-            "short_extend_kv_gbs": kvb / (sp1_total / args.steps * 1e-3) / 1e9,
+            "short_extend_kv_gbs": p1_gbs,
             "short_extend_ms": sp1_total / args.steps,
+            "short_extend_roofline": {"bound": "hbm", "achieved": p1_gbs, "peak": hbm, "unit": "GB/s",
+                                      "frac": p1_gbs / hbm, "peak_source": f"hbm_gbs of {peak_kind}",
+                                      "traffic": recorded_traffic("short_extend_page1")},
             "bit_exact_vs_page_16": bool(torch.equal(r1.out, run.out) and torch.equal(r1.lse, run.lse) and
                                          torch.equal(sr1.out, srun.out) and torch.equal(sr1.lse, srun.lse))}
         del r1, sr1, b1, sb1
@@ -593,13 +598,14 @@ def run_profile(args):
         return
     heads, batch, q_len, kv_len = WORKLOADS[args.workload]
     batch = args.batch or batch
-    b = make_batch(heads, batch, q_len, kv_len, device)
+    b = make_batch(heads, batch, q_len, kv_len, device, page_size=args.page_size)
     run = Runner(b, device)
     total, per = run.timed(args.steps, args.warmup)
     ms = statistics.mean(per)
     fl = flops_of(heads, b.q_lens, b.kv_lens)
     kvb = kv_bytes_of(heads, b.kv_lens)
-    print(json.dumps({"profile": args.workload, "batch": batch, "ms": ms, "tflops": fl / ms / 1e9,
+    print(json.dumps({"profile": args.workload, "page_size": args.page_size, "batch": batch, "ms": ms,
+                      "tflops": fl / ms / 1e9,
                       "kv_gbs": kvb / ms / 1e6, "launches_per_step": run.launches_per_step,
                       "items": run.plan.info["num_items"], "grid": run.plan.info["grid"],
                       "source_hash": source_hash()}), flush=True)
@@ -643,6 +649,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--profile", action="store_true", help="time only the main step (for ncu captures)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
+    ap.add_argument("--page-size", type=int, default=16, help="with --profile: slots per KV page")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
