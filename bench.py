@@ -618,7 +618,7 @@ def run_sweep(args):
     device = torch.device("cuda:0")
     peaks, kind = load_peaks()
     for heads, q_len, kv_len in W.sweep_grid():
-        b = make_batch(heads, 16, q_len, kv_len, device)
+        b = make_batch(heads, 16, q_len, kv_len, device, page_size=args.page_size)
         try:
             run = Runner(b, device)
         except Exception as e:  # unsupported shapes are reported, not fatal
@@ -628,7 +628,8 @@ def run_sweep(args):
         ms = statistics.mean(per)
         fl = flops_of(heads, b.q_lens, b.kv_lens)
         kvb = kv_bytes_of(heads, b.kv_lens)
-        print(json.dumps({"heads": list(heads), "batch": 16, "q_len": q_len, "kv_len": kv_len, "ms": ms,
+        print(json.dumps({"heads": list(heads), "batch": 16, "page_size": args.page_size, "q_len": q_len,
+                          "kv_len": kv_len, "ms": ms,
                           "tflops": fl / ms / 1e9, "tensor_frac": fl / ms / 1e9 / peaks["bf16_tflops"],
                           "kv_gbs": kvb / ms / 1e6, "hbm_frac": kvb / ms / 1e6 / peaks["hbm_gbs"],
                           "items": run.plan.info["num_items"], "split_units": run.plan.info["num_split_units"]}),
@@ -649,7 +650,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--profile", action="store_true", help="time only the main step (for ncu captures)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
-    ap.add_argument("--page-size", type=int, default=16, help="with --profile: slots per KV page")
+    ap.add_argument("--page-size", type=int, default=16, help="with --profile or --sweep: slots per KV page")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
