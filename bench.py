@@ -161,7 +161,8 @@ class Runner:
         self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty_like(b.q)
         self.lse = torch.empty(b.q.shape[0], b.q.shape[1], dtype=torch.float32, device=device)
-        self.launches_per_step = 1 + (1 if self.plan.info["num_split_units"] else 0)
+        # work-list upload kernel + attention (+ merge when units are split)
+        self.launches_per_step = 2 + (1 if self.plan.info["num_split_units"] else 0)
 
     def step(self, q=None, kp=None, vp=None, idx=None):
         b = self.b

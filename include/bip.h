@@ -163,8 +163,10 @@ bip_status bip_plan_destroy(bip_plan_t plan);
  *   out      bf16 [num_q_rows, num_qo_heads, head_dim]
  *   lse      fp32 [num_q_rows, num_qo_heads], natural log
  *   workspace  >= the plan's workspace_bytes, 256-byte aligned; its first
- *            bytes receive this call's work list (one host->device copy on
- *            `stream`) and a status word.
+ *            bytes receive this call's work list and a status word, copied
+ *            on `stream` by a small kernel that reads the plan's pinned,
+ *            mapped host image (so the call never waits behind bulk copies
+ *            that other streams have queued on the copy engines).
  * q, pages and out must be 16-byte aligned; page_stride_elems * element size
  * must be a multiple of 16 bytes (and, for page sizes below 8, below 2^31
  * bytes, else BIP_ERR_UNSUPPORTED).  k_scale multiplies the logits (folded

@@ -61,6 +61,7 @@ struct bip_plan_s {
   size_t off_items = 0, off_merges = 0, off_reqs = 0, off_partials = 0, off_scratch = 0;
   size_t partial_bytes = 0, scratch_bytes = 0, ws_bytes = 0, upload_bytes = 0;
   uint8_t* upload = nullptr;  // header + items + merges, as copied to the workspace
+  const void* upload_dev = nullptr;  // the same pinned buffer as the device sees it (mapped), if it is
   bool pinned = false;
 };
 
@@ -430,8 +431,13 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
 
   // ---- host image of what each call uploads: header + items + merge units
   void* buf = nullptr;
-  if (cudaMallocHost(&buf, p->upload_bytes) == cudaSuccess) {
+  if (cudaHostAlloc(&buf, p->upload_bytes, cudaHostAllocMapped | cudaHostAllocPortable) == cudaSuccess) {
     p->pinned = true;
+    void* dev = nullptr;
+    if (cudaHostGetDevicePointer(&dev, buf, 0) == cudaSuccess && (reinterpret_cast<uintptr_t>(dev) & 15) == 0)
+      p->upload_dev = dev;
+    else
+      cudaGetLastError();
   } else {
     cudaGetLastError();
     buf = std::malloc(p->upload_bytes);
@@ -537,6 +543,14 @@ void set_pools(bip::AttnParams& ap, const void* k_pages, const void* v_pages, in
 
 }  // namespace
 
+// The first `bytes` of the plan's host image into the workspace, on `stream`:
+// by the upload kernel when the pinned image is mapped into the device's
+// address space, else by one copy-engine copy.
+cudaError_t upload(const bip_plan_s* p, uint8_t* ws, size_t bytes, cudaStream_t stream) {
+  if (p->upload_dev) return bip::launch_upload(p->upload_dev, ws, bytes, stream);
+  return cudaMemcpyAsync(ws, p->upload, bytes, cudaMemcpyHostToDevice, stream);
+}
+
 // TMA descriptors of one launch.  q: [rows, Hq, d] as dims (d, Hq, rows); box
 // (64, group, T) = one tile chunk.  pages: [pages, slot, Hkv, d] as dims (d,
 // Hkv, slot, page).  bf16: box (64, 1, page_size, 1), one 128-byte-swizzled
@@ -599,8 +613,7 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
     return BIP_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemcpyAsync(ws, p->upload, p->upload_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return BIP_ERR_CUDA;
+  if (upload(p, ws, p->upload_bytes, stream) != cudaSuccess) return BIP_ERR_CUDA;
 
   bip::AttnParams ap;
   ap.items = reinterpret_cast<const WorkItem*>(ws + p->off_items);
@@ -667,8 +680,7 @@ extern "C" bip_status bip_append_kv(bip_plan_t p, const void* k_new, const void*
 
   // header (status word cleared) and request rows only
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemcpyAsync(ws, p->upload, p->off_items, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return BIP_ERR_CUDA;
+  if (upload(p, ws, p->off_items, stream) != cudaSuccess) return BIP_ERR_CUDA;
   bip::AppendParams ap;
   ap.rows = reinterpret_cast<const bip::AppendRow*>(ws + p->off_reqs);
   ap.n_rows = int32_t(p->reqs.size());

@@ -160,7 +160,7 @@ struct DevPlanParams {
 };
 
 // Kernel launchers (bip_attn.cu / bip_attn_gather.cu / bip_merge.cu /
-// bip_append.cu / bip_plan_dev.cu).  launch_attention hands page sizes below
+// bip_append.cu / bip_plan_dev.cu / bip_upload.cu).  launch_attention hands page sizes below
 // 8 to launch_attention_gather.
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
@@ -171,5 +171,8 @@ cudaError_t launch_attention_gather(int head_dim, int tiles_per_unit, bool kv_fp
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int head_dim, bool kv_fp8, const AppendParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_device_plan(const DevPlanParams& p, cudaStream_t stream);
+// bytes (a multiple of 16) from a device-visible pinned host buffer to the
+// workspace, by SM loads (bip_upload.cu).
+cudaError_t launch_upload(const void* src_dev, void* dst, size_t bytes, cudaStream_t stream);
 
 }  // namespace bip
