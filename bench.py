@@ -407,6 +407,76 @@ def windowed_work(heads, q_lens, kv_lens, window: int):
     return 4 * d * hq * pairs, keys * 2 * hkv * d * 2
 
 
+def measure_configs(device, reps: int = 20):
+    """The smaller configurations of the benchmark's list: bit-exactness checks
+    and latencies (median of ``reps`` CUDA-event timings per call, inputs
+    resident; these are latency figures, not L2-flushed throughput)."""
+    from invariant_paged_prefill_gb300 import workloads as W
+    import invariant_paged_prefill_gb300 as bip
+
+    def timed_run(b):
+        r = Runner(b, device)
+        r.step()
+        torch.cuda.synchronize()
+        st = bip.read_device_status(r.ws)
+        s = torch.cuda.current_stream()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            r.step()
+            e1.record(s)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return r.out.cpu(), r.lse.cpu(), statistics.median(ts), st, r
+
+    def rows_equal(o1, l1, a, o2, l2, b2, n):
+        return bool(torch.equal(o1[a:a + n], o2[b2:b2 + n]) and torch.equal(l1[a:a + n], l2[b2:b2 + n]))
+
+    res = {}
+    # tiny: a 64-token prefill and the 3-row extend behind its 61-token prefix
+    fo, fl, f_ms, f_st, _ = timed_run(W.tiny(64, device=device))
+    eo, el, e_ms, e_st, _ = timed_run(W.tiny(3, device=device))
+    res["tiny"] = {"extend_rows_bit_exact": rows_equal(eo, el, 0, fo, fl, 61, 3) and f_st == 0 and e_st == 0,
+                   "prefill_us": f_ms * 1e3, "extend_us": e_ms * 1e3}
+    # radix-hit burst: 16 extends behind a shared 1024-token prefix vs the cold prefill
+    ext, cold = W.radix_burst(device=device)
+    xo, xl, x_ms, x_st, _ = timed_run(ext)
+    co, cl, c_ms, c_st, _ = timed_run(cold)
+    ok = x_st == 0 and c_st == 0
+    for r in range(len(ext.q_lens)):
+        ok &= rows_equal(xo, xl, int(ext.qo_indptr[r]), co, cl,
+                         int(cold.qo_indptr[r]) + ext.kv_lens[r] - ext.q_lens[r], ext.q_lens[r])
+    res["radix_burst"] = {"extend_rows_bit_exact_vs_cold": bool(ok), "extend_latency_us": x_ms * 1e3,
+                          "extend_rows": int(ext.q.shape[0]), "cold_ms": c_ms,
+                          "cold_tflops": flops_of(W.HEADS_A, cold.q_lens, cold.kv_lens) / (c_ms * 1e-3) / 1e12}
+    # mixed ragged batch: each request against itself alone and against its own full prefill
+    prompts, q_lens = W.mixed_ragged_prompts(device=device)
+    mixed = W.layout(prompts, q_lens, 16, seed_pages=1)
+    mo, ml, m_ms, m_st, _ = timed_run(mixed)
+    ok = m_st == 0
+    for r, (p, ql) in enumerate(zip(prompts, q_lens)):
+        ao, al, _, a_st, _ = timed_run(W.layout([p], [ql], 16, seed_pages=5 + r))
+        po, pl, _, p_st, _ = timed_run(W.layout([p], [p.n], 16, seed_pages=9 + r))
+        m0 = int(mixed.qo_indptr[r])
+        ok &= a_st == 0 and p_st == 0 and rows_equal(mo, ml, m0, ao, al, 0, ql)
+        ok &= rows_equal(mo, ml, m0, po, pl, p.n - ql, ql)
+    res["mixed_ragged"] = {"bit_exact_vs_alone_and_full_prefill": bool(ok), "ms": m_ms,
+                           "tflops": flops_of(W.HEADS_A, mixed.q_lens, mixed.kv_lens) / (m_ms * 1e-3) / 1e12}
+    # large-head GQA: single fresh prefills of 8192 and 32768 tokens, 24/4/256
+    for n in (8192, 32768):
+        lb = W.large_head(n, device=device)
+        _, _, l_ms, l_st, r = timed_run(lb)
+        bound = bip.workspace_bound(1, n, 24, 4, 256)
+        tf = flops_of(W.HEADS_B, lb.q_lens, lb.kv_lens) / (l_ms * 1e-3) / 1e12
+        res[f"large_head_{n}"] = {"ms": l_ms, "tflops": tf,
+                                  "status": l_st, "workspace_bytes": r.plan.workspace_bytes,
+                                  "workspace_bound_bytes": bound,
+                                  "within_bound": r.plan.workspace_bytes <= bound}
+        del r, lb
+    return res
+
+
 def time_graph(b, device, steps: int, warmup: int):
     """Device-planned prefill captured in a CUDA graph (buffers sized to b):
     ms per replay, and whether the replay matches the host-planned result."""
@@ -577,6 +647,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": a_gbs, "peak": hbm, "unit": "GB/s", "frac": a_gbs / hbm,
                          "peak_source": f"hbm_gbs of {peak_kind}", "traffic": recorded_traffic("append")},
             "short_extend_us": sa_ms * 1e3}
+        line["configs"] = measure_configs(device)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -619,7 +690,7 @@ def run_sweep(args):
     device = torch.device("cuda:0")
     peaks, kind = load_peaks()
     for heads, q_len, kv_len in W.sweep_grid():
-        b = make_batch(heads, 16, q_len, kv_len, device, page_size=args.page_size)
+        b = make_batch(heads, 16, q_len, kv_len, device, kv_dtype=args.kv_dtype, page_size=args.page_size)
         try:
             run = Runner(b, device)
         except Exception as e:  # unsupported shapes are reported, not fatal
@@ -628,8 +699,9 @@ def run_sweep(args):
         total, per = run.timed(args.steps, args.warmup)
         ms = statistics.mean(per)
         fl = flops_of(heads, b.q_lens, b.kv_lens)
-        kvb = kv_bytes_of(heads, b.kv_lens)
-        print(json.dumps({"heads": list(heads), "batch": 16, "page_size": args.page_size, "q_len": q_len,
+        kvb = kv_bytes_of(heads, b.kv_lens, elem=2 if args.kv_dtype == "bf16" else 1)
+        print(json.dumps({"heads": list(heads), "batch": 16, "page_size": args.page_size,
+                          "kv_dtype": args.kv_dtype, "q_len": q_len,
                           "kv_len": kv_len, "ms": ms,
                           "tflops": fl / ms / 1e9, "tensor_frac": fl / ms / 1e9 / peaks["bf16_tflops"],
                           "kv_gbs": kvb / ms / 1e6, "hbm_frac": kvb / ms / 1e6 / peaks["hbm_gbs"],
@@ -652,6 +724,7 @@ def main():
     ap.add_argument("--profile", action="store_true", help="time only the main step (for ncu captures)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
     ap.add_argument("--page-size", type=int, default=16, help="with --profile or --sweep: slots per KV page")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16", help="with --sweep: KV page type")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
