@@ -670,13 +670,14 @@ def run_profile(args):
         return
     heads, batch, q_len, kv_len = WORKLOADS[args.workload]
     batch = args.batch or batch
-    b = make_batch(heads, batch, q_len, kv_len, device, page_size=args.page_size)
+    b = make_batch(heads, batch, q_len, kv_len, device, kv_dtype=args.kv_dtype, page_size=args.page_size)
     run = Runner(b, device)
     total, per = run.timed(args.steps, args.warmup)
     ms = statistics.mean(per)
     fl = flops_of(heads, b.q_lens, b.kv_lens)
-    kvb = kv_bytes_of(heads, b.kv_lens)
-    print(json.dumps({"profile": args.workload, "page_size": args.page_size, "batch": batch, "ms": ms,
+    kvb = kv_bytes_of(heads, b.kv_lens, elem=2 if args.kv_dtype == "bf16" else 1)
+    print(json.dumps({"profile": args.workload, "page_size": args.page_size, "kv_dtype": args.kv_dtype,
+                      "batch": batch, "ms": ms,
                       "tflops": fl / ms / 1e9,
                       "kv_gbs": kvb / ms / 1e6, "launches_per_step": run.launches_per_step,
                       "items": run.plan.info["num_items"], "grid": run.plan.info["grid"],
@@ -724,7 +725,7 @@ def main():
     ap.add_argument("--profile", action="store_true", help="time only the main step (for ncu captures)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
     ap.add_argument("--page-size", type=int, default=16, help="with --profile or --sweep: slots per KV page")
-    ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16", help="with --sweep: KV page type")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16", help="with --sweep or --profile: KV page type")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -877,15 +877,29 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) 
           if (use > 0 && !wait_warp(c, bar(c, freeb + slot), (use - 1) & 1, 32 + which)) { ok = false; break; }
           const uint32_t src = sbase + (which ? C::OFF_V8 : C::OFF_K8) + ss * C::KV8_BYTES;
           const uint32_t dst = sbase + (which ? C::OFF_V : C::OFF_K) + slot * C::KV_BYTES;
-          for (int u = tid; u < C::BN * GROUPS; u += 128) {
-            const int r = u / GROUPS, gi = u % GROUPS;
-            uint32_t x, y, z, q;
+          // All of this thread's staged chunks are loaded before any is
+          // converted: each load and store is an ordered asm statement, so
+          // a load-convert-store loop would pay the shared-memory latency
+          // once per 16-code chunk.
+          constexpr int ITER = C::BN * GROUPS / 128;
+          static_assert(C::BN * GROUPS % 128 == 0, "whole chunks per thread");
+          uint32_t raw[ITER][4];
+#pragma unroll
+          for (int k = 0; k < ITER; ++k) {
+            const int u = tid + 128 * k, r = u / GROUPS, gi = u % GROUPS;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x), "=r"(y), "=r"(z), "=r"(q)
+                         : "=r"(raw[k][0]), "=r"(raw[k][1]), "=r"(raw[k][2]), "=r"(raw[k][3])
                          : "r"(src + r * D + gi * 16));
-            uint32_t o[8] = {e4m3x2_to_bf16x2(x), e4m3x2_to_bf16x2(x >> 16), e4m3x2_to_bf16x2(y),
-                             e4m3x2_to_bf16x2(y >> 16), e4m3x2_to_bf16x2(z), e4m3x2_to_bf16x2(z >> 16),
-                             e4m3x2_to_bf16x2(q), e4m3x2_to_bf16x2(q >> 16)};
+          }
+#pragma unroll
+          for (int k = 0; k < ITER; ++k) {
+            const int u = tid + 128 * k, r = u / GROUPS, gi = u % GROUPS;
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              o[2 * j] = e4m3x2_to_bf16x2(raw[k][j]);
+              o[2 * j + 1] = e4m3x2_to_bf16x2(raw[k][j] >> 16);
+            }
             if (which == 1 && r >= valid_rows) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) o[j] = 0u;
