@@ -253,11 +253,17 @@ class Runner:
         for i in range(warmup):
             one(i)
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(steps):
-            one(i)
-        torch.cuda.synchronize()
-        dt = (time.perf_counter() - t0) / steps
+        # The host link is shared with the node's other GPUs: a loop now and
+        # then stalls for tens of milliseconds.  Three timed loops, median.
+        runs = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            for i in range(steps):
+                one(i)
+            torch.cuda.synchronize()
+            runs.append((time.perf_counter() - t0) / steps)
+        dt = statistics.median(runs)
+        self.e2e_runs_ms = [r * 1e3 for r in runs]
         h2d = hq.numel() * hq.element_size() + hk.numel() + hv.numel() + hidx.numel() * 4
         d2h = self.out.numel() * self.out.element_size() + self.lse.numel() * self.lse.element_size()
         ref = self.out.cpu()
@@ -588,7 +594,9 @@ def run_ours(args):
                                  "sample": f"{len(rows)} q rows of request 0, all heads, float64",
                                  "seconds": odt},
                 "e2e": {"value": world * fl / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h},
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                        "runs_ms_per_step": run.e2e_runs_ms,
+                        "note": "median of three timed loops of pipelined steps (copies in, prefill, copies out)"},
                 "gpu_launches": launches, "clocks": clk.summary(), "kv_read": kv_read,
                 "parity": {"rows": len(rows), "within_tolerance": parity_ok,
                            "max_abs_out": float(np.abs(got - ro).max()), "max_abs_lse": float(np.abs(gl - rl).max())},
