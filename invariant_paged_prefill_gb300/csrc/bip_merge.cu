@@ -6,7 +6,7 @@
 // fixed 4096-token splits, batch_prefill_tmp_v); here their number is
 // bounded by the plan's split budget.
 //
-// One CTA (4 warps) per merge unit; one warp per valid row; lane L holds
+// One CTA (8 warps) per merge unit; one warp per valid row; lane L holds
 // columns {c * 128 + 4 L .. +3}.  Element arithmetic is per column, so the
 // distribution over lanes does not change any bit.
 
@@ -18,31 +18,51 @@
 namespace bip {
 namespace {
 
+constexpr int kMergeThreads = 256;  // one warp per valid row, eight rows at a time
+
 template <int D>
-__global__ void __launch_bounds__(128) bip_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) bip_merge_kernel(const MergeParams p) {
   constexpr int E = D / 128;  // float4 groups per lane
+  constexpr int G = 4;        // segments whose partials are loaded before any is folded
+  constexpr int W = kMergeThreads / 32;
   const MergeUnit u = p.units[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int first_valid = max(u.tile * p.tile_pos, u.q_lo);
-  for (int vr = warp; vr < u.rows; vr += 4) {
+  for (int vr = warp; vr < u.rows; vr += W) {
     float o[E][4];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e][0] = o[e][1] = o[e][2] = o[e][3] = 0.f;
     float M = -INFINITY, L = 0.f;
-    for (int s = 0; s < u.nseg; ++s) {
-      const float* prow = p.partials + (size_t(u.part_base) + size_t(s) * u.rows + vr) * (D + 4);
-      const float2 ml = *reinterpret_cast<const float2*>(prow);
-      const MergeStep st = merge_step(M, L, ml.x, ml.y);
+    for (int s0 = 0; s0 < u.nseg; s0 += G) {
+      // The loads of a group do not depend on the folds before them, so
+      // they are all issued first: one memory latency per group of
+      // segments instead of one per segment.  The fold order is unchanged.
+      float2 ml[G];
+      float4 v[G][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float4 v = *reinterpret_cast<const float4*>(prow + 4 + e * 128 + lane * 4);
-        o[e][0] = merge_elem(st, o[e][0], v.x);
-        o[e][1] = merge_elem(st, o[e][1], v.y);
-        o[e][2] = merge_elem(st, o[e][2], v.z);
-        o[e][3] = merge_elem(st, o[e][3], v.w);
+      for (int k = 0; k < G; ++k) {
+        if (s0 + k < u.nseg) {
+          const float* prow = p.partials + (size_t(u.part_base) + size_t(s0 + k) * u.rows + vr) * (D + 4);
+          ml[k] = *reinterpret_cast<const float2*>(prow);
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[k][e] = *reinterpret_cast<const float4*>(prow + 4 + e * 128 + lane * 4);
+        }
       }
-      M = st.m;
-      L = st.l;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (s0 + k < u.nseg) {
+          const MergeStep st = merge_step(M, L, ml[k].x, ml[k].y);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            o[e][0] = merge_elem(st, o[e][0], v[k][e].x);
+            o[e][1] = merge_elem(st, o[e][1], v[k][e].y);
+            o[e][2] = merge_elem(st, o[e][2], v[k][e].z);
+            o[e][3] = merge_elem(st, o[e][3], v[k][e].w);
+          }
+          M = st.m;
+          L = st.l;
+        }
+      }
     }
     const int pos = first_valid + vr / p.group;
     const int hg = vr % p.group;
@@ -65,9 +85,9 @@ __global__ void __launch_bounds__(128) bip_merge_kernel(const MergeParams p) {
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream) {
   if (p.n_units <= 0) return cudaSuccess;
   if (head_dim == 128)
-    bip_merge_kernel<128><<<p.n_units, 128, 0, stream>>>(p);
+    bip_merge_kernel<128><<<p.n_units, kMergeThreads, 0, stream>>>(p);
   else if (head_dim == 256)
-    bip_merge_kernel<256><<<p.n_units, 128, 0, stream>>>(p);
+    bip_merge_kernel<256><<<p.n_units, kMergeThreads, 0, stream>>>(p);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
