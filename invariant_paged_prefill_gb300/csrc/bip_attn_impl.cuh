@@ -92,7 +92,14 @@ struct Cfg {
   // 2 (V): a fifth warpgroup would leave too few registers at launch.
   static constexpr int SM_WARPS = 4 * NT;
   static constexpr int DQ_WARP0 = SM_WARPS;
-  static constexpr int GA_WARP0 = SM_WARPS + (KV8 ? 4 : 0);
+  // FP8 dequant warpgroups, taking alternate blocks.  With two, each owns
+  // one staging stage and one ring slot (block index mod 2), so its parity
+  // waits never run two phases ahead of a barrier; one stage (d = 256)
+  // keeps one warpgroup.  Two give up registers (setmaxnreg); one keeps
+  // its launch count.
+  static constexpr int DQ_WGS = KV8 ? (D == 128 ? 2 : 1) : 0;
+  static constexpr int DQ_REGS = 80;
+  static constexpr int GA_WARP0 = SM_WARPS + 4 * DQ_WGS;
   static constexpr int GA_WARPS = GATHER && !KV8 ? 8 : 0;
   static constexpr int GW = GATHER ? (KV8 ? 1 : 4) : 0;  // gather warps per stream (K or V)
   static constexpr int CTL_WARP0 = GA_WARP0 + GA_WARPS;
@@ -106,7 +113,8 @@ struct Cfg {
   static constexpr bool SPLIT_REGS = THREADS > 256;
   static constexpr int CTL_REGS = KV8 ? 80 : (GATHER ? 72 : 56);  // FP8: softmax is capped at 240 anyway
   static constexpr int GA_REGS = 56;
-  static constexpr int FIXED_REGS = CTL_REGS * 128 + GA_REGS * 32 * GA_WARPS + (KV8 ? LAUNCH_REGS * 128 : 0);
+  static constexpr int FIXED_REGS = CTL_REGS * 128 + GA_REGS * 32 * GA_WARPS +
+                                   (DQ_WGS == 2 ? DQ_REGS * 256 : DQ_WGS * LAUNCH_REGS * 128);
   static constexpr int SM_REGS_FREE = ((LAUNCH_REGS * THREADS - FIXED_REGS) / (32 * SM_WARPS)) & ~7;
   static constexpr int SM_REGS = SPLIT_REGS ? (SM_REGS_FREE < 240 ? SM_REGS_FREE : 240) : 255;
   static_assert(!SPLIT_REGS || SM_REGS * 32 * SM_WARPS + FIXED_REGS <= LAUNCH_REGS * THREADS,
@@ -129,6 +137,7 @@ struct Cfg {
   static_assert(NT == 2 || (2 * BN <= 256 && 256 + D <= TM_COLS), "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(!KV8 || NT == 1, "FP8 pages use the one-tile variant");
+  static_assert(DQ_WGS <= 1 || (SS == DQ_WGS && ST == DQ_WGS), "one staging stage and one slot per dequant warpgroup");
 };
 
 // Barrier slots (8 bytes each) at OFF_BAR.
@@ -850,15 +859,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
   return pack_bf16x2(f.x, f.y);
 }
 
-// FP8 pages: convert each staged block (BN rows x D codes, row-major) into the
+// FP8 pages (warpgroup wg of DQ_WGS takes the blocks b with b mod DQ_WGS = wg):
+// convert each staged block (BN rows x D codes, row-major) into the
 // bf16, 128-byte-swizzled K/V ring slot the MMAs read; V rows at or past
 // kv_len are written as zeros.  K, then V, per block; the bf16 slot is taken
 // once the MMA that last read it has completed.
 template <int D, int NT, int ST, bool KV8>
-__device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) {
+__device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, const int wg) {
   if constexpr (KV8) {
     using C = Cfg<D, NT, ST, KV8>;
-    const int tid = int(threadIdx.x) - C::DQ_WARP0 * 32;  // 0..127
+    const int tid = (int(threadIdx.x) - C::DQ_WARP0 * 32) & 127;  // 0..127 within the warpgroup
     constexpr int GROUPS = D / 16;                          // 16-code groups per row
     uint32_t b = 0;
     bool ok = true;
@@ -866,6 +876,7 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p) 
       const WorkItem w = p.items[it];
       const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
       for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {
+        if (int(b % C::DQ_WGS) != wg) continue;  // the other warpgroup's block
         const int ss = b % C::SS, slot = b % ST;
         const uint32_t suse = b / C::SS, use = b / ST;
         const int valid_rows = w.kv_len - blk * C::BN;
@@ -985,7 +996,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
     if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
     softmax_role<D, NT, ST, KV8, WIN, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4);
   } else if (warp < C::GA_WARP0) {
-    dequant_role<D, NT, ST, KV8>(c, sbase, p);
+    if constexpr (C::DQ_WGS == 2) reg_dealloc<C::DQ_REGS>();
+    dequant_role<D, NT, ST, KV8>(c, sbase, p, (warp - C::DQ_WARP0) / 4);
   } else if (warp < C::CTL_WARP0) {
     if constexpr (C::GA_WARPS > 0) {
       reg_dealloc<C::GA_REGS>();

@@ -40,8 +40,9 @@ class _Bar:
         return (self.phase & 1) != parity
 
 
-def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0):
-    """items: list of (nb, mask); SS > 0 models FP8 staging + dequant; GW > 0
+def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
+    """items: list of (nb, mask); SS > 0 models FP8 staging + dequant (DQ
+    dequant warpgroups taking alternate blocks); GW > 0
     models token-granular pages: GW row-gather warps per stream, whose 32
     lanes each arrive on the landing barrier when their own copies land,
     and a q/K producer that loads q tiles only."""
@@ -133,10 +134,13 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0):
             if not q_done:
                 yield from load_q()
 
-    def dequant():
+    def dequant(wg=0, nwg=1):
         b = 0
         for nb, _ in items:
             for _ in range(nb):
+                if b % nwg != wg:  # the other warpgroup's block
+                    b += 1
+                    continue
                 ss, slot = b % SS, b % ST
                 for kv in ("K", "V"):
                     yield wait(f"{kv}8_FULL{ss}", b // SS)
@@ -217,7 +221,7 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0):
         roles = [("producer_k", producer(False)), ("producer_v", producer(True)), ("issuer", issuer())]
     roles += [(f"softmax{t}.{w}", softmax(t)) for t in range(NT) for w in range(warps)]
     if SS:
-        roles.append(("dequant", dequant()))
+        roles += [(f"dequant{w}", dequant(w, DQ)) for w in range(DQ)]
     state, done = {n: None for n, _ in roles}, set()
     for _ in range(500000):
         clock[0] += 1
@@ -248,26 +252,27 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0):
     raise AssertionError("schedule did not finish")
 
 
-VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, GW gather warps per stream)
-    "d128_two_tiles": (2, 1, 2, 0, 0),
-    "d128_one_tile": (1, 2, 3, 0, 0),
-    "d256": (1, 2, 2, 0, 0),
-    "d128_fp8": (1, 2, 2, 2, 0),
-    "d256_fp8": (1, 2, 2, 1, 0),
-    "d128_rows": (1, 2, 3, 0, 4),
-    "d256_rows": (1, 2, 2, 0, 4),
-    "d128_fp8_rows": (1, 2, 2, 2, 1),
-    "d256_fp8_rows": (1, 2, 2, 1, 1),
+VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, GW gather warps per stream,
+    #           DQ dequant warpgroups)
+    "d128_two_tiles": (2, 1, 2, 0, 0, 1),
+    "d128_one_tile": (1, 2, 3, 0, 0, 1),
+    "d256": (1, 2, 2, 0, 0, 1),
+    "d128_fp8": (1, 2, 2, 2, 0, 2),
+    "d256_fp8": (1, 2, 2, 1, 0, 1),
+    "d128_rows": (1, 2, 3, 0, 4, 1),
+    "d256_rows": (1, 2, 2, 0, 4, 1),
+    "d128_fp8_rows": (1, 2, 2, 2, 1, 2),
+    "d256_fp8_rows": (1, 2, 2, 1, 1, 1),
 }
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 def test_schedule_never_deadlocks_or_aliases(variant):
-    NT, NS, ST, SS, GW = VARIANTS[variant]
+    NT, NS, ST, SS, GW, DQ = VARIANTS[variant]
     full = (1 << NT) - 1
     item_sets = [[(1, full)], [(9, full)], [(4, full), (1, full), (17, full)], [(3, 1), (2, full), (5, 1)]]
     if NT == 2:
         item_sets.append([(6, 2), (2, 1), (7, 3)])
     for items in item_sets:
         for seed in range(60 if not GW else 25):
-            _simulate(NT, NS, ST, SS, items, seed, GW=GW)
+            _simulate(NT, NS, ST, SS, items, seed, GW=GW, DQ=DQ)
