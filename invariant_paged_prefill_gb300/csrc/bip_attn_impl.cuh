@@ -12,8 +12,10 @@
 //                   and sum, writes P_t (bf16) over S_t in TMEM, rescales
 //                   O_t when needed, and at each segment end folds or
 //                   writes the segment.
-//   (FP8 pages)     a dequant warpgroup converts staged E4M3 blocks to bf16.
-//   (token pages)   row-gather warps copy K and V rows with cp.async.
+//   (FP8 pages)     dequant warpgroups (two at head_dim 128, on alternate
+//                   blocks) convert staged E4M3 blocks to bf16.
+//   (token pages)   row-gather warps copy K and V rows with cp.async (bf16:
+//                   their own two warpgroups; FP8: control warps 2 and 3).
 //   control         warp 0: q tiles and K blocks by TMA through an ST-deep
 //                   ring (q only when rows are gathered); warp 1: the
 //                   tcgen05 issuer, S_t = Q_t K^T into TMEM, then
