@@ -28,9 +28,10 @@
  * on K/V at positions <= its own.
  *
  * Ownership: the caller owns every device buffer and the stream.  A plan
- * owns host copies of its work list (pinned when a CUDA device is present)
- * and is immutable after creation; one plan may serve many bip_prefill
- * calls (one per layer) with the same lengths and shapes.
+ * owns host copies of its work list (pinned and mapped into the device's
+ * address space when a CUDA device is present: each call's upload reads it
+ * from the GPU) and is immutable after creation; one plan may serve many
+ * bip_prefill calls (one per layer) with the same lengths and shapes.
  *
  * Errors: every entry point returns a status and never aborts or exits the
  * process (the model-serving-minefield issue 73 correction: a fixed 2 GiB
@@ -149,7 +150,8 @@ bip_status bip_plan_get_info(bip_plan_t plan, bip_plan_info* info);
  * Writes at most capacity items; *count receives the total. */
 bip_status bip_plan_get_items(bip_plan_t plan, int32_t* items, int32_t capacity, int32_t* count);
 
-/* Release a plan.  Call only after work enqueued with it has completed. */
+/* Release a plan.  Call only after work enqueued with it has completed
+ * (its host image is read by that work). */
 bip_status bip_plan_destroy(bip_plan_t plan);
 
 /* Enqueue the attention on `stream`; never synchronizes.  DEVICE pointers:

@@ -78,7 +78,7 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + ST * KV_BYTES;
   // FP8 pages land raw (BN rows x D bytes, unswizzled) in a staging ring and
-  // are converted to the bf16 operand layout by the dequant warpgroup.
+  // are converted to the bf16 operand layout by the dequant warpgroups.
   static constexpr int SS = KV8 ? (D == 128 ? 2 : 1) : 0;  // staging stages
   static constexpr int KV8_BYTES = BN * D;
   static constexpr int OFF_K8 = OFF_V + ST * KV_BYTES;
