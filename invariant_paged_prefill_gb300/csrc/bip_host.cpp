@@ -546,7 +546,7 @@ void set_pools(bip::AttnParams& ap, const void* k_pages, const void* v_pages, in
 // The first `bytes` of the plan's host image into the workspace, on `stream`:
 // by the upload kernel when the pinned image is mapped into the device's
 // address space, else by one copy-engine copy.
-cudaError_t upload(const bip_plan_s* p, uint8_t* ws, size_t bytes, cudaStream_t stream) {
+static cudaError_t upload(const bip_plan_s* p, uint8_t* ws, size_t bytes, cudaStream_t stream) {
   if (p->upload_dev) return bip::launch_upload(p->upload_dev, ws, bytes, stream);
   return cudaMemcpyAsync(ws, p->upload, bytes, cudaMemcpyHostToDevice, stream);
 }
@@ -556,9 +556,10 @@ cudaError_t upload(const bip_plan_s* p, uint8_t* ws, size_t bytes, cudaStream_t 
 // Hkv, slot, page).  bf16: box (64, 1, page_size, 1), one 128-byte-swizzled
 // chunk of a page.  FP8: box (d, 1, page_size, 1), a whole page row-major,
 // unswizzled (the dequant warps lay out the bf16 operand).
-bool encode_maps(int32_t d, int32_t hq, int32_t hkv, int32_t group, int32_t T, int32_t page_size, bool fp8,
-                 const void* q, int64_t q_rows, const void* k_pages, const void* v_pages, int64_t num_pages,
-                 int64_t page_stride_elems, CUtensorMap* tm_q, CUtensorMap* tm_k, CUtensorMap* tm_v) {
+static bool encode_maps(int32_t d, int32_t hq, int32_t hkv, int32_t group, int32_t T, int32_t page_size,
+                        bool fp8, const void* q, int64_t q_rows, const void* k_pages, const void* v_pages,
+                        int64_t num_pages, int64_t page_stride_elems, CUtensorMap* tm_q, CUtensorMap* tm_k,
+                        CUtensorMap* tm_v) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
   {
