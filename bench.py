@@ -403,13 +403,14 @@ def time_append(b, device, steps: int, warmup: int):
 
 def windowed_work(heads, q_lens, kv_lens, window: int):
     """(FLOP, KV bytes) of sliding-window attention: row at position p sees
-    min(p + 1, window + 1) keys; a request reads its last q + window keys."""
+    min(p + 1, window + 1) keys; a request with rows reads its last q + window
+    keys (one with none reads nothing)."""
     hq, hkv, d = heads
     pairs, keys = 0, 0
     for q, kv in zip(q_lens, kv_lens):
         for p in range(kv - q, kv):
             pairs += min(p + 1, window + 1)
-        keys += min(kv, q + window)
+        keys += min(kv, q + window) if q > 0 else 0
     return 4 * d * hq * pairs, keys * 2 * hkv * d * 2
 
 
