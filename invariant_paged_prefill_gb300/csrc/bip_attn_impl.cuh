@@ -12,10 +12,11 @@
 //                   and sum, writes P_t (bf16) over S_t in TMEM, rescales
 //                   O_t when needed, and at each segment end folds or
 //                   writes the segment.
-//   (FP8 pages)     dequant warpgroups (two at head_dim 128, on alternate
-//                   blocks) convert staged E4M3 blocks to bf16.
+//   (FP8 pages)     dequant warpgroups (two at head_dim 128 with whole
+//                   pages, on alternate blocks) convert staged E4M3 blocks
+//                   to bf16.
 //   (token pages)   row-gather warps copy K and V rows with cp.async (bf16:
-//                   their own two warpgroups; FP8: control warps 2 and 3).
+//                   two warpgroups; FP8: one).
 //   control         warp 0: q tiles and K blocks by TMA through an ST-deep
 //                   ring (q only when rows are gathered); warp 1: the
 //                   tcgen05 issuer, S_t = Q_t K^T into TMEM, then
@@ -87,11 +88,10 @@ struct Cfg {
   static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
   // Warp roles, whole warpgroups each: softmax warps 0 .. 4 NT - 1 (slot
   // t = warp / 4, TMEM lane quarter = warp % 4), then the FP8 dequant
-  // warpgroup, then (GATHER with bf16 pages) two row-gather warpgroups,
-  // four warps for K and four for V, then the control warpgroup: q/K producer,
-  // MMA issuer, V producer and one spare warp.  GATHER with FP8 pages (half
-  // the bytes a row) gathers with the control warpgroup's warps 3 (K) and
-  // 2 (V): a fifth warpgroup would leave too few registers at launch.
+  // warpgroups, then (GATHER) the row-gather warps, half for K and half for
+  // V (bf16: two warpgroups; FP8: one, next to a single dequant warpgroup),
+  // then the control warpgroup: q/K producer, MMA issuer, V producer and
+  // one spare warp.
   static constexpr int SM_WARPS = 4 * NT;
   static constexpr int DQ_WARP0 = SM_WARPS;
   // FP8 dequant warpgroups, taking alternate blocks.  With two, each owns
@@ -99,11 +99,11 @@ struct Cfg {
   // waits never run two phases ahead of a barrier; one stage (d = 256)
   // keeps one warpgroup.  Two give up registers (setmaxnreg); one keeps
   // its launch count.
-  static constexpr int DQ_WGS = KV8 ? (D == 128 ? 2 : 1) : 0;
+  static constexpr int DQ_WGS = KV8 ? ((D == 128 && !GATHER) ? 2 : 1) : 0;
   static constexpr int DQ_REGS = 80;
   static constexpr int GA_WARP0 = SM_WARPS + 4 * DQ_WGS;
-  static constexpr int GA_WARPS = GATHER && !KV8 ? 8 : 0;
-  static constexpr int GW = GATHER ? (KV8 ? 1 : 4) : 0;  // gather warps per stream (K or V)
+  static constexpr int GA_WARPS = GATHER ? (KV8 ? 4 : 8) : 0;
+  static constexpr int GW = GATHER ? (KV8 ? 2 : 4) : 0;  // gather warps per stream (K or V)
   static constexpr int CTL_WARP0 = GA_WARP0 + GA_WARPS;
   static constexpr int THREADS = 32 * (CTL_WARP0 + 4);
   // Register split: launches of more than 256 threads start at LAUNCH_REGS
@@ -861,12 +861,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
   return pack_bf16x2(f.x, f.y);
 }
 
-// FP8 pages (warpgroup wg of DQ_WGS takes the blocks b with b mod DQ_WGS = wg):
+// FP8 pages (warpgroup wg of NWG takes the blocks b with b mod NWG = wg; NWG
+// is the launching kernel's count, passed explicitly):
 // convert each staged block (BN rows x D codes, row-major) into the
 // bf16, 128-byte-swizzled K/V ring slot the MMAs read; V rows at or past
 // kv_len are written as zeros.  K, then V, per block; the bf16 slot is taken
 // once the MMA that last read it has completed.
-template <int D, int NT, int ST, bool KV8>
+template <int D, int NT, int ST, bool KV8, int NWG>
 __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, const int wg) {
   if constexpr (KV8) {
     using C = Cfg<D, NT, ST, KV8>;
@@ -878,7 +879,7 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, 
       const WorkItem w = p.items[it];
       const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
       for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {
-        if (int(b % C::DQ_WGS) != wg) continue;  // the other warpgroup's block
+        if (int(b % NWG) != wg) continue;  // another warpgroup's block
         const int ss = b % C::SS, slot = b % ST;
         const uint32_t suse = b / C::SS, use = b / ST;
         const int valid_rows = w.kv_len - blk * C::BN;
@@ -999,7 +1000,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
     softmax_role<D, NT, ST, KV8, WIN, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4);
   } else if (warp < C::GA_WARP0) {
     if constexpr (C::DQ_WGS == 2) reg_dealloc<C::DQ_REGS>();
-    dequant_role<D, NT, ST, KV8>(c, sbase, p, (warp - C::DQ_WARP0) / 4);
+    dequant_role<D, NT, ST, KV8, C::DQ_WGS>(c, sbase, p, (warp - C::DQ_WARP0) / 4);
   } else if (warp < C::CTL_WARP0) {
     if constexpr (C::GA_WARPS > 0) {
       reg_dealloc<C::GA_REGS>();
@@ -1021,8 +1022,6 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
         if (lane == 0) prefetch_tmap(&tm_v);
         producer<D, NT, ST, KV8, GATHER>(c, sbase, &tm_q, &tm_v, p, true);
       }
-    } else if (KV8) {
-      row_gatherer<D, NT, ST, KV8, 1>(c, sbase, p, role == 2 ? 1 : 0);
     }
   }
 

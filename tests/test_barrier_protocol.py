@@ -261,8 +261,8 @@ VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, 
     "d256_fp8": (1, 2, 2, 1, 0, 1),
     "d128_rows": (1, 2, 3, 0, 4, 1),
     "d256_rows": (1, 2, 2, 0, 4, 1),
-    "d128_fp8_rows": (1, 2, 2, 2, 1, 2),
-    "d256_fp8_rows": (1, 2, 2, 1, 1, 1),
+    "d128_fp8_rows": (1, 2, 2, 2, 2, 1),
+    "d256_fp8_rows": (1, 2, 2, 1, 2, 1),
 }
 
 
