@@ -283,3 +283,27 @@ def test_items_grouped_by_request_and_head_longest_first():
     assert (np.diff(keys) >= 0).all()
     for k in np.unique(keys):
         assert (np.diff(it[keys == k, 6]) <= 0).all()
+
+
+def test_work_list_does_not_depend_on_the_page_size(lib):
+    # the same lengths in pools of 16-slot pages and of single slots: the plan
+    # (units, segments, splits, order) is the same; only page offsets differ
+    rng = np.random.default_rng(11)
+    for trial in range(12):
+        batch = int(rng.integers(1, 7))
+        kv_lens = [int(x) for x in rng.integers(1, 9000, batch)]
+        q_lens = [int(rng.integers(0, k + 1)) for k in kv_lens]
+        qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+        plans = []
+        for ps in (16, 1):
+            pages = [(k + ps - 1) // ps for k in kv_lens]
+            kv = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+            last = [k - ps * (n - 1) for k, n in zip(kv_lens, pages)]
+            for policy in ("never", "auto"):
+                plans.append((ps, policy, bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                                                   page_size=ps, split_policy=policy, tiles_per_unit=1)))
+        by_policy = {}
+        for ps, policy, plan in plans:
+            by_policy.setdefault(policy, []).append(plan.items())
+        for policy, (a, b) in by_policy.items():
+            assert np.array_equal(a, b), f"trial {trial}, policy {policy}"
