@@ -110,6 +110,15 @@ class Plan:
             pass
 
 
+def _require_cuda(**tensors):
+    """Every given tensor (None = to be allocated) must live on a CUDA device:
+    there is no CPU path."""
+    import torch
+    for name, t in tensors.items():
+        if t is not None and (not isinstance(t, torch.Tensor) or not t.is_cuda):
+            raise BipError(1, f"{name} must be a CUDA tensor")
+
+
 def _dev_ptr(t, name: str):
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
@@ -126,6 +135,8 @@ def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, 
     kv_indices int32 on the device.  Returns (out bf16, lse fp32 natural log).
     """
     import torch
+    _require_cuda(q=q, k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices, out=out, lse=lse,
+                  workspace=workspace)
     dev = q.device
     if out is None:
         out = torch.empty_like(q)
@@ -171,6 +182,8 @@ def append_kv(plan: Plan, k_new, v_new, k_pages, v_pages, kv_indices, *, workspa
     unchanged, or e4m3(x / scale) for uint8 (E4M3) pools.
     """
     import torch
+    _require_cuda(k_new=k_new, v_new=v_new, k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices,
+                  workspace=workspace)
     dev = k_new.device
     if workspace is None:
         workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
@@ -241,6 +254,8 @@ def prefill_graph(plan: GraphPlan, batch: int, qo_indptr, kv_indptr, kv_last_pag
     graph's static buffers.  Results equal ``prefill`` on the same batch.
     """
     import torch
+    _require_cuda(qo_indptr=qo_indptr, kv_indptr=kv_indptr, kv_last_page_len=kv_last_page_len, q=q,
+                  k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices, out=out, lse=lse, workspace=workspace)
     for name, t, n in (("qo_indptr", qo_indptr, batch + 1), ("kv_indptr", kv_indptr, batch + 1),
                        ("kv_last_page_len", kv_last_page_len, batch)):
         if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n:

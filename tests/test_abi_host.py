@@ -307,3 +307,25 @@ def test_work_list_does_not_depend_on_the_page_size(lib):
             by_policy.setdefault(policy, []).append(plan.items())
         for policy, (a, b) in by_policy.items():
             assert np.array_equal(a, b), f"trial {trial}, policy {policy}"
+
+
+def test_entry_points_refuse_host_tensors_instead_of_computing_on_the_cpu(lib):
+    # There is no CPU path: every compute entry point wants device tensors and
+    # says so, before anything runs.
+    import torch
+    from invariant_paged_prefill_gb300 import workloads as W
+    b = W.tiny(3)
+    plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8)
+    with pytest.raises(bip.BipError, match="CUDA tensor"):
+        bip.prefill(plan, b.q, b.k_pages, b.v_pages, b.kv_indices, workspace=ws)
+    k_new = torch.zeros(3, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(bip.BipError, match="CUDA tensor"):
+        bip.append_kv(plan, k_new, k_new, b.k_pages, b.v_pages, b.kv_indices, workspace=ws)
+    gp = bip.GraphPlan(2, 8, num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    i32 = torch.zeros(3, dtype=torch.int32)
+    out = torch.zeros(8, 32, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(8, 32, dtype=torch.float32)
+    with pytest.raises(bip.BipError, match="CUDA tensor"):
+        bip.prefill_graph(gp, 2, i32, i32, i32[:2], out, b.k_pages, b.v_pages, b.kv_indices, out, lse,
+                          torch.empty(gp.workspace_bytes, dtype=torch.uint8))
