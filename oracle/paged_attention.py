@@ -35,6 +35,13 @@ so this module is that definition written out; it restates no algorithm.
   decoded values is the reading, and equals folding ``k_scale`` into the
   logit scale and ``v_scale`` into the output).
 * Slots at or beyond ``kv_len`` are never read.
+* Custom masks.  The pages list "custom KV indices/masks" among the cases
+  the padding skipped (sglang PR 46351, "Fix") without defining them.  The
+  reading taken: an optional boolean mask per request, one row per q row and
+  one column per key, that narrows the causal (and window) rule -- key j is
+  visible to row i when the causal rule allows it and ``mask[i, j]`` is set.
+  A row left with no visible key has no softmax; it is defined as out = 0,
+  lse = -inf.
 
 Structure: the small helpers below are the definition's pieces; the tests
 replace one at a time with a plausible mistake to show the pins catch it.
@@ -111,22 +118,29 @@ def gather_request_kv(pages: np.ndarray, kv_indices: Sequence[int], page_lo: int
 
 
 def attend_rows(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, positions: np.ndarray,
-                sm_scale: float, window_left: int = 0) -> tuple[np.ndarray, np.ndarray]:
-    """Causal (optionally sliding-window) softmax attention of some rows against one head's keys.
+                sm_scale: float, window_left: int = 0,
+                mask_rows: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Causal (optionally sliding-window, optionally custom-masked) softmax
+    attention of some rows against one head's keys.
 
-    q_rows ``[n, d]``, keys/values ``[kv_len, d]``, positions ``[n]``.
-    Returns out ``[n, d]`` and natural-log lse ``[n]`` in float64.
+    q_rows ``[n, d]``, keys/values ``[kv_len, d]``, positions ``[n]``;
+    mask_rows ``[n, >= kv_len]`` booleans (columns past kv_len ignored).
+    Returns out ``[n, d]`` and natural-log lse ``[n]`` in float64; a row with
+    no visible key gets out = 0 and lse = -inf.
     """
     scores = (q_rows @ keys.T) * sm_scale                       # [n, kv_len]
     kv_idx = np.arange(keys.shape[0])[None, :]
     visible = kv_idx < np.array([visible_keys(int(p)) for p in positions])[:, None]
     visible &= kv_idx >= np.array([first_visible_key(int(p), window_left) for p in positions])[:, None]
+    if mask_rows is not None:
+        visible &= np.asarray(mask_rows, dtype=bool)[:, :keys.shape[0]]
     scores = np.where(visible, scores, -np.inf)
-    m = scores.max(axis=1, keepdims=True)
+    empty = ~visible.any(axis=1)
+    m = np.where(empty[:, None], 0.0, scores.max(axis=1, keepdims=True))
     w = np.exp(scores - m)                                       # masked entries -> 0
     denom = w.sum(axis=1, keepdims=True)
-    out = (w @ values) / denom
-    lse = (m + np.log(denom))[:, 0]
+    out = (w @ values) / np.where(empty[:, None], 1.0, denom)
+    lse = np.where(empty, -np.inf, (m + np.log(np.where(empty[:, None], 1.0, denom)))[:, 0])
     return out, lse
 
 
@@ -145,7 +159,8 @@ def paged_prefill(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, kv_last
                   num_qo_heads: int, num_kv_heads: int, page_size: int, *,
                   q_kind: str = "f64", kv_kind: str = "f64", k_scale: float = 1.0,
                   v_scale: float = 1.0, sm_scale: float | None = None,
-                  rows: Iterable[int] | None = None, row_chunk: int = 512, window_left: int = 0):
+                  rows: Iterable[int] | None = None, row_chunk: int = 512, window_left: int = 0,
+                  custom_mask: Sequence[np.ndarray | None] | None = None):
     """Reference output and lse of paged causal GQA prefill.
 
     q ``[total_tokens, num_qo_heads, head_dim]``; k_pages/v_pages
@@ -155,6 +170,8 @@ def paged_prefill(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, kv_last
     ``rows`` restricts the computation to the listed token rows (all rows when
     None); the returned arrays then hold those rows in the order given.
     ``window_left`` > 0 restricts each row to its last window_left + 1 keys.
+    ``custom_mask`` (one entry per request: a boolean ``[q_len, kv_len]``
+    array, or None) further narrows which keys each q row sees.
     Returns ``(out [n, num_qo_heads, head_dim], lse [n, num_qo_heads])``.
     """
     q_raw = np.asarray(q)
@@ -192,8 +209,14 @@ def paged_prefill(q, k_pages, v_pages, qo_indptr, kv_indptr, kv_indices, kv_last
             q_rows = _as_f64(q_raw[toks], q_kind)          # decode only the rows used
             for h in range(hq):
                 hk = kv_head_of(h, num_qo_heads, num_kv_heads)
+                mrows = None
+                if custom_mask is not None and custom_mask[r] is not None:
+                    mask_r = np.asarray(custom_mask[r], dtype=bool)
+                    if mask_r.shape != (ql, kl):
+                        raise ValueError(f"request {r}: custom mask must be [{ql}, {kl}]")
+                    mrows = mask_r[[t - qo[r] for t in toks], :last]
                 o, s = attend_rows(q_rows[:, h, :], keys[:last, hk, :], vals[:last, hk, :], pos, sm_scale,
-                                   window_left)
+                                   window_left, mrows)
                 idx = [order[t] for t in toks]
                 out[idx, h, :] = o
                 lse[idx, h] = s
