@@ -35,8 +35,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged prefill attn TFLOP/s (long q) & KV-read GB/s (short extends), bit-exact"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["bip_host.cpp", "bip_attn.cu", "bip_attn_gather.cu", "bip_attn_impl.cuh", "bip_merge.cu",
-                  "bip_append.cu", "bip_plan_dev.cu", "bip_internal.h", "bip_numerics.cuh", "bip_ptx.cuh"]
+KERNEL_SOURCES = ["bip_host.cpp", "bip_attn.cu", "bip_attn_gather.cu", "bip_attn_mask.cu", "bip_attn_impl.cuh",
+                  "bip_merge.cu", "bip_append.cu", "bip_plan_dev.cu", "bip_internal.h", "bip_numerics.cuh",
+                  "bip_ptx.cuh"]
 
 
 # ----------------------------------------------------------------- helpers

@@ -180,6 +180,29 @@ bip_status bip_prefill(bip_plan_t plan, const void* q, int64_t num_q_rows, const
                        const int32_t* kv_indices, float k_scale, float v_scale, void* out,
                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* bip_prefill under a per-row custom mask: custom masks are one of the cases
+ * the padding skipped (sglang PR 46351, "Fix").  The mask narrows the causal
+ * rule (and the plan's sliding window): key j of a request is visible to one
+ * of its q rows when j <= the row's position, the window allows it, and the
+ * row's mask bit j is set.  Bits for keys past the row's position are never
+ * read.  A row left with no visible key gets out = 0 and lse = -inf.
+ *   mask     DEVICE uint32 words, 4-byte aligned: q row r (the row of q, over
+ *            the whole batch) owns words [r * mask_row_words, (r + 1) *
+ *            mask_row_words); bit j % 32 (least significant first) of word
+ *            j / 32 is key j of the row's request
+ *   mask_row_words  >= ceil(kv_len / 32) for every request with q rows, else
+ *            BIP_ERR_INVALID_ARG
+ * Every other argument, the contract and the errors as for bip_prefill.  A row
+ * depends on its q row, its keys and its own mask row only: a radix-cache hit
+ * whose tail rows carry the same mask rows as the full prefill gets the same
+ * bits.  Blocks a mask leaves empty are still visited (the work list does not
+ * depend on the mask). */
+bip_status bip_prefill_masked(bip_plan_t plan, const void* q, int64_t num_q_rows, const void* k_pages,
+                              const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                              const int32_t* kv_indices, const uint32_t* mask, int64_t mask_row_words,
+                              float k_scale, float v_scale, void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
 /* Write each request's new K/V rows into its pages: the paged KV append that
  * precedes the attention of an extend: on a radix-cache prefix hit only the
  * uncached tail is computed and its K/V join the cached pages (sglang PR 46351,

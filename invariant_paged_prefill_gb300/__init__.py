@@ -22,7 +22,7 @@ import numpy as np
 from . import _lib
 
 __all__ = ["BipError", "Plan", "prefill", "append_kv", "GraphPlan", "prefill_graph", "workspace_bound",
-           "read_device_status", "STATUS"]
+           "read_device_status", "pack_mask", "STATUS"]
 
 STATUS = {
     0: "BIP_OK", 1: "BIP_ERR_INVALID_ARG", 2: "BIP_ERR_UNSUPPORTED", 3: "BIP_ERR_WORKSPACE_TOO_SMALL",
@@ -126,17 +126,43 @@ def _dev_ptr(t, name: str):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def pack_mask(masks, row_words: Optional[int] = None) -> np.ndarray:
+    """Per-request boolean masks ``[q_len, kv_len]`` (in request order) as the
+    words ``bip_prefill_masked`` reads: int32 ``[total_q, row_words]``, bit
+    ``j % 32`` (least significant first) of word ``j // 32`` of a q row = key j
+    visible.  ``row_words`` defaults to the fewest that hold the longest row.
+    Host-side input preparation (numpy); copy the result to the device."""
+    rows = [np.asarray(m, dtype=bool) for m in masks]
+    if any(m.ndim != 2 for m in rows):
+        raise BipError(1, "each mask must be a 2-d [q_len, kv_len] array")
+    need = max([(m.shape[1] + 31) // 32 for m in rows], default=0)
+    words = need if row_words is None else int(row_words)
+    if words < need:
+        raise BipError(1, f"row_words {words} < {need} needed for the longest mask row")
+    total = sum(m.shape[0] for m in rows)
+    out = np.zeros((total, words * 4), dtype=np.uint8)
+    r = 0
+    for m in rows:
+        packed = np.packbits(m, axis=1, bitorder="little")  # byte b, bit i = key 8 b + i
+        out[r:r + m.shape[0], :packed.shape[1]] = packed
+        r += m.shape[0]
+    return out.view("<u4").view(np.int32).reshape(total, words)
+
+
 def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, workspace=None,
-            k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+            k_scale: float = 1.0, v_scale: float = 1.0, stream=None, custom_mask=None):
     """Enqueue the attention on ``stream`` (default: torch's current stream).
 
     q [total_q, Hq, d] bf16; k_pages / v_pages [num_pages, page_size, Hkv, d]
     (a page stride other than page_size*Hkv*d is allowed, the same for K and V);
-    kv_indices int32 on the device.  Returns (out bf16, lse fp32 natural log).
+    kv_indices int32 on the device.  ``custom_mask``: None, or int32 words
+    ``[total_q, row_words]`` on the device (see ``pack_mask``) that narrow each
+    row's causal keys (``bip_prefill_masked``).  Returns (out bf16, lse fp32
+    natural log).
     """
     import torch
     _require_cuda(q=q, k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices, out=out, lse=lse,
-                  workspace=workspace)
+                  workspace=workspace, custom_mask=custom_mask)
     dev = q.device
     if out is None:
         out = torch.empty_like(q)
@@ -161,14 +187,23 @@ def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, 
             raise BipError(1, f"{name}: slots and heads must be contiguous inside a page")
     if k_pages.shape[0] != v_pages.shape[0] or k_pages.stride(0) != v_pages.stride(0):
         raise BipError(1, "k_pages and v_pages must share page count and stride")
+    if custom_mask is not None:
+        if custom_mask.dtype != torch.int32 or custom_mask.dim() != 2 or not custom_mask.is_contiguous():
+            raise BipError(1, "custom_mask must be contiguous int32 [total_q, row_words]")
+        if custom_mask.shape[0] != q.shape[0]:
+            raise BipError(1, "custom_mask must have one row per q row")
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sptr = ctypes.c_void_p(stream.cuda_stream)
-    _check(plan._lib.bip_prefill(plan._h, _dev_ptr(q, "q"), q.shape[0], _dev_ptr(k_pages, "k_pages"),
-                                 _dev_ptr(v_pages, "v_pages"), k_pages.shape[0], k_pages.stride(0),
-                                 _dev_ptr(kv_indices, "kv_indices"), float(k_scale), float(v_scale),
-                                 _dev_ptr(out, "out"), _dev_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
-                                 workspace.numel() * workspace.element_size(), sptr), "bip_prefill")
+    args = (_dev_ptr(q, "q"), q.shape[0], _dev_ptr(k_pages, "k_pages"), _dev_ptr(v_pages, "v_pages"),
+            k_pages.shape[0], k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"))
+    tail = (float(k_scale), float(v_scale), _dev_ptr(out, "out"), _dev_ptr(lse, "lse"),
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(), sptr)
+    if custom_mask is None:
+        _check(plan._lib.bip_prefill(plan._h, *args, *tail), "bip_prefill")
+    else:
+        _check(plan._lib.bip_prefill_masked(plan._h, *args, _dev_ptr(custom_mask, "custom_mask"),
+                                            custom_mask.shape[1], *tail), "bip_prefill_masked")
     return out, lse
 
 

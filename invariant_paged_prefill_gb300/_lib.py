@@ -46,6 +46,8 @@ SIGNATURES = {
     "bip_plan_destroy": (ctypes.c_int, [c_vp]),
     "bip_prefill": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp, c_f32, c_f32, c_vp, c_vp,
                                    c_vp, c_size, c_vp]),
+    "bip_prefill_masked": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp, c_vp, c_i64, c_f32,
+                                          c_f32, c_vp, c_vp, c_vp, c_size, c_vp]),
     "bip_append_kv": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp, c_f32, c_f32, c_vp,
                                      c_size, c_vp]),
     "bip_graph_plan": (ctypes.c_int, [ctypes.POINTER(c_vp), c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.c_int,

@@ -38,6 +38,11 @@
 // memory), and segments wholly beyond it are empty and skipped by the merge.
 // The running max is moved (and O rescaled) only when a row's block max
 // exceeds it by more than kLazyRescale in log2 units: a per-row decision.
+//
+// Mask kinds (template MK): 0 causal; 1 causal with a sliding window; 2
+// causal narrowed by a per-row custom mask (and by the window when
+// window_left > 0).  A custom mask row is read one block of bits at a time,
+// and a row that ends with no visible key is written as zeros with lse -inf.
 
 #pragma once
 
@@ -599,7 +604,14 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
   drain_wait(bar(c, B_DRAIN), 0);
 }
 
-template <int D, int NT, int ST, bool KV8, bool WIN, bool NARROW_LD>
+// Column j of a block is visible to a row when lo <= j <= lim and, with a
+// custom mask, bit j of the row's mask bits for the block is set.
+template <int MK, int NB>
+__device__ __forceinline__ bool col_visible(int j, int lim, int lo, const uint32_t (&mb)[NB]) {
+  return j <= lim && (MK == 0 || j >= lo) && (MK != 2 || ((mb[j >> 5] >> (j & 31)) & 1u));
+}
+
+template <int D, int NT, int ST, bool KV8, int MK, bool NARROW_LD>
 __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t) {
   using C = Cfg<D, NT, ST, KV8>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -639,13 +651,30 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
       bool seg_first = true;  // first block of this segment: O is overwritten, never rescaled
       for (int blk = sb_lo; blk <= sb_hi; ++blk, ++cnt, seg_first = false) {
         const int sbuf = cnt % C::NS;
-        if (!wait_warp(c, bar(c, B_S_FULL + 2 * t + sbuf), (cnt / C::NS) & 1, 21)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sa = t_lane + C::tm_s(t, sbuf);
         // Columns lo..lim are visible: keys up to the row's position, and
         // with a sliding window none before position - window_left.
         const int lim = valid ? pos - blk * C::BN : -1;
-        const int lo = WIN ? pos - p.window_left - blk * C::BN : INT_MIN / 2;
+        const int lo = (MK == 0 || (MK == 2 && p.window_left <= 0)) ? INT_MIN / 2
+                                                                    : pos - p.window_left - blk * C::BN;
+        // Custom mask: the row's bits for this block (bit j of word j / 32 =
+        // column j), loaded before the wait on S.  Only words holding a
+        // column <= lim are read; they lie inside the row, since lim + blk *
+        // BN is the row's position, below its kv_len.
+        uint32_t mb[C::BN / 32];
+#pragma unroll
+        for (int k = 0; k < C::BN / 32; ++k) mb[k] = 0u;
+        if constexpr (MK == 2) {
+          if (valid) {
+            const uint32_t* mrow =
+                p.mask + int64_t(w.q_tok0 + pos) * p.mask_row_words + int64_t(blk) * (C::BN / 32);
+#pragma unroll
+            for (int k = 0; k < C::BN / 32; ++k)
+              if (32 * k <= lim) mb[k] = __ldg(mrow + k);
+          }
+        }
+        if (!wait_warp(c, bar(c, B_S_FULL + 2 * t + sbuf), (cnt / C::NS) & 1, 21)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = t_lane + C::tm_s(t, sbuf);
 
         // Blocks wholly visible to every valid row of the warp skip the
         // per-column mask (same values for those rows, fewer instructions).
@@ -657,8 +686,16 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // the arithmetic but still stores P = 0: its rows may be valid rows
         // past whose position the block lies, and their O keeps accumulating
         // P V.
-        const bool whole = __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (!WIN || lo <= 0)));
-        const bool live = __any_sync(0xffffffffu, lim >= 0 && (!WIN || lo < C::BN));
+        bool all_bits = true;
+        if constexpr (MK == 2) {
+          uint32_t a = ~0u;
+#pragma unroll
+          for (int k = 0; k < C::BN / 32; ++k) a &= mb[k];
+          all_bits = a == ~0u;
+        }
+        const bool whole =
+            __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (MK == 0 || lo <= 0) && all_bits));
+        const bool live = __any_sync(0xffffffffu, lim >= 0 && (MK == 0 || lo < C::BN));
 
         // Block max.  One TMEM round trip for the whole S row; a 128-column
         // row is then reread in two halves for the exponentials instead of
@@ -679,8 +716,8 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           for (int j = 0; j < C::BN; j += 2) {
             float a = __uint_as_float(sv[j]), b = __uint_as_float(sv[j + 1]);
             if (!kWhole) {
-              a = (j <= lim && (!WIN || j >= lo)) ? a : -INFINITY;
-              b = (j + 1 <= lim && (!WIN || j + 1 >= lo)) ? b : -INFINITY;
+              a = col_visible<MK>(j, lim, lo, mb) ? a : -INFINITY;
+              b = col_visible<MK>(j + 1, lim, lo, mb) ? b : -INFINITY;
             }
             m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], a, b);
           }
@@ -740,8 +777,8 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                 if (kFmaPairs >> pair & 1) e = ex2_fma2(x);
                 else e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
                 if (!kWhole)
-                  e = f2_bits((cu <= lim && (!WIN || cu >= lo)) ? f2_lo(e) : 0.f,
-                              (cu + 1 <= lim && (!WIN || cu + 1 >= lo)) ? f2_hi(e) : 0.f);
+                  e = f2_bits(col_visible<MK>(cu, lim, lo, mb) ? f2_lo(e) : 0.f,
+                              col_visible<MK>(cu + 1, lim, lo, mb) ? f2_hi(e) : 0.f);
                 acc[pair & 3] = fadd2(acc[pair & 3], e);
                 hv[j / 2] = pack_bf16x2(f2_lo(e), f2_hi(e));
               }
@@ -805,7 +842,10 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         const MergeStep st = merge_step(Mrun, Lrun, m_seg, l);
         const bool last = (s == w.seg_hi);
         const bool use_scratch = (w.seg_hi > w.seg_lo);
-        const float osc = last ? out_scale(st.l, p.v_scale) : 0.f;
+        // A row with no visible key at all (possible only under a custom
+        // mask) is written as zeros, with lse = -inf.
+        const bool empty = MK == 2 && st.m == -INFINITY;
+        const float osc = (last && !empty) ? out_scale(st.l, p.v_scale) : 0.f;
         const int tok = w.q_tok0 + pos;
         const int head = w.kv_head * p.group + hg;
         uint16_t* orow = p.out + (size_t(tok) * p.num_qo_heads + head) * D;
@@ -827,6 +867,10 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(ov[j]);
+            }
+            if (empty) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = 0.f;
             }
             if (!last) {
               float4* dst = reinterpret_cast<float4*>(scratch_row + c0);
@@ -936,7 +980,7 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, 
   }
 }
 
-template <int D, int NT, int ST, bool KV8, bool WIN, bool GATHER>
+template <int D, int NT, int ST, bool KV8, int MK, bool GATHER>
 __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
     bip_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -997,7 +1041,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   if (warp < C::SM_WARPS) {
     if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
-    softmax_role<D, NT, ST, KV8, WIN, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4);
+    softmax_role<D, NT, ST, KV8, MK, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4);
   } else if (warp < C::GA_WARP0) {
     if constexpr (C::DQ_WGS == 2) reg_dealloc<C::DQ_REGS>();
     dequant_role<D, NT, ST, KV8, C::DQ_WGS>(c, sbase, p, (warp - C::DQ_WARP0) / 4);
@@ -1031,29 +1075,29 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
   if (warp == C::CTL_WARP0 + 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-// The sliding-window mask is a separate instantiation, so that the plain
-// causal kernel carries none of its arithmetic; so is the row gather of
-// token-granular pages.
-template <int D, int NT, int ST, bool KV8, bool WIN, bool GATHER>
+// Each mask kind is a separate instantiation, so that the plain causal
+// kernel carries none of the window or custom-mask arithmetic; so is the row
+// gather of token-granular pages.
+template <int D, int NT, int ST, bool KV8, int MK, bool GATHER>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                        int grid, cudaStream_t stream) {
   using C = Cfg<D, NT, ST, KV8, GATHER>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D, NT, ST, KV8, WIN, GATHER>,
+    cudaError_t e = cudaFuncSetAttribute(bip_attn_kernel<D, NT, ST, KV8, MK, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  bip_attn_kernel<D, NT, ST, KV8, WIN, GATHER><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  bip_attn_kernel<D, NT, ST, KV8, MK, GATHER><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 template <int D, int NT, int ST, bool KV8, bool GATHER>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                    int grid, cudaStream_t stream) {
-  return p.window_left > 0 ? launch_one<D, NT, ST, KV8, true, GATHER>(tq, tk, tv, p, grid, stream)
-                           : launch_one<D, NT, ST, KV8, false, GATHER>(tq, tk, tv, p, grid, stream);
+  return p.window_left > 0 ? launch_one<D, NT, ST, KV8, 1, GATHER>(tq, tk, tv, p, grid, stream)
+                           : launch_one<D, NT, ST, KV8, 0, GATHER>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace

@@ -48,6 +48,7 @@ struct UnitDesc {
 struct bip_plan_s {
   int32_t batch = 0, hq = 0, hkv = 0, d = 0, page_size = 0, kv_dtype = 0;
   int32_t group = 0, T = 0, bn = 0, nt = 1, total_q = 0;
+  int32_t max_kv_q = 0;  // longest kv_len among requests with q rows (custom mask row length)
   bip_plan_options opts{};
   std::vector<WorkItem> items;
   std::vector<MergeUnit> merges;
@@ -329,6 +330,8 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->page_size = page_size;
   p->kv_dtype = kv_dtype;
   p->group = group;
+  for (int32_t r = 0; r < batch; ++r)
+    if (q_len[r] > 0) p->max_kv_q = std::max(p->max_kv_q, kv_len[r]);
   p->T = T;
   p->bn = bn;
   p->nt = NT;
@@ -588,12 +591,14 @@ static bool encode_maps(int32_t d, int32_t hq, int32_t hkv, int32_t group, int32
   return true;
 }
 
-extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const void* k_pages,
-                                  const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
-                                  const int32_t* kv_indices, float k_scale, float v_scale, void* out, float* lse,
-                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// bip_prefill, and bip_prefill_masked with a mask (null: none).
+static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const void* k_pages, const void* v_pages,
+                          int64_t num_pages, int64_t page_stride_elems, const int32_t* kv_indices,
+                          const uint32_t* mask, int64_t mask_row_words, float k_scale, float v_scale, void* out,
+                          float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!p) return BIP_ERR_INVALID_ARG;
   if (num_q_rows != p->total_q) return BIP_ERR_INVALID_ARG;
+  if (mask && mask_row_words < (int64_t(p->max_kv_q) + 31) / 32) return BIP_ERR_INVALID_ARG;
   if (p->items.empty()) return BIP_OK;  // nothing to compute (all q_len = 0)
   if (!q || !k_pages || !v_pages || !kv_indices || !out || !lse || !workspace) return BIP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return BIP_ERR_INVALID_ARG;
@@ -636,8 +641,11 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
   ap.wait_limit_cycles = p->wait_limit_cycles;
   ap.window_left = p->opts.window_left;
   set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
-  if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
-    return BIP_ERR_CUDA;
+  ap.mask = mask;
+  ap.mask_row_words = mask ? mask_row_words : 0;
+  const cudaError_t le = mask ? bip::launch_attention_masked(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream)
+                              : bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream);
+  if (le != cudaSuccess) return BIP_ERR_CUDA;
 
   if (!p->merges.empty()) {
     bip::MergeParams mp;
@@ -653,6 +661,24 @@ extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_row
     if (bip::launch_merge(p->d, mp, stream) != cudaSuccess) return BIP_ERR_CUDA;
   }
   return BIP_OK;
+}
+
+extern "C" bip_status bip_prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const void* k_pages,
+                                  const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                                  const int32_t* kv_indices, float k_scale, float v_scale, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return prefill(p, q, num_q_rows, k_pages, v_pages, num_pages, page_stride_elems, kv_indices, nullptr, 0, k_scale,
+                 v_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" bip_status bip_prefill_masked(bip_plan_t p, const void* q, int64_t num_q_rows, const void* k_pages,
+                                         const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                                         const int32_t* kv_indices, const uint32_t* mask, int64_t mask_row_words,
+                                         float k_scale, float v_scale, void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream) {
+  if (!mask || (reinterpret_cast<uintptr_t>(mask) & 3) != 0) return BIP_ERR_INVALID_ARG;
+  return prefill(p, q, num_q_rows, k_pages, v_pages, num_pages, page_stride_elems, kv_indices, mask, mask_row_words,
+                 k_scale, v_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" bip_status bip_append_kv(bip_plan_t p, const void* k_new, const void* v_new, int64_t num_new_rows,
@@ -854,6 +880,8 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
   ap.v_scale = v_scale;
   ap.wait_limit_cycles = p->wait_limit_cycles;
   ap.window_left = p->window_left;
+  ap.mask = nullptr;
+  ap.mask_row_words = 0;
   set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
   if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
     return BIP_ERR_CUDA;

@@ -93,6 +93,11 @@ struct AttnParams {
   const uint8_t* v_pool;
   int64_t page_stride_bytes;
   int32_t slot_bytes;          // one token slot: num_kv_heads * head_dim * element size
+  // Custom mask (null: none): q row r's bits start at mask + r * mask_row_words;
+  // bit j % 32 of word j / 32 set = key j of the request visible to the row
+  // (within the causal and window rule).
+  const uint32_t* mask;
+  int64_t mask_row_words;
 };
 
 struct MergeParams {
@@ -159,13 +164,17 @@ struct DevPlanParams {
   WsHeader* header;
 };
 
-// Kernel launchers (bip_attn.cu / bip_attn_gather.cu / bip_merge.cu /
+// Kernel launchers (bip_attn.cu / bip_attn_gather.cu / bip_attn_mask.cu / bip_merge.cu /
 // bip_append.cu / bip_plan_dev.cu / bip_upload.cu).  launch_attention hands page sizes below
 // 8 to launch_attention_gather.
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
                              cudaStream_t stream);
 cudaError_t launch_attention_gather(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
+                                    const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
+                                    cudaStream_t stream);
+// The custom-mask variants of both (bip_attn_mask.cu): p.mask is set.
+cudaError_t launch_attention_masked(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                                     const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
                                     cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);

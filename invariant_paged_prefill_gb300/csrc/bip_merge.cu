@@ -68,7 +68,9 @@ __global__ void __launch_bounds__(kMergeThreads) bip_merge_kernel(const MergePar
     const int hg = vr % p.group;
     const size_t tok = size_t(u.q_tok0 + pos);
     const int head = u.kv_head * p.group + hg;
-    const float osc = out_scale(L, p.v_scale);
+    // A row with no visible key in any segment (only under a custom mask)
+    // has L = 0 and o = 0: written as zeros, with lse = -inf.
+    const float osc = L > 0.f ? out_scale(L, p.v_scale) : 0.f;
     uint16_t* orow = p.out + (tok * p.num_qo_heads + head) * D;
 #pragma unroll
     for (int e = 0; e < E; ++e) {

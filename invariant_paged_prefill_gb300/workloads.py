@@ -11,6 +11,10 @@ Value recipe (the pages' model shapes with synthetic values):
 * Page ids: a seeded random permutation of the pool; pool pages and slots
   that no request owns are poisoned (NaN) so that any read of them shows up.
 * Seeds: data 0, pages 1, lengths 2 unless a caller passes others.
+* Custom masks (``prompt_mask``): one boolean ``[n, n]`` mask per prompt, a
+  row pattern drawn per row (all keys, a random half, a contiguous range of
+  keys ending at the row, or none); an extend takes the prompt mask's tail
+  rows, so its rows carry the same mask rows as the full prefill.
 
 A request is a *prompt* (per-token q, k, v for ``kv_len`` tokens) plus the
 number of tail rows ``q_len`` sent to attention.  The q rows of a request
@@ -24,6 +28,7 @@ from __future__ import annotations
 import dataclasses
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 BF16_NAN_BITS = 0x7FC0
@@ -276,3 +281,25 @@ def sweep_grid():
                 if (heads, ql, kv_eff) not in pts:
                     pts.append((heads, ql, kv_eff))
     return pts
+
+
+MASK_ROW_KINDS = ("all", "half", "range", "none")
+
+
+def prompt_mask(n: int, seed: int, probs: Sequence[float] = (0.4, 0.4, 0.15, 0.05)) -> np.ndarray:
+    """Seeded boolean custom mask ``[n, n]`` for the full prefill of an n-token prompt.
+
+    Row i (sequence position i) follows one of ``MASK_ROW_KINDS``, drawn with
+    ``probs``: every key; each key with probability 1/2; keys s .. n - 1 for a
+    uniform s in [0, i]; no key.  Bits past a row's own position are drawn too
+    (attention ignores them).  Row i of an extend is row kv_len - q_len + i.
+    """
+    rng = np.random.default_rng(seed)
+    kind = rng.choice(len(MASK_ROW_KINDS), size=n, p=np.asarray(probs, dtype=np.float64))
+    m = rng.random((n, n)) < 0.5
+    start = (rng.random(n) * (np.arange(n) + 1)).astype(np.int64)
+    cols = np.arange(n)[None, :]
+    m[kind == 0] = True
+    m[kind == 2] = cols >= start[kind == 2][:, None]
+    m[kind == 3] = False
+    return m

@@ -27,8 +27,11 @@ def to_device(b: W.PagedBatch, device) -> W.PagedBatch:
 
 def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 << 20, num_sms: int = 0,
             wait_limit_ns: int = 0, check_status: bool = True, k_scale: float = 1.0, v_scale: float = 1.0,
-            tiles_per_unit: int = 0, window_left: int = 0):
-    """Plan + prefill on the device; returns (out, lse, plan) on the host."""
+            tiles_per_unit: int = 0, window_left: int = 0, custom_mask=None, mask_row_words=None):
+    """Plan + prefill on the device; returns (out, lse, plan) on the host.
+
+    ``custom_mask``: one boolean ``[q_len, kv_len]`` array per request (packed
+    with ``pack_mask`` and copied to the device), or None."""
     d = b if b.q.is_cuda else to_device(b, device)
     plan = bip.Plan(d.qo_indptr, d.kv_indptr, d.kv_last_page_len, num_qo_heads=d.num_qo_heads,
                     num_kv_heads=d.num_kv_heads, head_dim=d.head_dim, page_size=d.page_size, kv_dtype=d.kv_dtype,
@@ -37,8 +40,11 @@ def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     out = torch.full_like(d.q, float("nan"))
     lse = torch.full((d.q.shape[0], d.q.shape[1]), float("nan"), dtype=torch.float32, device=device)
+    words = None
+    if custom_mask is not None:
+        words = torch.from_numpy(bip.pack_mask(custom_mask, mask_row_words)).to(device)
     bip.prefill(plan, d.q, d.k_pages, d.v_pages, d.kv_indices, out=out, lse=lse, workspace=ws,
-                k_scale=k_scale, v_scale=v_scale)
+                k_scale=k_scale, v_scale=v_scale, custom_mask=words)
     status = bip.read_device_status(ws)
     if check_status:
         where = int(ws[4:8].view(torch.int32).item())  # header: status, wait site, bad page count
@@ -46,7 +52,7 @@ def run_gpu(b: W.PagedBatch, device, *, policy: str = "auto", budget: int = 256 
     return out.cpu(), lse.cpu(), plan
 
 
-def oracle(b: W.PagedBatch, rows=None, window_left: int = 0):
+def oracle(b: W.PagedBatch, rows=None, window_left: int = 0, custom_mask=None):
     kind = "bf16" if b.kv_dtype == "bf16" else "e4m3"
     kp = b.k_pages.cpu() if b.k_pages.is_cuda else b.k_pages
     vp = b.v_pages.cpu() if b.v_pages.is_cuda else b.v_pages
@@ -55,7 +61,8 @@ def oracle(b: W.PagedBatch, rows=None, window_left: int = 0):
     return pa.paged_prefill(b.q.cpu().view(torch.int16).numpy(), kview.numpy(), vview.numpy(),
                             b.qo_indptr.tolist(), b.kv_indptr.tolist(), b.kv_indices.cpu().tolist(),
                             b.kv_last_page_len.tolist(), b.num_qo_heads, b.num_kv_heads, b.page_size,
-                            q_kind="bf16", kv_kind=kind, rows=rows, window_left=window_left)
+                            q_kind="bf16", kv_kind=kind, rows=rows, window_left=window_left,
+                            custom_mask=custom_mask)
 
 
 def assert_close_to_oracle(out, lse, ref_out, ref_lse, rows=None):

@@ -105,6 +105,44 @@ def test_prefill_rejects_before_touching_memory(lib):
     assert lib.bip_prefill(empty._h, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, None, None, 0, None) == 0
 
 
+def test_masked_prefill_rejects_before_touching_memory(lib):
+    # kv_len 37 (pages 16, 16, 5): a mask row needs ceil(37 / 32) = 2 words
+    plan = bip.Plan([0, 3], [0, 3], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(mask, words):
+        return lib.bip_prefill_masked(plan._h, fake, 3, fake, fake, 3, 16 * 8 * 128, fake, mask, words, 1.0, 1.0,
+                                      fake, fake, fake, plan.workspace_bytes - 1, None)
+    assert call(None, 2) == 1                                  # no mask
+    assert call(ctypes.c_void_p((1 << 20) + 2), 2) == 1        # mask not 4-byte aligned
+    assert call(fake, 1) == 1                                  # rows shorter than the longest kv_len
+    assert call(fake, 2) == 3                                  # valid mask: on to the workspace check
+    # the rule counts only requests with q rows: a long request without any
+    # sets no minimum
+    mixed = bip.Plan([0, 0, 2], [0, 40, 41], [16, 9], num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    rc = lib.bip_prefill_masked(mixed._h, fake, 2, fake, fake, 41, 16 * 8 * 128, fake, fake, 1, 1.0, 1.0, fake,
+                                fake, fake, mixed.workspace_bytes - 1, None)
+    assert rc == 3
+
+
+def test_pack_mask_bit_layout():
+    rng = np.random.default_rng(4)
+    masks = [rng.random((3, 37)) < 0.5, rng.random((2, 70)) < 0.5, np.zeros((0, 5), dtype=bool)]
+    words = bip.pack_mask(masks)
+    assert words.dtype == np.int32 and words.shape == (5, 3)
+    row = 0
+    for m in masks:
+        for i in range(m.shape[0]):
+            for j in range(3 * 32):
+                bit = (int(words[row, j // 32]) >> (j % 32)) & 1
+                assert bit == (int(m[i, j]) if j < m.shape[1] else 0), (row, j)
+            row += 1
+    assert bip.pack_mask(masks, row_words=5).shape == (5, 5)
+    assert np.array_equal(bip.pack_mask(masks, row_words=5)[:, :3], words)
+    with pytest.raises(bip.BipError):
+        bip.pack_mask(masks, row_words=2)
+
+
 def test_append_rejects_before_touching_memory(lib):
     plan = bip.Plan([0, 3], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
     fake = ctypes.c_void_p(1 << 20)

@@ -1,0 +1,153 @@
+"""Custom masks on the GPU: each q row sees the keys that the causal (and
+window) rule allows and its own mask row selects.  Parity with the oracle in
+every kernel variant (both head dims, FP8 pages, token-granular pages, one or
+two tiles per CTA), rows with no visible key written as zeros with lse -inf,
+and the plain path's bit-exactness properties under a mask: extend rows equal
+full-prefill rows, split / fold / tiles per CTA change no bit, an all-ones
+mask equals no mask, a band mask equals the sliding window."""
+
+import numpy as np
+import pytest
+import torch
+
+import invariant_paged_prefill_gb300 as bip
+from invariant_paged_prefill_gb300 import workloads as W
+
+from gpu_helpers import ATOL, RTOL, assert_bitwise, oracle, run_gpu, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+# a fresh prefill across two segments, extends behind long and short
+# prefixes, a short fresh prefill
+LENS, Q_LENS = (5000, 4700, 1300, 60), (5000, 37, 3, 60)
+
+
+def _batch(heads, kv_dtype="bf16", page_size=16, lens=LENS, q_lens=Q_LENS, seed_pages=9):
+    prompts = [W.make_prompt(n, *heads, seed=90 + i, kv_dtype=kv_dtype) for i, n in enumerate(lens)]
+    return W.layout(prompts, list(q_lens), page_size, seed_pages=seed_pages, kv_dtype=kv_dtype, poison=True)
+
+
+def _masks(b, seed=0):
+    """Request r's rows of its prompt's mask (the prompt mask's tail rows)."""
+    return [W.prompt_mask(n, seed + 31 * r)[n - ql:, :n] for r, (n, ql) in enumerate(zip(b.kv_lens, b.q_lens))]
+
+
+def _rows(b, masks, seed, per_request=12):
+    """Sampled rows plus up to six rows per request with no visible key."""
+    rows = set(sample_rows(b, per_request=per_request, seed=seed))
+    for r, m in enumerate(masks):
+        lo, _ = b.row_range(r)
+        ql, kl = b.q_lens[r], b.kv_lens[r]
+        empty = [i for i in range(ql) if not m[i, :kl - ql + i + 1].any()]
+        rows.update(lo + i for i in empty[:6])
+    return sorted(rows)
+
+
+def _check(out, lse, ref_out, ref_lse, rows):
+    """Rows with no visible key: out exactly 0 and lse -inf; the rest within
+    the tolerance.  Returns how many (row, head) pairs were empty."""
+    o = out.float().numpy().astype(np.float64)[rows]
+    l = lse.numpy().astype(np.float64)[rows]
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(l), empty), "the rows with no visible key differ"
+    assert (o[empty] == 0).all(), "a row with no visible key has a nonzero output"
+    full = ~empty
+    assert np.isfinite(o[full]).all() and np.isfinite(l[full]).all(), "non-finite output"
+    for name, got, ref in (("out", o[full], ref_out[full]), ("lse", l[full], ref_lse[full])):
+        err = np.abs(got - ref)
+        bad = err > ATOL + RTOL * np.abs(ref)
+        assert not bad.any(), f"{name}: {bad.sum()} elements outside tolerance, max abs err {err.max():.3e}"
+    return int(empty.sum())
+
+
+VARIANTS = [
+    (W.HEADS_A, "bf16", 16, 2), (W.HEADS_A, "bf16", 16, 1), (W.HEADS_B, "bf16", 16, 1),
+    (W.HEADS_A, "fp8_e4m3", 16, 1), (W.HEADS_B, "fp8_e4m3", 16, 1),
+    (W.HEADS_A, "bf16", 1, 1), (W.HEADS_B, "bf16", 2, 1), (W.HEADS_A, "fp8_e4m3", 1, 1), (W.HEADS_B, "fp8_e4m3", 4, 1),
+]
+
+
+@pytest.mark.parametrize("heads,kv_dtype,page_size,tiles", VARIANTS)
+def test_mask_matches_oracle(cuda, heads, kv_dtype, page_size, tiles):
+    b = _batch(heads, kv_dtype, page_size)
+    masks = _masks(b, seed=page_size)
+    out, lse, _ = run_gpu(b, cuda, custom_mask=masks, tiles_per_unit=tiles)
+    rows = _rows(b, masks, seed=page_size)
+    ro, rl = oracle(b, rows=rows, custom_mask=masks)
+    assert _check(out, lse, ro, rl, rows) > 0  # rows with no visible key were covered
+
+
+@pytest.mark.parametrize("page_size", [16, 1])
+def test_mask_with_window_matches_oracle(cuda, page_size):
+    b = _batch(W.HEADS_A, page_size=page_size)
+    masks = _masks(b, seed=5)
+    out, lse, _ = run_gpu(b, cuda, custom_mask=masks, window_left=700)
+    rows = _rows(b, masks, seed=5)
+    ro, rl = oracle(b, rows=rows, custom_mask=masks, window_left=700)
+    _check(out, lse, ro, rl, rows)
+
+
+@pytest.mark.parametrize("window", [0, 777])
+def test_mask_extend_equals_full_prefill(cuda, window):
+    # the extend rows of each prompt, with their rows of the prompt's mask,
+    # equal the same rows of its full prefill
+    prompts = [W.make_prompt(n, *W.HEADS_A, seed=120 + i) for i, n in enumerate((4300, 900, 6100))]
+    full = W.layout(prompts, [p.n for p in prompts], 16, seed_pages=2, poison=True)
+    ext = W.layout(prompts, [5, 300, 1], 16, seed_pages=5, poison=True)
+    fo, fl, _ = run_gpu(full, cuda, custom_mask=_masks(full, seed=7), window_left=window)
+    eo, el, _ = run_gpu(ext, cuda, custom_mask=_masks(ext, seed=7), window_left=window)
+    for r in range(3):
+        f0, e0 = int(full.qo_indptr[r]), int(ext.qo_indptr[r])
+        n, off = ext.q_lens[r], full.q_lens[r] - ext.q_lens[r]
+        assert_bitwise(eo[e0:e0 + n], fo[f0 + off:f0 + off + n], f"request {r} out")
+        assert torch.equal(el[e0:e0 + n], fl[f0 + off:f0 + off + n]), f"request {r} lse"
+
+
+def test_mask_split_fold_tiles_and_row_words_are_neutral(cuda):
+    b = _batch(W.HEADS_A)
+    masks = _masks(b, seed=11)
+    ref_o, ref_l, _ = run_gpu(b, cuda, custom_mask=masks, policy="never")
+    assert torch.isneginf(ref_l).any()  # empty rows take part, also in the merge kernel below
+    for kw in (dict(policy="always"), dict(policy="auto"), dict(tiles_per_unit=1), dict(tiles_per_unit=2),
+               dict(mask_row_words=170)):
+        o, l, _ = run_gpu(b, cuda, custom_mask=masks, **kw)
+        assert_bitwise(o, ref_o, f"mask {kw}")
+        assert torch.equal(l, ref_l), f"mask {kw} lse"
+
+
+@pytest.mark.parametrize("heads,kv_dtype,page_size", [(W.HEADS_A, "bf16", 16), (W.HEADS_B, "fp8_e4m3", 16),
+                                                      (W.HEADS_A, "bf16", 1)])
+def test_all_ones_mask_is_no_mask(cuda, heads, kv_dtype, page_size):
+    b = _batch(heads, kv_dtype, page_size)
+    ones = [np.ones((ql, n), dtype=bool) for n, ql in zip(b.kv_lens, b.q_lens)]
+    mo, ml, _ = run_gpu(b, cuda, custom_mask=ones)
+    po, pl, _ = run_gpu(b, cuda)
+    assert_bitwise(mo, po, "all-ones mask vs none")
+    assert_bitwise(ml, pl, "all-ones mask vs none lse")
+
+
+@pytest.mark.parametrize("window", [100, 4500])
+def test_band_mask_equals_window(cuda, window):
+    # keys position - window .. position of every row, as a mask and as the
+    # plan's sliding window: the mask visits the blocks the window skips,
+    # which contribute exact zeros
+    b = _batch(W.HEADS_A)
+    bands = []
+    for n, ql in zip(b.kv_lens, b.q_lens):
+        pos = np.arange(n - ql, n)[:, None]
+        cols = np.arange(n)[None, :]
+        bands.append((cols >= pos - window) & (cols <= pos))
+    mo, ml, _ = run_gpu(b, cuda, custom_mask=bands)
+    wo, wl, _ = run_gpu(b, cuda, window_left=window)
+    assert_bitwise(mo, wo, f"band {window} vs window")
+    assert_bitwise(ml, wl, f"band {window} vs window lse")
+
+
+def test_mask_rows_too_short_are_rejected(cuda):
+    b = to_device(_batch(W.HEADS_A, lens=(100, 40), q_lens=(100, 40)), cuda)
+    plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=32, num_kv_heads=8, head_dim=128)
+    short = torch.zeros(b.q.shape[0], 3, dtype=torch.int32, device=cuda)  # 100 keys need 4 words
+    with pytest.raises(bip.BipError):
+        bip.prefill(plan, b.q, b.k_pages, b.v_pages, b.kv_indices, custom_mask=short)
+    with pytest.raises(bip.BipError):
+        bip.prefill(plan, b.q, b.k_pages, b.v_pages, b.kv_indices, custom_mask=short[:-1, :].contiguous())
