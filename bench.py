@@ -153,9 +153,10 @@ def make_batch(heads, batch, q_len, kv_len, device, kv_dtype="bf16", seed=0, pag
 class Runner:
     """One workload resident on the device, with its plan and buffers."""
 
-    def __init__(self, b, device, window_left: int = 0):
+    def __init__(self, b, device, window_left: int = 0, mask=None):
         import invariant_paged_prefill_gb300 as bip
         self.bip, self.b, self.device = bip, b, device
+        self.mask = mask  # packed custom mask words on the device, or None
         self.plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=b.num_qo_heads,
                              num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
                              kv_dtype=b.kv_dtype, window_left=window_left)
@@ -169,7 +170,7 @@ class Runner:
         b = self.b
         self.bip.prefill(self.plan, b.q if q is None else q, b.k_pages if kp is None else kp,
                          b.v_pages if vp is None else vp, b.kv_indices if idx is None else idx,
-                         out=self.out, lse=self.lse, workspace=self.ws)
+                         out=self.out, lse=self.lse, workspace=self.ws, custom_mask=self.mask)
 
     def timed(self, steps, warmup, barrier=lambda: None):
         for _ in range(warmup):
@@ -665,6 +666,47 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def profile_mask(b, kind: str, seed: int = 0):
+    """Packed custom mask words ([total_q, words] int32) for a profile run, and
+    the fraction of causal (row, key) pairs it leaves visible.  'half': every
+    key visible with probability 1/2 (no block has all bits set, so every block
+    takes the masked softmax path); 'documents': each request cut into
+    documents of 512 to 4096 tokens, a row seeing only its own document's keys
+    (packed sequences; blocks are wholly in, wholly out or cut once)."""
+    rng = np.random.default_rng(seed)
+    words = (max(b.kv_lens) + 31) // 32
+    out = np.zeros((b.total_q, words), dtype=np.uint32)
+    visible = causal = 0
+    col = np.arange(words, dtype=np.int64)[None, :] * 32
+    for r in range(b.batch):
+        lo, hi = b.row_range(r)
+        ql, kl = b.q_lens[r], b.kv_lens[r]
+        if ql == 0:
+            continue
+        pos = np.arange(kl - ql, kl, dtype=np.int64)
+        causal += int((pos + 1).sum())
+        if kind == "half":
+            out[lo:hi] = rng.integers(0, 1 << 32, size=(ql, words), dtype=np.uint32)
+            bits = np.unpackbits(out[lo:hi].view(np.uint8), axis=1, bitorder="little").reshape(ql, words, 32)
+            rows, wp = np.arange(ql), pos // 32   # the word holding each row's own position
+            before = np.cumsum(bits.sum(axis=2, dtype=np.int64), axis=1)[rows, wp] - bits[rows, wp].sum(axis=1)
+            upto = np.cumsum(bits[rows, wp], axis=1, dtype=np.int64)[rows, pos % 32]
+            visible += int((before + upto).sum())
+        else:
+            cuts = [0]
+            while cuts[-1] < kl:
+                cuts.append(cuts[-1] + int(rng.integers(512, 4097)))
+            start = np.asarray(cuts, dtype=np.int64)[np.searchsorted(cuts, pos, side="right") - 1][:, None]
+            full = col >= start
+            part = (col < start) & (col + 32 > start)
+            shift = np.clip(start - col, 0, 31).astype(np.uint64)
+            w = np.where(full, np.uint64(0xFFFFFFFF),
+                         np.where(part, (np.uint64(0xFFFFFFFF) << shift) & np.uint64(0xFFFFFFFF), np.uint64(0)))
+            out[lo:hi] = w.astype(np.uint32)
+            visible += int((pos[:, None] - start + 1).sum())
+    return out.view(np.int32), visible / max(causal, 1)
+
+
 def run_profile(args):
     """The timed step alone (no extras), for ncu: --workload, --batch override."""
     from invariant_paged_prefill_gb300 import build as B
@@ -681,13 +723,18 @@ def run_profile(args):
     heads, batch, q_len, kv_len = WORKLOADS[args.workload]
     batch = args.batch or batch
     b = make_batch(heads, batch, q_len, kv_len, device, kv_dtype=args.kv_dtype, page_size=args.page_size)
-    run = Runner(b, device)
+    mask, density = None, 1.0
+    if args.mask != "none":
+        words, density = profile_mask(b, args.mask)
+        mask = torch.from_numpy(words).to(device)
+    run = Runner(b, device, mask=mask)
     total, per = run.timed(args.steps, args.warmup)
     ms = statistics.mean(per)
+    # causal pairs: a custom mask narrows what is visible, not what is computed
     fl = flops_of(heads, b.q_lens, b.kv_lens)
     kvb = kv_bytes_of(heads, b.kv_lens, elem=2 if args.kv_dtype == "bf16" else 1)
     print(json.dumps({"profile": args.workload, "page_size": args.page_size, "kv_dtype": args.kv_dtype,
-                      "batch": batch, "ms": ms,
+                      "mask": args.mask, "mask_density": density, "batch": batch, "ms": ms,
                       "tflops": fl / ms / 1e9,
                       "kv_gbs": kvb / ms / 1e6, "launches_per_step": run.launches_per_step,
                       "items": run.plan.info["num_items"], "grid": run.plan.info["grid"],
@@ -736,6 +783,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
     ap.add_argument("--page-size", type=int, default=16, help="with --profile or --sweep: slots per KV page")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16", help="with --sweep or --profile: KV page type")
+    ap.add_argument("--mask", choices=["none", "half", "documents"], default="none",
+                    help="with --profile: a custom mask (random half of the keys, or per-document causal)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -68,3 +68,29 @@ def test_window_at_least_the_sequence_is_plain_causal():
     q_lens, kv_lens = [5, 17, 128], [9, 17, 4103]
     fl, _ = bench.windowed_work(HEADS, q_lens, kv_lens, 5000)
     assert fl == bench.flops_of(HEADS, q_lens, kv_lens)
+
+
+@pytest.mark.parametrize("kind", ["half", "documents"])
+def test_profile_mask_density_and_shape(kind):
+    # the profile's packed mask, unpacked: its reported density is the visible
+    # share of causal pairs; a document mask shows each row a contiguous run of
+    # keys that ends at the row's own position
+    b = bench.make_batch((8, 2, 128), 3, 700, 5000, "cpu")
+    words, density = bench.profile_mask(b, kind, seed=1)
+    assert words.dtype == np.int32 and words.shape == (b.total_q, (5000 + 31) // 32)
+    bits = np.unpackbits(words.view(np.uint8), axis=1, bitorder="little").astype(bool)
+    visible = causal = 0
+    for r in range(b.batch):
+        lo, hi = b.row_range(r)
+        ql, kl = b.q_lens[r], b.kv_lens[r]
+        for i in range(ql):
+            p = row_position(i, ql, kl)
+            seen = bits[lo + i, :p + 1]
+            visible += int(seen.sum())
+            causal += p + 1
+            if kind == "documents":
+                first = int(np.argmax(seen))
+                assert seen[p] and seen[first:].all() and not seen[:first].any()
+                assert p - first < 4096
+    assert abs(density - visible / causal) < 1e-12
+    assert (0.45 < density < 0.55) if kind == "half" else (0.0 < density < 0.5)
