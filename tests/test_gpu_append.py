@@ -8,7 +8,7 @@ import torch
 
 import invariant_paged_prefill_gb300 as bip
 from invariant_paged_prefill_gb300 import workloads as W
-from oracle.kv_append import append_paged_kv, new_row_slots
+from oracle.kv_append import append_paged_kv
 
 from gpu_helpers import assert_bitwise, oracle, assert_close_to_oracle, run_gpu, to_device
 
@@ -102,29 +102,37 @@ def test_fp8_append_writes_exactly_the_oracle_codes(cuda, heads, scales):
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
 def test_append_then_extend_equals_the_full_prefill(cuda, kv_dtype):
-    # Pools laid out from the whole prompts, the tails' slots overwritten with
-    # junk, then the tails appended: the pools come back bit for bit, and the
-    # extend's attention on them equals the full prefill's rows.
-    b, _ = W.radix_burst(n_req=6, prefix=304, kv_dtype=kv_dtype)
-    slots = new_row_slots(b.qo_indptr.tolist(), b.kv_indptr.tolist(), b.kv_indices.tolist(),
-                          b.kv_last_page_len.tolist(), b.page_size)
-    assert len(set(slots)) == len(slots)
-    kp, vp = b.k_pages.clone(), b.v_pages.clone()
-    k_new = torch.stack([b.k_pages[p, s] for p, s in slots])
-    v_new = torch.stack([b.v_pages[p, s] for p, s in slots])
+    # Six prompts behind a shared 304-token prefix.  Pools laid out from the
+    # prompts with junk tail rows get each prompt's own tail rows appended
+    # (sglang PR 46351, "Root cause": the extend sends q_len = seq_len -
+    # prefix_len tail rows): the pools must equal the whole prompts' layout
+    # byte for byte, and the extend's attention on them equals the extend on
+    # the laid-out pools and the oracle.
+    hq, hkv, d = W.HEADS_A
+    tails = [1, 4, 2, 3, 4, 1]
+    pre = W.make_prompt(304, hq, hkv, d, seed=0, kv_dtype=kv_dtype)
+    prompts = [W.concat_prompts(pre, W.make_prompt(t, hq, hkv, d, seed=1000 + i, kv_dtype=kv_dtype))
+               for i, t in enumerate(tails)]
+    junk = 0x7F if kv_dtype == "fp8_e4m3" else float("nan")
+    holes = []
+    for p, t in zip(prompts, tails):
+        k, v = p.k.clone(), p.v.clone()
+        k[p.n - t:] = junk
+        v[p.n - t:] = junk
+        holes.append(W.Prompt(p.q, k, v))
+    kw = dict(seed_pages=1, share_prefix_tokens=304, kv_dtype=kv_dtype)
+    b = W.layout(prompts, tails, 16, **kw)
+    holey = W.layout(holes, tails, 16, **kw)
+    k_new = torch.cat([p.k[p.n - t:] for p, t in zip(prompts, tails)])
+    v_new = torch.cat([p.v[p.n - t:] for p, t in zip(prompts, tails)])
     if kv_dtype == "fp8_e4m3":  # rows to append are bf16: the decoded E4M3 values re-encode to the same codes
         k_new = k_new.view(torch.float8_e4m3fn).to(torch.bfloat16)
         v_new = v_new.view(torch.float8_e4m3fn).to(torch.bfloat16)
-    junk_k, junk_v = b.k_pages.clone(), b.v_pages.clone()
-    for p, s in slots:
-        for junk in (junk_k, junk_v):
-            junk[p, s] = 0x7F if kv_dtype == "fp8_e4m3" else float("nan")
-    holey = W.PagedBatch(**{**b.__dict__, "k_pages": junk_k, "v_pages": junk_v})
-    d, status = _append_gpu(holey, cuda, k_new, v_new)
+    d_, status = _append_gpu(holey, cuda, k_new, v_new)
     assert status == 0
-    assert torch.equal(d.k_pages.cpu().view(torch.uint8), kp.view(torch.uint8))
-    assert torch.equal(d.v_pages.cpu().view(torch.uint8), vp.view(torch.uint8))
-    out_a, lse_a, _ = run_gpu(d, cuda)
+    assert np.array_equal(_pool_bits(d_.k_pages), _pool_bits(b.k_pages))
+    assert np.array_equal(_pool_bits(d_.v_pages), _pool_bits(b.v_pages))
+    out_a, lse_a, _ = run_gpu(d_, cuda)
     out_b, lse_b, _ = run_gpu(b, cuda)
     assert_bitwise(out_a, out_b, "extend after append vs extend on the laid-out pools")
     assert_bitwise(lse_a, lse_b, "lse")
