@@ -65,12 +65,6 @@ namespace {
 // (log2 units): probabilities then stay below 2^8 and O is rescaled rarely.
 constexpr float kLazyRescale = 8.0f;
 
-// Column pairs (mod 8) whose exponentials run on the FMA pipe instead of
-// MUFU.  Measured on GB300: every pair moved to the polynomial made the
-// softmax slower (the exp pass is latency- and register-bound, not MUFU
-// throughput-bound), so none is.
-constexpr uint32_t kFmaPairs = 0x00;
-
 template <int D, int NT, int ST, bool KV8 = false, bool GATHER = false>
 struct Cfg {
   static constexpr int BN = kv_block_for(D);        // keys per block
@@ -749,12 +743,9 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         const float ms = (m == -INFINITY) ? 0.f : __fmul_rn(m, scale);
 
         // Probabilities, the row sum and P (bf16 pairs, packed in place)
-        // written back over the S columns already read.  Column pairs (2i,
-        // 2i+1) whose bit i (mod 8) is set in kFmaPairs take 2^x on the FMA
-        // pipe, the rest on MUFU; the choice depends only on the key's
-        // absolute position (blocks start at multiples of 16).  Masked columns
-        // are computed and then replaced by exact zeros, so a row gets the
-        // same bits through the whole-block and the masked path.
+        // written back over the S columns already read; 2^x on MUFU.  Masked
+        // columns are computed and then replaced by exact zeros, so a row gets
+        // the same bits through the whole-block and the masked path.
         // Row-sum partials: acc[i] holds columns 2i, 2i + 1 (mod 8), each
         // pair summed with one packed add (four chains, so that the adds do
         // not wait on each other); they are combined pairwise at the end.
@@ -773,9 +764,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                 const uint64_t x =
                     ffma2(f2_bits(__uint_as_float(hv[j]), __uint_as_float(hv[j + 1])), sc2, nm2);
                 const int pair = (cu >> 1) & 7;
-                uint64_t e;
-                if (kFmaPairs >> pair & 1) e = ex2_fma2(x);
-                else e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
+                uint64_t e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
                 if (!kWhole)
                   e = f2_bits(col_visible<MK>(cu, lim, lo, mb) ? f2_lo(e) : 0.f,
                               col_visible<MK>(cu + 1, lim, lo, mb) ? f2_hi(e) : 0.f);

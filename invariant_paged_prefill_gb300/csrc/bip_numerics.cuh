@@ -58,42 +58,11 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
 // max(a, b, c), exact.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
-}
-
-// 2^x for a pair of inputs on the FMA pipe, to take load off MUFU for a
-// fixed subset of columns.  Method (Cody-Waite style range reduction, base
-// 2): x = n + f with n the nearest integer (adding and subtracting
-// 1.5 * 2^23), 2^f from a degree-4 polynomial fitted by relative-error
-// weighted least squares on [-1/2, 1/2] (fit_exp2_poly.py; worst relative
-// error 2.7e-6 in float32), and n added to the exponent field.  The bits of
-// t = 1.5 * 2^23 + n are those of 1.5 * 2^23 plus n, and the low 22 bits of
-// 1.5 * 2^23 are zero, so t << 23 is n << 23 (mod 2^32): the exponent add is
-// bits(2^f) + (t << 23).  x is clamped to >= -125 so the result stays a
-// normal number; smaller terms vanish against a row sum that is at least 1.
-// Each lane's result depends only on its own input.
-__device__ __forceinline__ uint64_t ex2_fma2(uint64_t x) {
-  const uint64_t magic = f2_splat(12582912.f);  // 1.5 * 2^23
-  const uint64_t xc = f2_bits(fmaxf(f2_lo(x), -125.f), fmaxf(f2_hi(x), -125.f));
-  const uint64_t t = fadd2(xc, magic);
-  const uint64_t f = fsub2(xc, fsub2(t, magic));
-  uint64_t q = ffma2(f2_splat(0.009560510516166687f), f, f2_splat(0.05591703951358795f));
-  q = ffma2(q, f, f2_splat(0.24024981260299683f));
-  q = ffma2(q, f, f2_splat(0.6931219696998596f));
-  q = ffma2(q, f, f2_splat(0.9999991655349731f));
-  const uint32_t lo = uint32_t(q) + (uint32_t(t) << 23);
-  const uint32_t hi = uint32_t(q >> 32) + (uint32_t(t >> 32) << 23);
-  return uint64_t(lo) | (uint64_t(hi) << 32);
 }
 
 struct MergeStep {
