@@ -150,8 +150,11 @@ bip_status bip_plan_get_info(bip_plan_t plan, bip_plan_info* info);
  * Writes at most capacity items; *count receives the total. */
 bip_status bip_plan_get_items(bip_plan_t plan, int32_t* items, int32_t capacity, int32_t* count);
 
-/* Release a plan.  Call only after work enqueued with it has completed
- * (its host image is read by that work). */
+/* Release a plan.  Calls enqueued with it read its pinned host image when
+ * they run, so this first waits (on the host) for every call that was
+ * enqueued eagerly with the plan to complete.  A CUDA graph that captured a
+ * call reads the image again at each replay: destroy the plan only after
+ * the last replay of every such graph has completed. */
 bip_status bip_plan_destroy(bip_plan_t plan);
 
 /* Enqueue the attention on `stream`; never synchronizes.  DEVICE pointers:
@@ -294,6 +297,8 @@ bip_status bip_graph_plan_destroy(bip_graph_plan_t plan);
  *   - Uses the current device; the stream and buffers must belong to it.  The
  *     first call on a device looks up the array's device address with that
  *     device current (it may load the module): make it before any stream capture.
+ *     The address is kept for the life of the process; calls after a
+ *     cudaDeviceReset of that device are not supported.
  *   - Every call shares the one array, which keeps the last call's contents:
  *     calls whose work overlaps on the GPU race, so order them (one stream, or
  *     events).  Each call rewrites the status word at the head of the array

@@ -61,7 +61,11 @@ def workspace_bound(max_batch: int, max_total_q: int, num_qo_heads: int, num_kv_
 
 
 class Plan:
-    """A batch's tile schedule and work list (host only; immutable)."""
+    """A batch's tile schedule and work list (host only; immutable).
+
+    Closing (or dropping) a plan waits for the calls enqueued with it to
+    finish; keep it alive while a CUDA graph that captured a call with it can
+    still be replayed."""
 
     def __init__(self, qo_indptr, kv_indptr, kv_last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                  head_dim: int, page_size: int = 16, kv_dtype: str = "bf16", split_policy: str = "auto",
@@ -155,7 +159,9 @@ def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, 
 
     q [total_q, Hq, d] bf16; k_pages / v_pages [num_pages, page_size, Hkv, d]
     (a page stride other than page_size*Hkv*d is allowed, the same for K and V);
-    kv_indices int32 on the device.  ``custom_mask``: None, or int32 words
+    kv_indices int32 on the device.  ``out``, ``lse`` and ``workspace`` are
+    allocated on ``stream`` when not given; pass a workspace of your own to
+    read the call's device status afterwards (``read_device_status``).  ``custom_mask``: None, or int32 words
     ``[total_q, row_words]`` on the device (see ``pack_mask``) that narrow each
     row's causal keys (``bip_prefill_masked``).  Returns (out bf16, lse fp32
     natural log).
@@ -164,12 +170,17 @@ def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, 
     _require_cuda(q=q, k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices, out=out, lse=lse,
                   workspace=workspace, custom_mask=custom_mask)
     dev = q.device
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    # Buffers made here belong to the launch stream, so the caching allocator
+    # reuses a temporary workspace only behind this call's kernels.
+    with torch.cuda.stream(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or lse.dtype != torch.float32:
         raise BipError(1, "q/out must be bf16 and lse fp32")
     if not (q.is_contiguous() and out.is_contiguous() and lse.is_contiguous()):
@@ -192,8 +203,6 @@ def prefill(plan: Plan, q, k_pages, v_pages, kv_indices, *, out=None, lse=None, 
             raise BipError(1, "custom_mask must be contiguous int32 [total_q, row_words]")
         if custom_mask.shape[0] != q.shape[0]:
             raise BipError(1, "custom_mask must have one row per q row")
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     args = (_dev_ptr(q, "q"), q.shape[0], _dev_ptr(k_pages, "k_pages"), _dev_ptr(v_pages, "v_pages"),
             k_pages.shape[0], k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"))
@@ -220,8 +229,11 @@ def append_kv(plan: Plan, k_new, v_new, k_pages, v_pages, kv_indices, *, workspa
     _require_cuda(k_new=k_new, v_new=v_new, k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices,
                   workspace=workspace)
     dev = k_new.device
-    if workspace is None:
-        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if workspace is None:  # on the launch stream: reused only behind this call's kernel
+        with torch.cuda.stream(stream):
+            workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     for name, t in (("k_new", k_new), ("v_new", v_new)):
         if t.dtype != torch.bfloat16 or not t.is_contiguous():
             raise BipError(1, f"{name} must be contiguous bf16")
@@ -238,8 +250,6 @@ def append_kv(plan: Plan, k_new, v_new, k_pages, v_pages, kv_indices, *, workspa
             raise BipError(1, f"{name}: slots and heads must be contiguous inside a page")
     if k_pages.shape[0] != v_pages.shape[0] or k_pages.stride(0) != v_pages.stride(0):
         raise BipError(1, "k_pages and v_pages must share page count and stride")
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
     _check(plan._lib.bip_append_kv(plan._h, _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"), k_new.shape[0],
                                    _dev_ptr(k_pages, "k_pages"), _dev_ptr(v_pages, "v_pages"), k_pages.shape[0],
                                    k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"), float(k_scale),

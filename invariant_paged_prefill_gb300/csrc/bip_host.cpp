@@ -64,6 +64,11 @@ struct bip_plan_s {
   uint8_t* upload = nullptr;  // header + items + merges, as copied to the workspace
   const void* upload_dev = nullptr;  // the same pinned buffer as the device sees it (mapped), if it is
   bool pinned = false;
+  // One event per stream the plan's calls were enqueued on (eagerly, not
+  // under capture), recorded after each call: bip_plan_destroy waits for
+  // them before it frees the host image those calls read.
+  std::mutex use_mu;
+  std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;
 };
 
 extern "C" const char* bip_status_string(bip_status s) {
@@ -502,6 +507,11 @@ extern "C" bip_status bip_plan_get_items(bip_plan_t p, int32_t* items, int32_t c
 
 extern "C" bip_status bip_plan_destroy(bip_plan_t p) {
   if (!p) return BIP_ERR_INVALID_ARG;
+  for (auto& u : p->uses) {  // eager work that reads the host image has completed
+    cudaEventSynchronize(u.second);
+    cudaEventDestroy(u.second);
+  }
+  p->uses.clear();
   if (p->upload) {
     if (p->pinned)
       cudaFreeHost(p->upload);
@@ -545,6 +555,37 @@ void set_pools(bip::AttnParams& ap, const void* k_pages, const void* v_pages, in
 }
 
 }  // namespace
+
+// Record that `stream` has work reading the plan's host image (skipped while
+// the stream is being captured: a graph keeps reading the image at every
+// replay, so the plan must outlive it).  Streams beyond the first kMaxUses
+// reuse the oldest entry after waiting for it.
+static void note_use(bip_plan_s* p, cudaStream_t stream) {
+  constexpr size_t kMaxUses = 32;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return;
+  std::lock_guard<std::mutex> lk(p->use_mu);
+  cudaEvent_t ev = nullptr;
+  for (auto& u : p->uses)
+    if (u.first == stream) ev = u.second;
+  if (!ev) {
+    if (p->uses.size() >= kMaxUses) {
+      cudaEventSynchronize(p->uses.front().second);
+      cudaEventDestroy(p->uses.front().second);
+      p->uses.erase(p->uses.begin());
+    }
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    p->uses.emplace_back(stream, ev);
+  }
+  if (cudaEventRecord(ev, stream) != cudaSuccess) cudaGetLastError();
+}
 
 // The first `bytes` of the plan's host image into the workspace, on `stream`:
 // by the upload kernel when the pinned image is mapped into the device's
@@ -660,6 +701,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
     mp.v_scale = v_scale;
     if (bip::launch_merge(p->d, mp, stream) != cudaSuccess) return BIP_ERR_CUDA;
   }
+  note_use(p, stream);
   return BIP_OK;
 }
 
@@ -725,6 +767,7 @@ extern "C" bip_status bip_append_kv(bip_plan_t p, const void* k_new, const void*
   ap.v_scale = v_scale;
   ap.header = reinterpret_cast<bip::WsHeader*>(ws);
   if (bip::launch_append(p->d, fp8, ap, p->sms, stream) != cudaSuccess) return BIP_ERR_CUDA;
+  note_use(p, stream);
   return BIP_OK;
 }
 

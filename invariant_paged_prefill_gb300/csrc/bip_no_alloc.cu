@@ -36,7 +36,10 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_no_alloc_workspace[kNoAllocWorkspaceBytes];
 
 // Device address of the array per device, looked up once with that device
-// current (in host code the array's name is only a stand-in, not an address).
+// current (in host code the array's name is only a stand-in, not an address)
+// and kept for the life of the process: after a cudaDeviceReset of that
+// device the module may load at another address, so calls made after a
+// reset are not supported.
 void* g_no_alloc_addr[kMaxDevices] = {};
 std::mutex g_no_alloc_mu;
 
