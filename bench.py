@@ -486,6 +486,52 @@ def measure_configs(device, reps: int = 20):
     return res
 
 
+# Sweep points timed inside the default run, each reported with its own
+# CUDA-event time per step and roofline: the largest long-q points of both
+# head shapes, and the E4M3 pages.  (heads, q_len, kv_len, kv_dtype)
+SWEEP_EXTRAS = [
+    ((32, 8, 128), 8192, 32768, "bf16"),
+    ((24, 4, 256), 8192, 8192, "bf16"),
+    ((24, 4, 256), 8192, 32768, "bf16"),
+    ((24, 4, 256), 4, 8192, "bf16"),
+    ((24, 4, 256), 32, 32768, "bf16"),
+    ((32, 8, 128), 8192, 8192, "fp8_e4m3"),
+    ((32, 8, 128), 4, 32768, "fp8_e4m3"),
+    ((24, 4, 256), 8192, 8192, "fp8_e4m3"),
+    ((24, 4, 256), 1, 32768, "fp8_e4m3"),
+]
+
+
+def measure_point(heads, q_len, kv_len, kv_dtype, device, steps, warmup, peaks, peak_kind):
+    """One 16-request sweep point: CUDA-event ms per step (mean over ``steps``
+    launches after ``warmup``), TFLOP/s and KV GB/s, and the roofline of the
+    bound that applies (tensor for q_len >= 1028, HBM for q_len <= 32)."""
+    b = make_batch(heads, 16, q_len, kv_len, device, kv_dtype=kv_dtype)
+    run = Runner(b, device)
+    _, per = run.timed(steps, warmup)
+    ms = statistics.mean(per)
+    fl = flops_of(heads, b.q_lens, b.kv_lens)
+    kvb = kv_bytes_of(heads, b.kv_lens, elem=2 if kv_dtype == "bf16" else 1)
+    tflops, gbs = fl / ms / 1e9, kvb / ms / 1e6
+    if q_len >= 1028:
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                "peak_source": f"bf16_tflops (burst) of {peak_kind}"}
+    else:
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                "peak_source": f"hbm_gbs of {peak_kind}"}
+    st = run.bip.read_device_status(run.ws)
+    res = {"workload": f"{16} requests x q_len {q_len} behind kv_len {kv_len}, heads "
+                       f"{heads[0]}/{heads[1]}/{heads[2]}, {kv_dtype} pages of 16",
+           "heads": list(heads), "q_len": q_len, "kv_len": kv_len, "kv_dtype": kv_dtype, "steps": steps,
+           "ms_per_step": ms, "tflops": tflops, "kv_gbs": gbs, "roofline": roof, "status": st,
+           "items": run.plan.info["num_items"], "split_units": run.plan.info["num_split_units"]}
+    del run, b
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_graph(b, device, steps: int, warmup: int):
     """Device-planned prefill captured in a CUDA graph (buffers sized to b):
     ms per replay, and whether the replay matches the host-planned result."""
@@ -659,6 +705,8 @@ def run_ours(args):
                          "peak_source": f"hbm_gbs of {peak_kind}", "traffic": recorded_traffic("append")},
             "short_extend_us": sa_ms * 1e3}
         line["configs"] = measure_configs(device)
+        line["sweep_points"] = [measure_point(h, q, kv, dt, device, args.steps, args.warmup, peaks, peak_kind)
+                                for h, q, kv, dt in SWEEP_EXTRAS]
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
