@@ -65,6 +65,10 @@ namespace {
 // (log2 units): probabilities then stay below 2^8 and O is rescaled rarely.
 constexpr float kLazyRescale = 8.0f;
 
+// Bytes at the end of shared memory for the mbarriers, the TMEM address,
+// the abort mark and (FP8 pages) the q rows' scale exponents.
+constexpr int kBarArea = 1024;
+
 template <int D, int NT, int ST, bool KV8 = false, bool GATHER = false>
 struct Cfg {
   static constexpr int BN = kv_block_for(D);        // keys per block
@@ -84,7 +88,7 @@ struct Cfg {
   static constexpr int OFF_K8 = OFF_V + ST * KV_BYTES;
   static constexpr int OFF_V8 = OFF_K8 + SS * KV8_BYTES;
   static constexpr int OFF_BAR = OFF_V8 + SS * KV8_BYTES;
-  static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + room to align the base to 1024
+  static constexpr int SMEM = OFF_BAR + kBarArea + 1024;  // + room to align the base to 1024
   // Warp roles, whole warpgroups each: softmax warps 0 .. 4 NT - 1 (slot
   // t = warp / 4, TMEM lane quarter = warp % 4), then the FP8 dequant
   // warpgroups, then (GATHER) the row-gather warps, half for K and half for
@@ -93,11 +97,13 @@ struct Cfg {
   // one spare warp.
   static constexpr int SM_WARPS = 4 * NT;
   static constexpr int DQ_WARP0 = SM_WARPS;
-  // FP8 dequant warpgroups, taking alternate blocks.  With two, each owns
-  // one staging stage and one ring slot (block index mod 2), so its parity
-  // waits never run two phases ahead of a barrier; one stage (d = 256)
-  // keeps one warpgroup.  Two give up registers (setmaxnreg); one keeps
-  // its launch count.
+  // FP8 dequant warpgroups.  With two, one converts every K block and the
+  // other every V block, so a K stage is released as soon as its codes are
+  // in registers even while a V block waits for its ring slot; each walks
+  // its stream's stages and slots in order, so its parity waits never run
+  // two phases ahead of a barrier.  One warpgroup converts both (d = 256,
+  // and next to the row-gather warpgroup).  Two give up registers
+  // (setmaxnreg); one keeps its launch count.
   static constexpr int DQ_WGS = KV8 ? ((D == 128 && !GATHER) ? 2 : 1) : 0;
   static constexpr int DQ_REGS = 80;
   static constexpr int GA_WARP0 = SM_WARPS + 4 * DQ_WGS;
@@ -134,11 +140,17 @@ struct Cfg {
     return NT == 2 ? uint32_t(t * 256) : uint32_t(s * BN);
   }
   __host__ __device__ static constexpr uint32_t tm_o(int t) { return NT == 2 ? uint32_t(t * 256 + BN) : 256u; }
+  // One q-tile slot: the q tile also lives in TMEM (D / 2 columns, copied
+  // once per item), so that S = Q K^T reads only K from shared memory.
+  // Two slots fill TMEM with S and O and read q from shared memory.
+  static constexpr bool QT = NT == 1;
+  static constexpr uint32_t TQ = (2 * BN + D / 2 <= 256) ? 2 * BN : 256 + D;
+  static_assert(!QT || (TQ + D / 2 <= TM_COLS && (TQ >= 2 * BN) && (TQ + D / 2 <= 256 || TQ >= 256 + D)),
+                "q tile columns clash with S or O");
   static_assert(NT == 1 || (BN + D <= 256), "two slots need S and O in 256 columns each");
   static_assert(NT == 2 || (2 * BN <= 256 && 256 + D <= TM_COLS), "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(!KV8 || NT == 1, "FP8 pages use the one-tile variant");
-  static_assert(DQ_WGS <= 1 || (SS == DQ_WGS && ST == DQ_WGS), "one staging stage and one slot per dequant warpgroup");
 };
 
 // Barrier slots (8 bytes each) at OFF_BAR.
@@ -153,11 +165,16 @@ enum Bar {
   B_DRAIN = 30,
   B_K8_FULL = 31, B_K8_FREE = 33, B_V8_FULL = 35, B_V8_FREE = 37,  // FP8 staging, up to 2 stages
   B_V_TX = 39,  // bf16 V blocks that end past kv_len land here first (the V producer zeroes the tail)
-  B_COUNT = 40
+  // FP8 pages: the q tile has been converted to f16 (Q_READY, 128 dequant
+  // threads) / the softmax has read the tile's row scales (QS_FREE, 128
+  // softmax threads).
+  B_Q_READY = 40, B_QS_FREE = 41,
+  B_COUNT = 42
 };
 constexpr int OFF_TMEM_SLOT = 8 * B_COUNT;    // u32: TMEM base address
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;  // u32: a wait expired somewhere in this CTA
-static_assert(OFF_ABORT + 4 <= 512, "barrier area");
+constexpr int OFF_QSCALE = 512;               // int8 [128]: FP8 pages, each q row's scale exponent
+static_assert(OFF_ABORT + 4 <= OFF_QSCALE && OFF_QSCALE + kTileRows <= kBarArea, "barrier area");
 
 struct Ctx {
   uint32_t bar0;
@@ -499,8 +516,11 @@ template <int D, int NT, int ST, bool KV8, bool GATHER>
 __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const AttnParams& p) {
   using C = Cfg<D, NT, ST, KV8>;
   const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);  // S = Q K^T, both K-major
-  constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);       // O += P V, V MN-major
+  // bf16 operands; with FP8 pages every operand is f16 (q rows converted
+  // exactly with a per-row power-of-two scale, K and V decoded from E4M3,
+  // P rounded to f16).
+  constexpr uint32_t kIdescS = idesc_f32acc(128, C::BN, false, false, KV8);  // S = Q K^T, both K-major
+  constexpr uint32_t kIdescO = idesc_f32acc(128, D, false, true, KV8);       // O += P V, V MN-major
   // bf16 token rows gathered with cp.async are generic-proxy writes: once
   // their landing phase is seen, a proxy fence orders them before the MMAs'
   // operand reads.  (TMA writes, and FP8 slots the dequant warps fenced,
@@ -515,8 +535,24 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
     const int nb = g.blk_hi - g.blk_lo + 1;
-    if (!wait_phase(c, bar(c, B_Q_FULL), n & 1, 10)) { ok = false; break; }
+    // FP8 pages: the q tile once the dequant warps have converted it to f16
+    if (!wait_phase(c, bar(c, KV8 ? B_Q_READY : B_Q_FULL), n & 1, 10)) { ok = false; break; }
     tc_fence_after();
+    if constexpr (C::QT) {
+      // The previous item's S MMAs read the q columns: wait for its last one
+      // (later PVs stay queued meanwhile), then copy this tile in, one
+      // 32-byte K slice per 8 columns, and free the shared q tile.
+      if (n > 0) {
+        const uint32_t last_s = s_cnt[0] - 1;
+        if (!wait_phase(c, bar(c, B_S_FULL + last_s % C::NS), (last_s / C::NS) & 1, 12)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+#pragma unroll 1
+      for (int k = 0; k < D / 16; ++k)
+        tc_cp_128x256b(tmem + C::TQ + k * 8, dq + uint32_t(((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4));
+      tc_commit(bar(c, B_Q_FREE));
+    }
 
     // S_t for item-local block j into the slot's next S buffer.
     auto issue_s = [&](int t, int j) -> bool {
@@ -539,12 +575,13 @@ __device__ void mma_issuer(const Ctx& c, uint32_t sbase, uint32_t tmem, const At
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t cq = ((k >> 2) * C::Q_CHUNK + (k & 3) * 32) >> 4;
         const uint32_t ck = ((k >> 2) * C::KV_CHUNK + (k & 3) * 32) >> 4;
-        tc_mma_ss(d_tmem, dq + cq, dk + ck, kIdescS, k > 0 ? 1u : 0u);
+        if constexpr (C::QT) tc_mma_ts(d_tmem, tmem + C::TQ + k * 8, dk + ck, kIdescS, k > 0 ? 1u : 0u);
+        else tc_mma_ss(d_tmem, dq + cq, dk + ck, kIdescS, k > 0 ? 1u : 0u);
       }
       tc_commit(bar(c, B_S_FULL + 2 * t + sbuf));
       if (t == g.last_slot) {
         tc_commit(bar(c, B_K_FREE + kslot));                // last reader of this K block
-        if (j == nb - 1) tc_commit(bar(c, B_Q_FREE));       // last reader of the q tiles
+        if (!C::QT && j == nb - 1) tc_commit(bar(c, B_Q_FREE));  // last reader of the q tiles
       }
       ++s_cnt[t];
       return true;
@@ -606,14 +643,16 @@ __device__ __forceinline__ bool col_visible(int j, int lim, int lo, const uint32
 }
 
 template <int D, int NT, int ST, bool KV8, int MK, bool NARROW_LD>
-__device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t) {
+__device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, const int t,
+                             const int8_t* p_qscale) {
   using C = Cfg<D, NT, ST, KV8>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;          // TMEM lanes this warp may access
   const int row = quarter * 32 + lane;   // packed tile row == TMEM lane
   const uint32_t t_lane = tmem + (uint32_t(quarter * 32) << 16);
-  const float scale = p.scale_log2;
+  float scale = p.scale_log2;     // log2(e) k_scale / sqrt(d), per logit of the MMA's S
   uint32_t cnt = 0, pv_seen = 0;  // blocks of this slot processed / PVs known complete
+  uint32_t n_items = 0;           // items of this CTA started
   bool ok = true;
 
   // PV of this slot's block x has completed.  PVs complete in order, so
@@ -625,9 +664,18 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
     return true;
   };
 
-  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x) {
+  for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x, ++n_items) {
     const WorkItem w = p.items[it];
     const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
+    if constexpr (KV8) {
+      // This row's q values were multiplied by 2^e (e from the row's largest
+      // magnitude) when the tile became f16, so its S is 2^e times the
+      // logits: the scale takes 2^-e back out, exactly.
+      if (!wait_warp(c, bar(c, B_Q_READY), n_items & 1, 22)) { ok = false; break; }
+      const int e = *reinterpret_cast<const volatile int8_t*>(p_qscale + row);
+      scale = __fmul_rn(p.scale_log2, __int_as_float((127 - e) << 23));
+      mbar_arrive(bar(c, B_QS_FREE));
+    }
     if (!(g.mask >> t & 1)) continue;
     const int local_pos = row / p.group;
     const int hg = row - local_pos * p.group;
@@ -769,7 +817,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                   e = f2_bits(col_visible<MK>(cu, lim, lo, mb) ? f2_lo(e) : 0.f,
                               col_visible<MK>(cu + 1, lim, lo, mb) ? f2_hi(e) : 0.f);
                 acc[pair & 3] = fadd2(acc[pair & 3], e);
-                hv[j / 2] = pack_bf16x2(f2_lo(e), f2_hi(e));
+                hv[j / 2] = KV8 ? pack_f16x2(f2_lo(e), f2_hi(e)) : pack_bf16x2(f2_lo(e), f2_hi(e));
               }
             };
             if (whole) exp_pass(std::true_type{});
@@ -886,83 +934,157 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
   }
 }
 
-// Two E4M3 codes (low byte first) -> two bf16 (low half first).  Exact: every
-// E4M3 value, subnormals included, is representable in f16, f32 and bf16.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+// Two E4M3 codes (low byte first) -> two f16 (low half first), one
+// conversion instruction.  Exact: every E4M3 value, subnormals included, is
+// an f16 normal number (or zero); the NaN codes give NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  return pack_bf16x2(f.x, f.y);
+  return uint32_t(h.x) | (uint32_t(h.y) << 16);
 }
 
-// FP8 pages (warpgroup wg of NWG takes the blocks b with b mod NWG = wg; NWG
-// is the launching kernel's count, passed explicitly):
-// convert each staged block (BN rows x D codes, row-major) into the
-// bf16, 128-byte-swizzled K/V ring slot the MMAs read; V rows at or past
-// kv_len are written as zeros.  K, then V, per block; the bf16 slot is taken
-// once the MMA that last read it has completed.
+// FP8 pages: the q tile (bf16, 128-byte swizzled rows of 64-column chunks)
+// becomes f16 in place, thread `row` taking one packed row.  The row is
+// multiplied by 2^e, e = 141 - (biased exponent of its largest magnitude),
+// clamped to [-64, 64], so that its largest value lands in [2^14, 2^15):
+// every bf16 value within 2^29 of the row's largest is then exact in f16
+// (8 significant bits, inside f16's normal range), smaller ones round to
+// f16's subnormal grid, which holds them to 2^-39 of the row's largest.
+// e goes to `qscale[row]`; the softmax multiplies its logit scale by 2^-e.
+// A row of zeros (or NaN/inf) keeps e at a clamp end.
+template <int D>
+__device__ __forceinline__ void q_tile_to_f16(uint32_t sQ, int row, int8_t* qscale) {
+  constexpr int DCH = D / 64;
+  const uint32_t rbase = sQ + row * 128;
+  // Units are visited at their swizzled positions (u ^ row % 8), so that the
+  // eight rows of a quarter-warp touch eight different bank groups.
+  uint32_t mx = 0;  // largest |q| as bf16 magnitude bits, in both halves
+#pragma unroll 1
+  for (int ch = 0; ch < DCH; ++ch)
+#pragma unroll 4
+    for (int u = 0; u < 8; ++u) {
+      uint32_t w[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(rbase + ch * kTileRows * 128 + ((u ^ (row & 7)) << 4))
+                   : "memory");
+#pragma unroll
+      for (int j = 0; j < 4; ++j) asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(w[j] & 0x7FFF7FFFu));
+    }
+  const uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);  // bf16 bits: exponent field at [7, 15)
+  const int e = min(64, max(-64, 141 - int(m16 >> 7)));
+  qscale[row] = int8_t(e);
+  const uint64_t s2 = f2_splat(__int_as_float((127 + e) << 23));
+#pragma unroll 1
+  for (int ch = 0; ch < DCH; ++ch)
+#pragma unroll 4
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t a = rbase + ch * kTileRows * 128 + ((u ^ (row & 7)) << 4);
+      uint32_t w[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(a)
+                   : "memory");
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t x = fmul2(f2_bits(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u)), s2);
+        w[j] = pack_f16x2(f2_lo(x), f2_hi(x));
+      }
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                   : "memory");
+    }
+}
+
+// FP8 pages (with NWG = 2 warpgroups, wg 0 converts the K blocks and wg 1
+// the V blocks; with one, it converts K then V of every block; NWG is the
+// launching kernel's count, passed explicitly): convert each staged block
+// (BN rows x D codes, row-major) into the f16, 128-byte-swizzled K/V ring
+// slot the MMAs read; V rows at or past kv_len are written as zeros.  The
+// staging stage is released once the codes are in registers; the ring slot
+// is taken once the MMA that last read it has completed.
 template <int D, int NT, int ST, bool KV8, int NWG>
-__device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, const int wg) {
+__device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, const int wg, int8_t* qscale) {
   if constexpr (KV8) {
     using C = Cfg<D, NT, ST, KV8>;
     const int tid = (int(threadIdx.x) - C::DQ_WARP0 * 32) & 127;  // 0..127 within the warpgroup
-    constexpr int GROUPS = D / 16;                          // 16-code groups per row
-    uint32_t b = 0;
+    uint32_t b = 0, n = 0;  // blocks / items started by this CTA
     bool ok = true;
-    for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < item_count(p) && ok; it += gridDim.x, ++n) {
       const WorkItem w = p.items[it];
       const Geom g = geom_of<NT, C::BN>(w, p.tile_pos);
+      // Warpgroup 0 turns each item's q tile into f16 (thread = packed row)
+      // once it has landed and the softmax has read the previous tile's row
+      // scales; the tile is ready for the MMAs after the proxy fence.
+      if (wg == 0) {
+        if (n > 0 && !wait_warp(c, bar(c, B_QS_FREE), (n - 1) & 1, 34)) { ok = false; break; }
+        if (!wait_warp(c, bar(c, B_Q_FULL), n & 1, 35)) { ok = false; break; }
+        q_tile_to_f16<D>(sbase + C::OFF_Q, tid, qscale);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(c, B_Q_READY));
+      }
       for (int blk = g.blk_lo; blk <= g.blk_hi && ok; ++blk, ++b) {
-        if (int(b % NWG) != wg) continue;  // another warpgroup's block
         const int ss = b % C::SS, slot = b % ST;
         const uint32_t suse = b / C::SS, use = b / ST;
         const int valid_rows = w.kv_len - blk * C::BN;
 #pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
+        for (int which = NWG == 2 ? wg : 0; which < (NWG == 2 ? wg + 1 : 2); ++which) {
           const int full8 = which ? B_V8_FULL : B_K8_FULL, free8 = which ? B_V8_FREE : B_K8_FREE;
           const int full = which ? B_V_FULL : B_K_FULL, freeb = which ? B_V_FREE : B_K_FREE;
           if (!wait_warp(c, bar(c, full8 + ss), suse & 1, 30 + which)) { ok = false; break; }
-          if (use > 0 && !wait_warp(c, bar(c, freeb + slot), (use - 1) & 1, 32 + which)) { ok = false; break; }
           const uint32_t src = sbase + (which ? C::OFF_V8 : C::OFF_K8) + ss * C::KV8_BYTES;
           const uint32_t dst = sbase + (which ? C::OFF_V : C::OFF_K) + slot * C::KV_BYTES;
-          // All of this thread's staged chunks are loaded before any is
-          // converted: each load and store is an ordered asm statement, so
-          // a load-convert-store loop would pay the shared-memory latency
-          // once per 16-code chunk.
-          constexpr int ITER = C::BN * GROUPS / 128;
-          static_assert(C::BN * GROUPS % 128 == 0, "whole chunks per thread");
-          uint32_t raw[ITER][4];
+          // Thread unit: 8 codes (8 staged bytes) -> one 16-byte f16 unit.
+          // Unit u of a block is row u / UPR, unit ui = u % UPR of the row;
+          // 16 consecutive lanes read a 128-byte staged run (conflict-free
+          // 8-byte loads) and each quarter-warp stores the 8 units of one
+          // 64-column chunk row, which the 128-byte swizzle spreads over all
+          // eight 16-byte bank groups (conflict-free stores).  All of this
+          // thread's staged units are loaded before any is converted: each
+          // load and store is an ordered asm statement, so a
+          // load-convert-store loop would pay the shared-memory latency once
+          // per unit.
+          constexpr int UPR = D / 8;                     // f16 units (8 codes) per row
+          constexpr int ITER = C::BN * UPR / 128;
+          constexpr int RSTEP = 128 / UPR;               // rows between a thread's units
+          static_assert(128 % UPR == 0 && C::BN % RSTEP == 0, "whole units per thread");
+          const int r0 = tid / UPR, ui = tid % UPR;
+          const uint32_t src0 = src + r0 * D + ui * 8;
+          uint32_t raw[ITER][2];
+#pragma unroll
+          for (int k = 0; k < ITER; ++k)
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                         : "=r"(raw[k][0]), "=r"(raw[k][1])
+                         : "r"(src0 + k * RSTEP * D)
+                         : "memory");
+          // The staged codes are in registers: the stage may take the next
+          // load while this block waits for its bf16 slot.  The next load is
+          // an async-proxy (TMA or cp.async) write, so a proxy fence orders
+          // the generic-proxy reads above before the arrival releases the
+          // stage to it.
+          fence_proxy_async_smem();
+          mbar_arrive(bar(c, free8 + ss));
+          if (use > 0 && !wait_warp(c, bar(c, freeb + slot), (use - 1) & 1, 32 + which)) { ok = false; break; }
+          const int ch = ui >> 3, pos = ui & 7;
+          const uint32_t dst0 = dst + ch * C::KV_CHUNK + r0 * 128;
 #pragma unroll
           for (int k = 0; k < ITER; ++k) {
-            const int u = tid + 128 * k, r = u / GROUPS, gi = u % GROUPS;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(raw[k][0]), "=r"(raw[k][1]), "=r"(raw[k][2]), "=r"(raw[k][3])
-                         : "r"(src + r * D + gi * 16));
-          }
+            const int r = r0 + k * RSTEP;
+            uint32_t o[4];
 #pragma unroll
-          for (int k = 0; k < ITER; ++k) {
-            const int u = tid + 128 * k, r = u / GROUPS, gi = u % GROUPS;
-            uint32_t o[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              o[2 * j] = e4m3x2_to_bf16x2(raw[k][j]);
-              o[2 * j + 1] = e4m3x2_to_bf16x2(raw[k][j] >> 16);
+            for (int j = 0; j < 2; ++j) {
+              o[2 * j] = e4m3x2_to_f16x2(raw[k][j]);
+              o[2 * j + 1] = e4m3x2_to_f16x2(raw[k][j] >> 16);
             }
             if (which == 1 && r >= valid_rows) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) o[j] = 0u;
+              for (int j = 0; j < 4; ++j) o[j] = 0u;
             }
-            const int ch = gi >> 2, u8 = (gi & 3) * 2;
-            const uint32_t rowb = dst + ch * C::KV_CHUNK + r * 128;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + ((u8 ^ (r & 7)) << 4)), "r"(o[0]),
-                         "r"(o[1]), "r"(o[2]), "r"(o[3])
-                         : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowb + (((u8 + 1) ^ (r & 7)) << 4)),
-                         "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         ::"r"(dst0 + k * RSTEP * 128 + ((pos ^ (r & 7)) << 4)), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                         "r"(o[3])
                          : "memory");
           }
           fence_proxy_async_smem();
           mbar_arrive(bar(c, full + slot));
-          mbar_arrive(bar(c, free8 + ss));
         }
       }
     }
@@ -987,6 +1109,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
   c.header = p.header;
   c.limit_cycles = p.wait_limit_cycles;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + OFF_TMEM_SLOT);
+  int8_t* qscale = reinterpret_cast<int8_t*>(smem + C::OFF_BAR + OFF_QSCALE);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(c, B_Q_FULL), 1);
@@ -1015,6 +1138,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
       }
     mbar_init(bar(c, B_DRAIN), 1);
     mbar_init(bar(c, B_V_TX), 1);
+    mbar_init(bar(c, B_Q_READY), 128);             // one dequant warpgroup
+    mbar_init(bar(c, B_QS_FREE), 32 * C::SM_WARPS);  // every softmax thread
     *c.abort = 0u;
     fence_mbar_init();
   }
@@ -1030,10 +1155,10 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   if (warp < C::SM_WARPS) {
     if constexpr (C::SPLIT_REGS) reg_alloc<C::SM_REGS>();
-    softmax_role<D, NT, ST, KV8, MK, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4);
+    softmax_role<D, NT, ST, KV8, MK, (C::LAUNCH_REGS < 160)>(c, tmem, p, warp / 4, qscale);
   } else if (warp < C::GA_WARP0) {
     if constexpr (C::DQ_WGS == 2) reg_dealloc<C::DQ_REGS>();
-    dequant_role<D, NT, ST, KV8, C::DQ_WGS>(c, sbase, p, (warp - C::DQ_WARP0) / 4);
+    dequant_role<D, NT, ST, KV8, C::DQ_WGS>(c, sbase, p, (warp - C::DQ_WARP0) / 4, qscale);
   } else if (warp < C::CTL_WARP0) {
     if constexpr (C::GA_WARPS > 0) {
       reg_dealloc<C::GA_REGS>();

@@ -18,6 +18,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace bip {
 
@@ -37,7 +38,7 @@ __device__ __forceinline__ float lg2(float x) {
 }
 
 // Packed fp32 pairs: one instruction for two round-to-nearest operations,
-// each lane exactly the scalar __fmaf_rn / __fadd_rn / __fsub_rn.
+// each lane exactly the scalar __fmaf_rn / __fmul_rn / __fadd_rn.
 __device__ __forceinline__ uint64_t f2_bits(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -51,6 +52,11 @@ __device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(uint
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
@@ -97,6 +103,11 @@ __device__ __forceinline__ float final_lse(float m, float l) { return __fmul_rn(
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -133,7 +133,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 x bf16 -> fp32, shape from idesc.
+// D[tmem] (+)= A[smem] * B[smem]^T (bf16 or f16 pairs) -> fp32, shape and types from idesc.
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -144,7 +144,7 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T: A is M rows (TMEM lanes) of K bf16 packed
+// D[tmem] (+)= A[tmem] * B[smem]^T: A is M rows (TMEM lanes) of K 16-bit values packed
 // two per 32-bit column, low half first; a K step of 16 spans 8 columns.
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -156,12 +156,21 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-//   [4,6) D format (1 = f32)   [7,10) A format (1 = bf16)  [10,13) B format
+// Copy a 128-row x 32-byte slice of a shared-memory matrix (described like
+// an MMA operand) into 128 TMEM lanes x 8 columns, 16-bit values packed two
+// per column, low half first: the layout an A operand read from TMEM takes.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor, kind::f16 with fp32 D; A and B both bf16 or both
+// f16 (the kind takes one type for the pair).
+//   [4,6) D format (1 = f32)   [7,10) A format (0 = f16, 1 = bf16)  [10,13) B format
 //   [15] A MN-major  [16] B MN-major  [17,23) N >> 3  [24,29) M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.

@@ -63,6 +63,7 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
         for s in range(NS):
             bar(f"S_FULL{t}{s}"), bar(f"P_FULL{t}{s}", 32 * warps), bar(f"O_DONE{t}{s}")
     bar("Q_FULL"), bar("Q_FREE"), bar("V_TX")
+    bar("Q_READY", 128), bar("QS_FREE", 32 * warps * NT)  # FP8: q tile converted / its row scales read
     clock, pending, last_mma = [0], [], [0]
 
     def later(name, lo=1, hi=8):
@@ -135,28 +136,40 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
                 yield from load_q()
 
     def dequant(wg=0, nwg=1):
+        """Warpgroup 0 converts each item's q tile (after the softmax read the
+        previous tile's row scales); with two warpgroups wg 0 dequantizes
+        every K block and wg 1 every V block, with one it does K then V:
+        staged codes into registers, stage freed, ring slot taken."""
         b = 0
-        for nb, _ in items:
+        for n, (nb, _) in enumerate(items):
+            if wg == 0:
+                if n > 0:
+                    yield wait("QS_FREE", n - 1)
+                yield wait("Q_FULL", n)
+                for _ in range(128):
+                    B["Q_READY"].arrive()
             for _ in range(nb):
-                if b % nwg != wg:  # the other warpgroup's block
-                    b += 1
-                    continue
                 ss, slot = b % SS, b % ST
-                for kv in ("K", "V"):
+                for kv in (("K", "V")[wg],) if nwg == 2 else ("K", "V"):
                     yield wait(f"{kv}8_FULL{ss}", b // SS)
+                    for _ in range(128):  # codes in registers: the stage is free
+                        B[f"{kv}8_FREE{ss}"].arrive()
                     if b // ST > 0:
                         yield wait(f"{kv}_FREE{slot}", b // ST - 1)
                     for _ in range(128):
                         B[f"{kv}_FULL{slot}"].arrive()
-                        B[f"{kv}8_FREE{ss}"].arrive()
                 b += 1
                 yield None
 
     def issuer():
         gb, s_cnt, pv_cnt, k_seen = 0, [0] * NT, [0] * NT, [0]
         for n, (nb, mask) in enumerate(items):
-            yield wait("Q_FULL", n)
+            yield wait("Q_READY" if SS else "Q_FULL", n)
             last = max(t for t in range(NT) if mask >> t & 1)
+            if NT == 1:  # q tile copied into TMEM once the previous item's last S has completed
+                if n > 0:
+                    yield wait(f"S_FULL0{(s_cnt[0] - 1) % NS}", (s_cnt[0] - 1) // NS)
+                commit("Q_FREE")
 
             def issue_s(t, j):
                 kb = gb + j
@@ -166,7 +179,7 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
                 commit(f"S_FULL{t}{s_cnt[t] % NS}")
                 if t == last:
                     commit(f"K_FREE{kb % ST}")
-                    if j == nb - 1:
+                    if NT == 2 and j == nb - 1:
                         commit("Q_FREE")
                 s_cnt[t] += 1
 
@@ -201,7 +214,11 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
                 yield wait(f"O_DONE{t}{x % NS}", x // NS)
                 pv_seen = x + 1
 
-        for nb, mask in items:
+        for n, (nb, mask) in enumerate(items):
+            if SS:  # FP8: the tile's row scales, read once the tile is converted
+                yield wait("Q_READY", n)
+                for _ in range(32):
+                    B["QS_FREE"].arrive()
             if not mask >> t & 1:
                 continue
             for blk in range(nb):
@@ -213,6 +230,8 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
                 cnt += 1
                 yield None
             yield from wait_pv(cnt - 1)                            # segment end: read O
+            for _ in range(rnd.randint(0, 40)):                    # a slow epilogue lets other roles run ahead
+                yield None
 
     if GW:
         roles = [("q_loader", q_loader()), ("issuer", issuer())]
@@ -270,7 +289,8 @@ VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, 
 def test_schedule_never_deadlocks_or_aliases(variant):
     NT, NS, ST, SS, GW, DQ = VARIANTS[variant]
     full = (1 << NT) - 1
-    item_sets = [[(1, full)], [(9, full)], [(4, full), (1, full), (17, full)], [(3, 1), (2, full), (5, 1)]]
+    item_sets = [[(1, full)], [(9, full)], [(4, full), (1, full), (17, full)], [(3, 1), (2, full), (5, 1)],
+                 [(6, full), (1, full), (1, full), (2, full), (1, full), (5, full)]]  # short items run ahead
     if NT == 2:
         item_sets.append([(6, 2), (2, 1), (7, 3)])
     for items in item_sets:
