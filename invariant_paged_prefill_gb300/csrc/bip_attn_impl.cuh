@@ -685,6 +685,20 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
     float Mrun = -INFINITY, Lrun = 0.f;  // merged state of the segments before this one
     float* scratch_row = p.scratch + ((size_t(blockIdx.x) * NT + t) * kTileRows + row) * D;
     const uint32_t o_addr = t_lane + C::tm_o(t);
+    // Custom mask: the row's bits for block blk (bit j of word j / 32 =
+    // column j).  Only words holding a column at or before the row's
+    // position are read (they lie inside the row, below its kv_len); the
+    // next block's words are loaded one block ahead, so that their latency
+    // hides behind a whole block.
+    const uint32_t* mrow = MK == 2 ? p.mask + int64_t(w.q_tok0 + pos) * p.mask_row_words : nullptr;
+    auto load_words = [&](int blk, uint32_t (&dst)[C::BN / 32]) {
+#pragma unroll
+      for (int k = 0; k < C::BN / 32; ++k)
+        dst[k] = (valid && blk <= g.blk_hi && 32 * k <= pos - blk * C::BN)
+                     ? __ldg(mrow + int64_t(blk) * (C::BN / 32) + k) : 0u;
+    };
+    uint32_t mb_next[C::BN / 32];
+    if constexpr (MK == 2) load_words(g.blk_lo, mb_next);
 
     for (int s = w.seg_lo; s <= w.seg_hi && ok; ++s) {
       const int sb_lo = max(s * C::BPS, g.blk_lo);
@@ -698,20 +712,22 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         const int lim = valid ? pos - blk * C::BN : -1;
         const int lo = (MK == 0 || (MK == 2 && p.window_left <= 0)) ? INT_MIN / 2
                                                                     : pos - p.window_left - blk * C::BN;
-        // Custom mask: the row's bits for this block (bit j of word j / 32 =
-        // column j), loaded before the wait on S.  Only words holding a
-        // column <= lim are read; they lie inside the row, since lim + blk *
-        // BN is the row's position, below its kv_len.
-        uint32_t mb[C::BN / 32];
+        // Custom mask: this block's visible columns as bits, vis = mask
+        // words & the causal limit & the window (one bit test per column in
+        // the masked loops); the next block's words are requested now.
+        uint32_t mb[C::BN / 32], vis[C::BN / 32];
 #pragma unroll
-        for (int k = 0; k < C::BN / 32; ++k) mb[k] = 0u;
+        for (int k = 0; k < C::BN / 32; ++k) mb[k] = vis[k] = 0u;
         if constexpr (MK == 2) {
-          if (valid) {
-            const uint32_t* mrow =
-                p.mask + int64_t(w.q_tok0 + pos) * p.mask_row_words + int64_t(blk) * (C::BN / 32);
 #pragma unroll
-            for (int k = 0; k < C::BN / 32; ++k)
-              if (32 * k <= lim) mb[k] = __ldg(mrow + k);
+          for (int k = 0; k < C::BN / 32; ++k) mb[k] = mb_next[k];
+          load_words(blk + 1, mb_next);
+#pragma unroll
+          for (int k = 0; k < C::BN / 32; ++k) {
+            const int base = 32 * k;
+            const uint32_t cw = lim >= base + 31 ? ~0u : (lim < base ? 0u : (~0u >> (31 - (lim - base))));
+            const uint32_t ww = lo <= base ? ~0u : (lo > base + 31 ? 0u : (~0u << (lo - base)));
+            vis[k] = mb[k] & cw & ww;
           }
         }
         if (!wait_warp(c, bar(c, B_S_FULL + 2 * t + sbuf), (cnt / C::NS) & 1, 21)) { ok = false; break; }
@@ -728,16 +744,25 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // the arithmetic but still stores P = 0: its rows may be valid rows
         // past whose position the block lies, and their O keeps accumulating
         // P V.
-        bool all_bits = true;
+        bool whole, live;
         if constexpr (MK == 2) {
-          uint32_t a = ~0u;
+          uint32_t a = ~0u, o = 0u;
 #pragma unroll
-          for (int k = 0; k < C::BN / 32; ++k) a &= mb[k];
-          all_bits = a == ~0u;
+          for (int k = 0; k < C::BN / 32; ++k) {
+            a &= vis[k];
+            o |= vis[k];
+          }
+          whole = __all_sync(0xffffffffu, !valid || a == ~0u);
+          live = __any_sync(0xffffffffu, o != 0u);  // the mask may leave a warp no column at all
+        } else {
+          whole = __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (MK == 0 || lo <= 0)));
+          live = __any_sync(0xffffffffu, lim >= 0 && (MK == 0 || lo < C::BN));
         }
-        const bool whole =
-            __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (MK == 0 || lo <= 0) && all_bits));
-        const bool live = __any_sync(0xffffffffu, lim >= 0 && (MK == 0 || lo < C::BN));
+        // column j visible (masked loops only)
+        auto seen = [&](int j) -> bool {
+          if constexpr (MK == 2) return (vis[j >> 5] >> (j & 31)) & 1u;
+          else return col_visible<MK>(j, lim, lo, mb);
+        };
 
         // Block max.  One TMEM round trip for the whole S row; a 128-column
         // row is then reread in two halves for the exponentials instead of
@@ -758,8 +783,8 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           for (int j = 0; j < C::BN; j += 2) {
             float a = __uint_as_float(sv[j]), b = __uint_as_float(sv[j + 1]);
             if (!kWhole) {
-              a = col_visible<MK>(j, lim, lo, mb) ? a : -INFINITY;
-              b = col_visible<MK>(j + 1, lim, lo, mb) ? b : -INFINITY;
+              a = seen(j) ? a : -INFINITY;
+              b = seen(j + 1) ? b : -INFINITY;
             }
             m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], a, b);
           }
@@ -814,8 +839,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                 const int pair = (cu >> 1) & 7;
                 uint64_t e = f2_bits(ex2(f2_lo(x)), ex2(f2_hi(x)));
                 if (!kWhole)
-                  e = f2_bits(col_visible<MK>(cu, lim, lo, mb) ? f2_lo(e) : 0.f,
-                              col_visible<MK>(cu + 1, lim, lo, mb) ? f2_hi(e) : 0.f);
+                  e = f2_bits(seen(cu) ? f2_lo(e) : 0.f, seen(cu + 1) ? f2_hi(e) : 0.f);
                 acc[pair & 3] = fadd2(acc[pair & 3], e);
                 hv[j / 2] = KV8 ? pack_f16x2(f2_lo(e), f2_hi(e)) : pack_bf16x2(f2_lo(e), f2_hi(e));
               }
