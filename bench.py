@@ -687,7 +687,8 @@ def run_ours(args):
         g_ms, g_out, g_lse = time_graph(b, device, args.steps, args.warmup)
         sg_ms, sg_out, sg_lse = time_graph(sb, device, args.steps, args.warmup)
         line["graph"] = {
-            "what": "device-planned prefill replayed from a captured CUDA graph (every unit folded in one CTA)",
+            "what": "device-planned prefill replayed from a captured CUDA graph (a batch of few units is split "
+                    "by segment on the device; tiles per CTA from the bucket's capacities)",
             "long_q_tflops": fl / (g_ms * 1e-3) / 1e12,
             "short_extend_kv_gbs": kvb / (sg_ms * 1e-3) / 1e9,
             "bit_exact_vs_host_planned": bool(torch.equal(g_out, run.out) and torch.equal(g_lse, run.lse) and

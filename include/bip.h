@@ -241,17 +241,23 @@ bip_status bip_append_kv(bip_plan_t plan, const void* k_new, const void* v_new, 
  * captured token count, Woody-Hu's follow-up; a radix hit and the full
  * recompute of a prompt usually land in different captured buckets,
  * jbymy2000's correction).  A graph plan fixes only capacities and shapes;
- * bip_prefill_graph plans on the device from the indptr arrays each launch
- * and folds every unit in one CTA.  Since no plan choice enters a row's
+ * bip_prefill_graph plans on the device from the indptr arrays each launch:
+ * a batch of few units (fewer than 8 per CTA, e.g. short extends behind long
+ * prefixes) has its multi-segment units split by segment, with partial
+ * states and a merge launch, when they fit the plan's capacities; any other
+ * batch folds every unit in one CTA.  Since no plan choice enters a row's
  * arithmetic, the results are the bits of bip_prefill for the same batch,
  * in any bucket. */
 typedef struct bip_graph_plan_s* bip_graph_plan_t;
 
 /* Capacities: batches of at most max_batch requests with at most
  * max_total_q q rows in all.  Heads, head_dim, page_size, kv_dtype as for
- * bip_plan; opts: num_sms, wait_limit_ns and tiles_per_unit apply,
- * split_policy must not be BIP_SPLIT_ALWAYS.  *workspace_bytes receives the
- * fixed workspace size.  Host only; no device work. */
+ * bip_plan; opts: num_sms, wait_limit_ns, tiles_per_unit and window_left
+ * apply; split_policy BIP_SPLIT_AUTO (default) lets short batches split
+ * within split_budget_bytes of partial states (default 64 MiB without
+ * opts), BIP_SPLIT_NEVER folds every unit, BIP_SPLIT_ALWAYS is refused.
+ * *workspace_bytes receives the fixed workspace size.  Host only; no device
+ * work. */
 bip_status bip_graph_plan(bip_graph_plan_t* plan, int32_t max_batch, int32_t max_total_q, int32_t num_qo_heads,
                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size, bip_kv_dtype kv_dtype,
                           const bip_plan_options* opts, size_t* workspace_bytes);
@@ -277,6 +283,18 @@ bip_status bip_prefill_graph(bip_graph_plan_t plan, int32_t batch, const int32_t
                              const void* k_pages, const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
                              const int32_t* kv_indices, float k_scale, float v_scale, void* out, float* lse,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* bip_prefill_graph under a custom mask (the bip_prefill_masked contract):
+ * mask is a DEVICE array of mask_row_words 32-bit words per q buffer row,
+ * read when the launch runs; a request with rows whose kv_len exceeds
+ * 32 * mask_row_words sets the status word to BIP_ERR_INVALID_ARG and the
+ * launch computes nothing. */
+bip_status bip_prefill_graph_masked(bip_graph_plan_t plan, int32_t batch, const int32_t* qo_indptr,
+                                    const int32_t* kv_indptr, const int32_t* kv_last_page_len, const void* q,
+                                    const void* k_pages, const void* v_pages, int64_t num_pages,
+                                    int64_t page_stride_elems, const int32_t* kv_indices, const uint32_t* mask,
+                                    int64_t mask_row_words, float k_scale, float v_scale, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Release a graph plan (host memory only). */
 bip_status bip_graph_plan_destroy(bip_graph_plan_t plan);

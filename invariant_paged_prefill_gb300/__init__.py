@@ -264,11 +264,12 @@ class GraphPlan:
 
     def __init__(self, max_batch: int, max_total_q: int, *, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                  page_size: int = 16, kv_dtype: str = "bf16", num_sms: int = 0, wait_limit_ns: int = 0,
-                 tiles_per_unit: int = 0, window_left: int = 0):
+                 tiles_per_unit: int = 0, window_left: int = 0, split_policy: str = "auto",
+                 split_budget_bytes: int = 64 << 20):
         self._lib = _lib.load()
         self._h = ctypes.c_void_p()
-        opts = _lib.PlanOptions(_POLICY["auto"], 256 << 20, int(num_sms), int(wait_limit_ns), int(tiles_per_unit),
-                                int(window_left))
+        opts = _lib.PlanOptions(_POLICY[split_policy], int(split_budget_bytes), int(num_sms), int(wait_limit_ns),
+                                int(tiles_per_unit), int(window_left))
         ws = ctypes.c_size_t()
         _check(self._lib.bip_graph_plan(ctypes.byref(self._h), int(max_batch), int(max_total_q), num_qo_heads,
                                         num_kv_heads, head_dim, page_size, _KV[kv_dtype], ctypes.byref(opts),
@@ -291,16 +292,20 @@ class GraphPlan:
 
 
 def prefill_graph(plan: GraphPlan, batch: int, qo_indptr, kv_indptr, kv_last_page_len, q, k_pages, v_pages,
-                  kv_indices, out, lse, workspace, *, k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+                  kv_indices, out, lse, workspace, *, k_scale: float = 1.0, v_scale: float = 1.0, stream=None,
+                  custom_mask=None):
     """Enqueue a device-planned prefill (capturable in a CUDA graph).
 
     The indptr arrays are int32 device tensors read when the launch runs;
     q/out [max_total_q, Hq, d] bf16 and lse [max_total_q, Hq] fp32 are the
-    graph's static buffers.  Results equal ``prefill`` on the same batch.
+    graph's static buffers.  ``custom_mask``: None, or int32 words
+    ``[max_total_q, row_words]`` on the device (``bip_prefill_graph_masked``).
+    Results equal ``prefill`` on the same batch.
     """
     import torch
     _require_cuda(qo_indptr=qo_indptr, kv_indptr=kv_indptr, kv_last_page_len=kv_last_page_len, q=q,
-                  k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices, out=out, lse=lse, workspace=workspace)
+                  k_pages=k_pages, v_pages=v_pages, kv_indices=kv_indices, out=out, lse=lse, workspace=workspace,
+                  custom_mask=custom_mask)
     for name, t, n in (("qo_indptr", qo_indptr, batch + 1), ("kv_indptr", kv_indptr, batch + 1),
                        ("kv_last_page_len", kv_last_page_len, batch)):
         if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n:
@@ -323,17 +328,24 @@ def prefill_graph(plan: GraphPlan, batch: int, qo_indptr, kv_indptr, kv_last_pag
             raise BipError(1, f"{name}: slots and heads must be contiguous inside a page")
     if k_pages.shape[0] != v_pages.shape[0] or k_pages.stride(0) != v_pages.stride(0):
         raise BipError(1, "k_pages and v_pages must share page count and stride")
+    if custom_mask is not None:
+        if custom_mask.dtype != torch.int32 or custom_mask.dim() != 2 or not custom_mask.is_contiguous():
+            raise BipError(1, "custom_mask must be contiguous int32 [max_total_q, row_words]")
+        if custom_mask.shape[0] != plan.max_total_q:
+            raise BipError(1, "custom_mask must have one row per q buffer row")
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    _check(plan._lib.bip_prefill_graph(plan._h, int(batch), _dev_ptr(qo_indptr, "qo_indptr"),
-                                       _dev_ptr(kv_indptr, "kv_indptr"), _dev_ptr(kv_last_page_len,
-                                                                                  "kv_last_page_len"),
-                                       _dev_ptr(q, "q"), _dev_ptr(k_pages, "k_pages"), _dev_ptr(v_pages, "v_pages"),
-                                       k_pages.shape[0], k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"),
-                                       float(k_scale), float(v_scale), _dev_ptr(out, "out"), _dev_ptr(lse, "lse"),
-                                       _dev_ptr(workspace, "workspace"),
-                                       workspace.numel() * workspace.element_size(),
-                                       ctypes.c_void_p(stream.cuda_stream)), "bip_prefill_graph")
+    head = (_dev_ptr(qo_indptr, "qo_indptr"), _dev_ptr(kv_indptr, "kv_indptr"),
+            _dev_ptr(kv_last_page_len, "kv_last_page_len"), _dev_ptr(q, "q"), _dev_ptr(k_pages, "k_pages"),
+            _dev_ptr(v_pages, "v_pages"), k_pages.shape[0], k_pages.stride(0), _dev_ptr(kv_indices, "kv_indices"))
+    tail = (float(k_scale), float(v_scale), _dev_ptr(out, "out"), _dev_ptr(lse, "lse"),
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            ctypes.c_void_p(stream.cuda_stream))
+    if custom_mask is None:
+        _check(plan._lib.bip_prefill_graph(plan._h, int(batch), *head, *tail), "bip_prefill_graph")
+    else:
+        _check(plan._lib.bip_prefill_graph_masked(plan._h, int(batch), *head, _dev_ptr(custom_mask, "custom_mask"),
+                                                  custom_mask.shape[1], *tail), "bip_prefill_graph_masked")
     return out, lse
 
 

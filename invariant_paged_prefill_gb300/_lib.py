@@ -54,6 +54,8 @@ SIGNATURES = {
                                       ctypes.POINTER(PlanOptions), ctypes.POINTER(c_size)]),
     "bip_prefill_graph": (ctypes.c_int, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_vp, c_f32,
                                          c_f32, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "bip_prefill_graph_masked": (ctypes.c_int, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_vp,
+                                                c_vp, c_i64, c_f32, c_f32, c_vp, c_vp, c_vp, c_size, c_vp]),
     "bip_graph_plan_destroy": (ctypes.c_int, [c_vp]),
     "bip_read_device_status": (ctypes.c_int, [c_vp, c_vp]),
     "bip_prefill_no_alloc": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_vp, c_f32, c_f32, c_vp,

@@ -692,6 +692,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
     bip::MergeParams mp;
     mp.units = reinterpret_cast<const MergeUnit*>(ws + p->off_merges);
     mp.n_units = int32_t(p->merges.size());
+    mp.n_units_dev = nullptr;
     mp.num_qo_heads = p->hq;
     mp.group = p->group;
     mp.tile_pos = p->T;
@@ -775,12 +776,20 @@ extern "C" bip_status bip_append_kv(bip_plan_t p, const void* k_new, const void*
 
 struct bip_graph_plan_s {
   int32_t max_batch = 0, max_total_q = 0, hq = 0, hkv = 0, d = 0, page_size = 0, group = 0, T = 0, nt = 1;
-  int32_t grid = 0, capacity = 0;
+  int32_t grid = 0, capacity = 0, merge_capacity = 0;
+  int64_t partial_capacity = 0;  // partial rows
   bip_kv_dtype kv_dtype = BIP_KV_BF16;
   uint64_t wait_limit_cycles = 0;
   int32_t window_left = 0;
-  size_t off_items = 0, off_scratch = 0, ws_bytes = 0;
+  size_t off_items = 0, off_merges = 0, off_partials = 0, off_scratch = 0, ws_bytes = 0;
 };
+
+// Split budget of a graph plan when the caller gives no options: batches
+// with few units split their segments within it (short extends behind long
+// prefixes need a few MB).
+constexpr size_t kDefaultGraphSplitBudget = size_t(64) << 20;
+// Items a graph plan holds beyond one per unit, for split segments.
+constexpr int64_t kGraphSplitItems = 65536;
 
 extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_batch, int32_t max_total_q,
                                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
@@ -797,14 +806,14 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   if ((page_size & (page_size - 1)) != 0 || page_size > bn) return BIP_ERR_UNSUPPORTED;
   bip_plan_options opts;
   opts.split_policy = BIP_SPLIT_AUTO;
-  opts.split_budget_bytes = kDefaultSplitBudget;
+  opts.split_budget_bytes = kDefaultGraphSplitBudget;
   opts.num_sms = 0;
   opts.wait_limit_ns = 0;
   opts.tiles_per_unit = 0;
   opts.window_left = 0;
   if (opts_in) opts = *opts_in;
   if (opts.window_left < 0) return BIP_ERR_INVALID_ARG;
-  if (opts.split_policy == BIP_SPLIT_ALWAYS) return BIP_ERR_UNSUPPORTED;  // graph launches fold every unit
+  if (opts.split_policy == BIP_SPLIT_ALWAYS) return BIP_ERR_UNSUPPORTED;  // the batch decides, on the device
   if (opts.split_policy != BIP_SPLIT_AUTO && opts.split_policy != BIP_SPLIT_NEVER) return BIP_ERR_INVALID_ARG;
   if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
   if (opts.tiles_per_unit < 0 || opts.tiles_per_unit > bip::max_tiles_per_unit_for(head_dim))
@@ -824,11 +833,14 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   p->kv_dtype = kv_dtype;
   p->group = num_qo_heads / num_kv_heads;
   p->T = bip::kTileRows / p->group;
-  // No batch statistics at capture time: two tiles per CTA wherever the
-  // variant exists (numerically neutral, like every plan choice).
+  // No batch statistics at capture time: the host planner's rule (two
+  // tiles per CTA when requests average at least two q tiles) applied to
+  // the bucket's capacities, where the variant exists (numerically neutral,
+  // like every plan choice).
   p->nt = opts.tiles_per_unit ? opts.tiles_per_unit
                               : (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 &&
-                                         page_size >= 8 ? 2 : 1);
+                                         page_size >= 8 && int64_t(max_total_q) >= 2 * int64_t(p->T) * max_batch
+                                     ? 2 : 1);
   int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
   p->grid = std::min(num_sms, bip::kMaxCtas);
   {
@@ -841,9 +853,24 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
     delete p;
     return BIP_ERR_UNSUPPORTED;
   }
-  p->capacity = int32_t(cap);
+  // Split segments (policy AUTO): up to kGraphSplitItems more items, one
+  // merge unit per q tile of a unit, and partial rows within the budget.
+  const bool may_split = opts.split_policy == BIP_SPLIT_AUTO && opts.split_budget_bytes >= partial_row_bytes(head_dim);
+  const int64_t item_cap = cap + (may_split ? kGraphSplitItems : 0);
+  const int64_t merge_cap = may_split ? cap * p->nt : 0;
+  const int64_t part_cap =
+      may_split ? std::min<int64_t>(int64_t(opts.split_budget_bytes / partial_row_bytes(head_dim)), INT32_MAX) : 0;
+  if (item_cap > INT32_MAX || merge_cap > INT32_MAX) {
+    delete p;
+    return BIP_ERR_UNSUPPORTED;
+  }
+  p->capacity = int32_t(item_cap);
+  p->merge_capacity = int32_t(merge_cap);
+  p->partial_capacity = part_cap;
   p->off_items = bip::kHeaderBytes;
-  p->off_scratch = align_up(p->off_items + size_t(cap) * sizeof(WorkItem), 256);
+  p->off_merges = align_up(p->off_items + size_t(item_cap) * sizeof(WorkItem), 256);
+  p->off_partials = align_up(p->off_merges + size_t(merge_cap) * sizeof(MergeUnit), 256);
+  p->off_scratch = align_up(p->off_partials + size_t(part_cap) * partial_row_bytes(head_dim), 256);
   p->ws_bytes = align_up(p->off_scratch + size_t(p->grid) * p->nt * bip::kTileRows * head_dim * sizeof(float), 256);
   *plan_out = p;
   if (workspace_bytes) *workspace_bytes = p->ws_bytes;
@@ -855,17 +882,19 @@ extern "C" bip_status bip_graph_plan_destroy(bip_graph_plan_t p) {
   return BIP_OK;
 }
 
-extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t* qo_indptr,
-                                        const int32_t* kv_indptr, const int32_t* kv_last_page_len, const void* q,
-                                        const void* k_pages, const void* v_pages, int64_t num_pages,
-                                        int64_t page_stride_elems, const int32_t* kv_indices, float k_scale,
-                                        float v_scale, void* out, float* lse, void* workspace,
-                                        size_t workspace_bytes, cudaStream_t stream) {
+// bip_prefill_graph, and bip_prefill_graph_masked with a mask (null: none).
+static bip_status prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t* qo_indptr,
+                                const int32_t* kv_indptr, const int32_t* kv_last_page_len, const void* q,
+                                const void* k_pages, const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
+                                const int32_t* kv_indices, const uint32_t* mask, int64_t mask_row_words,
+                                float k_scale, float v_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
   if (!p) return BIP_ERR_INVALID_ARG;
   if (batch < 0 || batch > p->max_batch) return BIP_ERR_INVALID_ARG;
   if (!qo_indptr || !kv_indptr || !kv_last_page_len || !q || !k_pages || !v_pages || !kv_indices || !out || !lse ||
       !workspace)
     return BIP_ERR_INVALID_ARG;
+  if (mask && mask_row_words <= 0) return BIP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return BIP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return BIP_ERR_INVALID_ARG;
   if (workspace_bytes < p->ws_bytes) return BIP_ERR_WORKSPACE_TOO_SMALL;
@@ -897,10 +926,15 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
   dp.kv_block = bip::kv_block_for(p->d);
   dp.capacity = p->capacity;
   dp.window_left = p->window_left;
+  dp.grid = p->grid;
+  dp.merge_capacity = p->merge_capacity;
+  dp.partial_capacity = p->partial_capacity;
+  dp.mask_row_words = mask ? mask_row_words : 0;
   dp.qo_indptr = qo_indptr;
   dp.kv_indptr = kv_indptr;
   dp.kv_last_page_len = kv_last_page_len;
   dp.items = reinterpret_cast<WorkItem*>(ws + p->off_items);
+  dp.merges = reinterpret_cast<MergeUnit*>(ws + p->off_merges);
   dp.header = header;
   if (bip::launch_device_plan(dp, stream) != cudaSuccess) return BIP_ERR_CUDA;
 
@@ -916,19 +950,60 @@ extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const
   ap.kv_indices = kv_indices;
   ap.out = static_cast<uint16_t*>(out);
   ap.lse = lse;
-  ap.partials = nullptr;  // every item folds its segments
+  ap.partials = reinterpret_cast<float*>(ws + p->off_partials);
   ap.scratch = reinterpret_cast<float*>(ws + p->off_scratch);
   ap.header = header;
   ap.scale_log2 = float(1.4426950408889634 * double(k_scale) / std::sqrt(double(p->d)));
   ap.v_scale = v_scale;
   ap.wait_limit_cycles = p->wait_limit_cycles;
   ap.window_left = p->window_left;
-  ap.mask = nullptr;
-  ap.mask_row_words = 0;
+  ap.mask = mask;
+  ap.mask_row_words = mask ? mask_row_words : 0;
   set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
-  if (bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream) != cudaSuccess)
-    return BIP_ERR_CUDA;
+  const cudaError_t le = mask ? bip::launch_attention_masked(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream)
+                              : bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream);
+  if (le != cudaSuccess) return BIP_ERR_CUDA;
+  if (p->merge_capacity > 0) {
+    // the merge units the planner wrote (none when the batch folded)
+    bip::MergeParams mp;
+    mp.units = dp.merges;
+    mp.n_units = std::min(p->merge_capacity, 4 * p->grid);
+    mp.n_units_dev = &header->n_merges;
+    mp.num_qo_heads = p->hq;
+    mp.group = p->group;
+    mp.tile_pos = p->T;
+    mp.partials = ap.partials;
+    mp.out = ap.out;
+    mp.lse = lse;
+    mp.v_scale = v_scale;
+    if (bip::launch_merge(p->d, mp, stream) != cudaSuccess) return BIP_ERR_CUDA;
+  }
   return BIP_OK;
+}
+
+extern "C" bip_status bip_prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t* qo_indptr,
+                                        const int32_t* kv_indptr, const int32_t* kv_last_page_len, const void* q,
+                                        const void* k_pages, const void* v_pages, int64_t num_pages,
+                                        int64_t page_stride_elems, const int32_t* kv_indices, float k_scale,
+                                        float v_scale, void* out, float* lse, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  return prefill_graph(p, batch, qo_indptr, kv_indptr, kv_last_page_len, q, k_pages, v_pages, num_pages,
+                       page_stride_elems, kv_indices, nullptr, 0, k_scale, v_scale, out, lse, workspace,
+                       workspace_bytes, stream);
+}
+
+extern "C" bip_status bip_prefill_graph_masked(bip_graph_plan_t p, int32_t batch, const int32_t* qo_indptr,
+                                               const int32_t* kv_indptr, const int32_t* kv_last_page_len,
+                                               const void* q, const void* k_pages, const void* v_pages,
+                                               int64_t num_pages, int64_t page_stride_elems,
+                                               const int32_t* kv_indices, const uint32_t* mask,
+                                               int64_t mask_row_words, float k_scale, float v_scale, void* out,
+                                               float* lse, void* workspace, size_t workspace_bytes,
+                                               cudaStream_t stream) {
+  if (!mask || (reinterpret_cast<uintptr_t>(mask) & 3) != 0) return BIP_ERR_INVALID_ARG;
+  return prefill_graph(p, batch, qo_indptr, kv_indptr, kv_last_page_len, q, k_pages, v_pages, num_pages,
+                       page_stride_elems, kv_indices, mask, mask_row_words, k_scale, v_scale, out, lse, workspace,
+                       workspace_bytes, stream);
 }
 
 extern "C" bip_status bip_read_device_status(const void* workspace, cudaStream_t stream) {

@@ -25,7 +25,8 @@ struct WsHeader {
   uint32_t where;           // which wait expired (diagnostics)
   uint32_t bad_pages;       // count of out-of-range page ids seen
   uint32_t n_items;         // work items, when the device planner wrote them
-  uint32_t reserved[60];
+  uint32_t n_merges;        // merge units, when the device planner wrote them
+  uint32_t reserved[59];
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
 
@@ -102,7 +103,8 @@ struct AttnParams {
 
 struct MergeParams {
   const MergeUnit* units;
-  int32_t n_units;
+  int32_t n_units;                 // merge CTAs launched (the count, or a capacity)
+  const uint32_t* n_units_dev;     // if set, the unit count is read here (device-planned launches)
   int32_t num_qo_heads;
   int32_t group;
   int32_t tile_pos;
@@ -142,10 +144,12 @@ struct AppendParams {
 };
 
 // Device-side planner for graph-replayable launches: reads the batch's
-// indptr arrays on the device and writes the fold-only work list (every
-// unit one item over all its segments; no partials, no merge kernel) and
-// its count into the workspace header.  Validation failures set the header
-// status and leave zero items.
+// indptr arrays on the device and writes the work list and its count into
+// the workspace header.  A batch of few units (fewer than 8 per CTA) has
+// every multi-segment unit split by segment, with partials and merge units
+// (count in the header), when they fit the capacities; otherwise every unit
+// folds its segments in one CTA.  Validation failures set the header status
+// and leave zero items.
 struct DevPlanParams {
   int32_t batch;
   int32_t max_total_q;   // q rows the buffers hold
@@ -157,10 +161,15 @@ struct DevPlanParams {
   int32_t kv_block;      // BN
   int32_t capacity;      // work items the workspace holds
   int32_t window_left;   // > 0: sliding window of this many keys left of the diagonal
+  int32_t grid;          // CTAs of the attention launch
+  int32_t merge_capacity;  // merge units the workspace holds (0: never split)
+  int64_t partial_capacity;  // partial rows the workspace holds
+  int64_t mask_row_words;  // > 0: a custom mask of this many words per row (each request's keys must fit)
   const int32_t* qo_indptr;
   const int32_t* kv_indptr;
   const int32_t* kv_last_page_len;
   WorkItem* items;
+  MergeUnit* merges;
   WsHeader* header;
 };
 

@@ -175,7 +175,20 @@ def test_graph_plan_validation_and_sizes(lib):
     assert lib.bip_prefill_graph(*args(8, q=ctypes.c_void_p((1 << 20) + 2))) == 1
     with pytest.raises(bip.BipError):
         bip.GraphPlan(8, 4096, num_qo_heads=32, num_kv_heads=8, head_dim=96)
-    opts = _lib.PlanOptions(2, 1 << 20, 0, 0, 0)   # BIP_SPLIT_ALWAYS: graph launches fold
+    # the masked launch takes the same checks, plus a non-null, 4-byte aligned mask of >= 1 word a row
+    margs = lambda batch, mask=fake, words=4: (gp._h, batch, fake, fake, fake, fake, fake, fake, 1, 16 * 8 * 128,
+                                               fake, mask, words, 1.0, 1.0, fake, fake, fake, gp.workspace_bytes,
+                                               None)
+    assert lib.bip_prefill_graph_masked(*margs(9)) == 1
+    assert lib.bip_prefill_graph_masked(*margs(8, mask=None)) == 1
+    assert lib.bip_prefill_graph_masked(*margs(8, mask=ctypes.c_void_p((1 << 20) + 2))) == 1
+    assert lib.bip_prefill_graph_masked(*margs(8, words=0)) == 1
+    # the split capacity follows the budget; NEVER reserves no partials
+    never = bip.GraphPlan(8, 4096, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_policy="never")
+    small = bip.GraphPlan(8, 4096, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_budget_bytes=1 << 20)
+    assert never.workspace_bytes < small.workspace_bytes < gp.workspace_bytes
+    assert gp.workspace_bytes - never.workspace_bytes >= 64 << 20
+    opts = _lib.PlanOptions(2, 1 << 20, 0, 0, 0)   # BIP_SPLIT_ALWAYS: the batch decides on the device
     h = ctypes.c_void_p()
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 0, ctypes.byref(opts), None) == 2
     opts = _lib.PlanOptions(0, 1 << 20, 0, 0, 2)   # FP8 pages use the one-tile variant

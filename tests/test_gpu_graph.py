@@ -1,7 +1,8 @@
 """Device-planned, graph-replayable prefill: the same bits as the host-planned
 launch for the same batch, eagerly, under CUDA graph replay with new batches
 in the captured buffers, and across captured buckets (a radix hit and the
-full recompute of the same prompts)."""
+full recompute of the same prompts); short batches split by segment on the
+device; custom masks through the graph launch."""
 
 import numpy as np
 import pytest
@@ -53,9 +54,26 @@ class Bucket:
         self.out.fill_(float("nan"))
         self.lse.fill_(float("nan"))
 
-    def launch(self, k_pages, v_pages):
+    def launch(self, k_pages, v_pages, custom_mask=None):
         bip.prefill_graph(self.plan, self.max_batch, self.qo, self.kv, self.last, self.q, k_pages, v_pages,
-                          self.idx, self.out, self.lse, self.ws)
+                          self.idx, self.out, self.lse, self.ws, custom_mask=custom_mask)
+
+
+def _merges_written(ws) -> int:
+    """Merge units the device planner wrote (workspace header word 4)."""
+    return int(ws[16:20].view(torch.int32).item())
+
+
+def _capture(fn):
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return graph
 
 
 def test_device_planned_launch_equals_host_planned(cuda):
@@ -162,3 +180,98 @@ def test_invalid_batch_on_the_device_reports_and_computes_nothing(cuda):
     bk.load(b)
     bk.launch(b.k_pages, b.v_pages)
     assert bip.read_device_status(bk.ws) == 0
+
+
+@pytest.mark.parametrize("heads,kv_dtype", [(W.HEADS_A, "bf16"), (W.HEADS_B, "bf16"), (W.HEADS_A, "fp8_e4m3")])
+def test_short_batch_splits_on_the_device_and_keeps_the_bits(cuda, heads, kv_dtype):
+    # Few units, each behind several 4096-key segments: the device planner
+    # splits them by segment (merge units written), and the results equal the
+    # host-planned launch bit for bit and the oracle within the tolerance,
+    # eagerly and replayed from a captured graph; a plan that never splits
+    # gives the same bits.
+    prompts = [W.make_prompt(n, *heads, seed=80 + i, kv_dtype=kv_dtype) for i, n in enumerate((9000, 5000, 12300))]
+    b = W.layout(prompts, [4, 1, 37], 16, seed_pages=8, kv_dtype=kv_dtype, poison=True)
+    d = to_device(b, cuda)
+    want_o, want_l, _ = run_gpu(d, cuda)
+    n = b.q.shape[0]
+    bk = Bucket(cuda, 4, 64, heads, d.k_pages.shape[0], kv_dtype, max_pages_idx=d.kv_indices.numel() + 8)
+    bk.load(d)
+    bk.launch(d.k_pages, d.v_pages)
+    torch.cuda.synchronize()
+    assert bip.read_device_status(bk.ws) == 0
+    assert _merges_written(bk.ws) > 0, "the short batch was not split"
+    assert_bitwise(bk.out[:n].cpu(), want_o, "split device-planned out")
+    assert_bitwise(bk.lse[:n].cpu(), want_l, "split device-planned lse")
+    graph = _capture(lambda: bk.launch(d.k_pages, d.v_pages))
+    bk.load(d)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert bip.read_device_status(bk.ws) == 0
+    assert_bitwise(bk.out[:n].cpu(), want_o, "split replay out")
+    assert_bitwise(bk.lse[:n].cpu(), want_l, "split replay lse")
+    ro, rl = oracle(b)
+    assert_close_to_oracle(bk.out[:n].cpu(), bk.lse[:n].cpu(), ro, rl)
+    hq, hkv, dd = heads
+    fold = bip.GraphPlan(4, 64, num_qo_heads=hq, num_kv_heads=hkv, head_dim=dd, kv_dtype=kv_dtype,
+                         split_policy="never")
+    ws = torch.empty(fold.workspace_bytes, dtype=torch.uint8, device=cuda)
+    bk.load(d)
+    bip.prefill_graph(fold, bk.max_batch, bk.qo, bk.kv, bk.last, bk.q, d.k_pages, d.v_pages, bk.idx, bk.out,
+                      bk.lse, ws)
+    torch.cuda.synchronize()
+    assert bip.read_device_status(ws) == 0 and _merges_written(ws) == 0
+    assert_bitwise(bk.out[:n].cpu(), want_o, "folded device-planned out")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_masked_graph_replay_matches_host_planned_and_oracle(cuda, kv_dtype):
+    # Custom masks through the graph-replayable launch: an extend behind two
+    # segments (split on the device) and a short fresh prefill, each row
+    # narrowed by its prompt mask's row.  Bits equal the host-planned masked
+    # launch, eagerly and under replay; rows with no visible key are 0 / -inf;
+    # the rest is within the tolerance of the oracle.
+    lens, q_lens = (5000, 300), (37, 300)
+    prompts = [W.make_prompt(n, *W.HEADS_A, seed=60 + i, kv_dtype=kv_dtype) for i, n in enumerate(lens)]
+    b = W.layout(prompts, list(q_lens), 16, seed_pages=4, kv_dtype=kv_dtype, poison=True)
+    d = to_device(b, cuda)
+    masks = [W.prompt_mask(n, 7 + r)[n - ql:, :n] for r, (n, ql) in enumerate(zip(lens, q_lens))]
+    words = (max(lens) + 31) // 32
+    want_o, want_l, _ = run_gpu(d, cuda, custom_mask=masks, mask_row_words=words)
+    n = b.q.shape[0]
+    bk = Bucket(cuda, 3, n + 40, W.HEADS_A, d.k_pages.shape[0], kv_dtype, max_pages_idx=d.kv_indices.numel() + 8)
+    mask_buf = torch.zeros(bk.max_total_q, words, dtype=torch.int32, device=cuda)
+    mask_buf[:n].copy_(torch.from_numpy(bip.pack_mask(masks, words)))
+    bk.load(d)
+    bk.launch(d.k_pages, d.v_pages, custom_mask=mask_buf)
+    torch.cuda.synchronize()
+    assert bip.read_device_status(bk.ws) == 0
+    assert_bitwise(bk.out[:n].cpu(), want_o, "masked device-planned out")
+    assert_bitwise(bk.lse[:n].cpu(), want_l, "masked device-planned lse")
+    graph = _capture(lambda: bk.launch(d.k_pages, d.v_pages, custom_mask=mask_buf))
+    bk.load(d)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert bip.read_device_status(bk.ws) == 0
+    out, lse = bk.out[:n].cpu(), bk.lse[:n].cpu()
+    assert_bitwise(out, want_o, "masked replay out")
+    assert_bitwise(lse, want_l, "masked replay lse")
+    ro, rl = oracle(b, custom_mask=masks)
+    o = out.float().numpy().astype(np.float64)
+    l = lse.numpy().astype(np.float64)
+    empty = np.isneginf(rl)
+    assert empty.any() and np.array_equal(np.isneginf(l), empty) and (o[empty] == 0).all()
+    full = ~empty
+    err_o = np.abs(o[full] - ro[full])
+    assert (err_o <= 2e-2 + 1e-2 * np.abs(ro[full])).all()
+    err_l = np.abs(l[full] - rl[full])
+    assert (err_l <= 2e-2 + 1e-2 * np.abs(rl[full])).all()
+
+
+def test_masked_graph_launch_rejects_a_mask_row_shorter_than_the_keys(cuda):
+    b = to_device(W.tiny(64), cuda)
+    bk = Bucket(cuda, 2, 128, W.HEADS_A, b.k_pages.shape[0], max_pages_idx=b.kv_indices.numel())
+    bk.load(b)
+    short = torch.full((128, 1), -1, dtype=torch.int32, device=cuda)   # 32 keys a row < kv_len 64
+    bk.launch(b.k_pages, b.v_pages, custom_mask=short)
+    assert bip.read_device_status(bk.ws) == 1  # BIP_ERR_INVALID_ARG
+    assert torch.isnan(bk.out.float()).all()
