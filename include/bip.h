@@ -130,8 +130,9 @@ size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, int32_t num_q
  * Supported now: head_dim 128 or 256, gqa_group <= 128, page_size a power of
  * two in [1, BN] (1 = a token-granular pool; below 8 the kernel gathers
  * token rows instead of whole pages, with the same bits), kv_dtype
- * BIP_KV_BF16 or BIP_KV_FP8_E4M3 (FP8 runs one q tile per CTA;
- * tiles_per_unit = 2 with FP8 returns BIP_ERR_UNSUPPORTED).
+ * BIP_KV_BF16 or BIP_KV_FP8_E4M3 (two q tiles per CTA exist at head_dim 128
+ * with pages of 8 or more slots; tiles_per_unit = 2 elsewhere returns
+ * BIP_ERR_UNSUPPORTED).
  * opts may be NULL (defaults).  On success *plan owns the result and
  * *workspace_bytes (if not NULL) receives the exact workspace size, never
  * above bip_workspace_bound for the same shapes.  No device work except a

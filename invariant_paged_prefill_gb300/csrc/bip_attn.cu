@@ -22,6 +22,8 @@ cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, cons
   } else if (tiles_per_unit == 1) {
     if (head_dim == 128) return launch<128, 1, 2, true, false>(tm_q, tm_k, tm_v, p, grid, stream);
     if (head_dim == 256) return launch<256, 1, 2, true, false>(tm_q, tm_k, tm_v, p, grid, stream);
+  } else if (head_dim == 128 && tiles_per_unit == 2) {
+    return launch<128, 2, 2, true, false>(tm_q, tm_k, tm_v, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -83,7 +83,8 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + ST * KV_BYTES;
   // FP8 pages land raw (BN rows x D bytes, unswizzled) in a staging ring and
   // are converted to the bf16 operand layout by the dequant warpgroups.
-  static constexpr int SS = KV8 ? (D == 128 ? 2 : 1) : 0;  // staging stages
+  // (two q-tile slots leave room for one)
+  static constexpr int SS = KV8 ? ((D == 128 && NT == 1) ? 2 : 1) : 0;  // staging stages
   static constexpr int KV8_BYTES = BN * D;
   static constexpr int OFF_K8 = OFF_V + ST * KV_BYTES;
   static constexpr int OFF_V8 = OFF_K8 + SS * KV8_BYTES;
@@ -104,7 +105,7 @@ struct Cfg {
   // two phases ahead of a barrier.  One warpgroup converts both (d = 256,
   // and next to the row-gather warpgroup).  Two give up registers
   // (setmaxnreg); one keeps its launch count.
-  static constexpr int DQ_WGS = KV8 ? ((D == 128 && !GATHER) ? 2 : 1) : 0;
+  static constexpr int DQ_WGS = KV8 ? ((D == 128 && NT == 1 && !GATHER) ? 2 : 1) : 0;
   static constexpr int DQ_REGS = 80;
   static constexpr int GA_WARP0 = SM_WARPS + 4 * DQ_WGS;
   static constexpr int GA_WARPS = GATHER ? (KV8 ? 4 : 8) : 0;
@@ -150,7 +151,7 @@ struct Cfg {
   static_assert(NT == 1 || (BN + D <= 256), "two slots need S and O in 256 columns each");
   static_assert(NT == 2 || (2 * BN <= 256 && 256 + D <= TM_COLS), "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  static_assert(!KV8 || NT == 1, "FP8 pages use the one-tile variant");
+  static_assert(!KV8 || NT == 1 || D == 128, "two FP8 q-tile slots exist at head_dim 128");
 };
 
 // Barrier slots (8 bytes each) at OFF_BAR.
@@ -173,8 +174,9 @@ enum Bar {
 };
 constexpr int OFF_TMEM_SLOT = 8 * B_COUNT;    // u32: TMEM base address
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;  // u32: a wait expired somewhere in this CTA
-constexpr int OFF_QSCALE = 512;               // int8 [128]: FP8 pages, each q row's scale exponent
-static_assert(OFF_ABORT + 4 <= OFF_QSCALE && OFF_QSCALE + kTileRows <= kBarArea, "barrier area");
+constexpr int OFF_QSCALE = 512;               // int8 [NT][128]: FP8 pages, each q row's scale exponent
+static_assert(OFF_ABORT + 4 <= OFF_QSCALE && OFF_QSCALE + kMaxTilesPerUnit * kTileRows <= kBarArea,
+              "barrier area");
 
 struct Ctx {
   uint32_t bar0;
@@ -672,7 +674,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
       // magnitude) when the tile became f16, so its S is 2^e times the
       // logits: the scale takes 2^-e back out, exactly.
       if (!wait_warp(c, bar(c, B_Q_READY), n_items & 1, 22)) { ok = false; break; }
-      const int e = *reinterpret_cast<const volatile int8_t*>(p_qscale + row);
+      const int e = *reinterpret_cast<const volatile int8_t*>(p_qscale + t * kTileRows + row);
       scale = __fmul_rn(p.scale_log2, __int_as_float((127 - e) << 23));
       mbar_arrive(bar(c, B_QS_FREE));
     }
@@ -1041,7 +1043,8 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, 
       if (wg == 0) {
         if (n > 0 && !wait_warp(c, bar(c, B_QS_FREE), (n - 1) & 1, 34)) { ok = false; break; }
         if (!wait_warp(c, bar(c, B_Q_FULL), n & 1, 35)) { ok = false; break; }
-        q_tile_to_f16<D>(sbase + C::OFF_Q, tid, qscale);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) q_tile_to_f16<D>(sbase + C::OFF_Q + t * C::Q_BYTES, tid, qscale + t * kTileRows);
         fence_proxy_async_smem();
         mbar_arrive(bar(c, B_Q_READY));
       }

@@ -33,6 +33,8 @@ cudaError_t launch_attention_masked(int head_dim, int tiles_per_unit, bool kv_fp
   } else if (tiles_per_unit == 1) {
     if (head_dim == 128) return launch_one<128, 1, 2, true, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
     if (head_dim == 256) return launch_one<256, 1, 2, true, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
+  } else if (head_dim == 128 && tiles_per_unit == 2) {
+    return launch_one<128, 2, 2, true, 2, false>(tm_q, tm_k, tm_v, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

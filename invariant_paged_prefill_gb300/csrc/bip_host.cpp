@@ -205,7 +205,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     return BIP_ERR_INVALID_ARG;
   // FP8 pages and token-granular pages (below 8 slots) run one-tile variants
   // (their dequant and row-gather warpgroups need the room).
-  if ((kv_dtype == BIP_KV_FP8_E4M3 || page_size < 8) && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
+  if (page_size < 8 && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
   if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
 
   // ---- lengths and validation
@@ -240,8 +240,7 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
       ++active;
       tiles += (kv_len[r] - 1) / T - (kv_len[r] - q_len[r]) / T + 1;
     }
-    NT = (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 && page_size >= 8 &&
-          tiles >= 2 * active) ? 2 : 1;
+    NT = (bip::max_tiles_per_unit_for(head_dim) >= 2 && page_size >= 8 && tiles >= 2 * active) ? 2 : 1;
   }
 
   // ---- units: (request, kv head, NT consecutive absolute q tiles sharing keys)
@@ -818,7 +817,7 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   if (opts.num_sms < 0) return BIP_ERR_INVALID_ARG;
   if (opts.tiles_per_unit < 0 || opts.tiles_per_unit > bip::max_tiles_per_unit_for(head_dim))
     return BIP_ERR_INVALID_ARG;
-  if ((kv_dtype == BIP_KV_FP8_E4M3 || page_size < 8) && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
+  if (page_size < 8 && opts.tiles_per_unit == 2) return BIP_ERR_UNSUPPORTED;
   if (opts.wait_limit_ns == 0) opts.wait_limit_ns = bip::kDefaultWaitNs;
 
   bip_graph_plan_s* p = new (std::nothrow) bip_graph_plan_s;
@@ -838,8 +837,8 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   // the bucket's capacities, where the variant exists (numerically neutral,
   // like every plan choice).
   p->nt = opts.tiles_per_unit ? opts.tiles_per_unit
-                              : (bip::max_tiles_per_unit_for(head_dim) >= 2 && kv_dtype == BIP_KV_BF16 &&
-                                         page_size >= 8 && int64_t(max_total_q) >= 2 * int64_t(p->T) * max_batch
+                              : (bip::max_tiles_per_unit_for(head_dim) >= 2 && page_size >= 8 &&
+                                         int64_t(max_total_q) >= 2 * int64_t(p->T) * max_batch
                                      ? 2 : 1);
   int num_sms = opts.num_sms > 0 ? opts.num_sms : query_sm_count();
   p->grid = std::min(num_sms, bip::kMaxCtas);

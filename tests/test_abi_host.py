@@ -191,8 +191,9 @@ def test_graph_plan_validation_and_sizes(lib):
     opts = _lib.PlanOptions(2, 1 << 20, 0, 0, 0)   # BIP_SPLIT_ALWAYS: the batch decides on the device
     h = ctypes.c_void_p()
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 0, ctypes.byref(opts), None) == 2
-    opts = _lib.PlanOptions(0, 1 << 20, 0, 0, 2)   # FP8 pages use the one-tile variant
-    assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 1, ctypes.byref(opts), None) == 2
+    opts = _lib.PlanOptions(0, 1 << 20, 0, 0, 2)   # FP8 pages have a two-tile variant at head_dim 128
+    assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 16, 1, ctypes.byref(opts), None) == 0
+    lib.bip_graph_plan_destroy(h)
     # so do token-granular pools (the row-gather warps take the second tile's room)
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 4, 0, ctypes.byref(opts), None) == 2
     assert lib.bip_graph_plan(ctypes.byref(h), 8, 4096, 32, 8, 128, 8, 0, ctypes.byref(opts), None) == 0
@@ -314,12 +315,14 @@ def test_tiles_per_unit_choice():
                     head_dim=256).info["tiles_per_unit"] == 1
     with pytest.raises(bip.BipError):
         bip.Plan([0, 8], [0, 1], [16], num_qo_heads=24, num_kv_heads=4, head_dim=256, tiles_per_unit=2)
-    # FP8 pages run one tile per CTA
+    # FP8 pages follow the same rule (two tiles exist at head_dim 128), except token-granular pools
     assert bip.Plan([0, 8192], [0, 512], [16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                    kv_dtype="fp8_e4m3").info["tiles_per_unit"] == 2
+    assert bip.Plan([0, 4], [0, 2048], [16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
                     kv_dtype="fp8_e4m3").info["tiles_per_unit"] == 1
     with pytest.raises(bip.BipError):
-        bip.Plan([0, 8], [0, 1], [16], num_qo_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="fp8_e4m3",
-                 tiles_per_unit=2)
+        bip.Plan([0, 8], [0, 8], [1], num_qo_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="fp8_e4m3",
+                 page_size=1, tiles_per_unit=2)
     # forcing either variant covers the same tiles
     for tpu in (1, 2):
         p = bip.Plan([0, 100, 103], [0, 7, 70], [4, 16], num_qo_heads=32, num_kv_heads=8, head_dim=128,

@@ -277,6 +277,7 @@ VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, 
     "d128_one_tile": (1, 2, 3, 0, 0, 1),
     "d256": (1, 2, 2, 0, 0, 1),
     "d128_fp8": (1, 2, 2, 2, 0, 2),
+    "d128_fp8_two_tiles": (2, 1, 2, 1, 0, 1),
     "d256_fp8": (1, 2, 2, 1, 0, 1),
     "d128_rows": (1, 2, 3, 0, 4, 1),
     "d256_rows": (1, 2, 2, 0, 4, 1),

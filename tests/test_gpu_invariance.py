@@ -132,12 +132,14 @@ def test_zero_length_requests_and_single_token(cuda):
     assert_bitwise(o[1:], ao)
 
 
-def test_one_and_two_tiles_per_cta_identical(cuda):
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_one_and_two_tiles_per_cta_identical(cuda, kv_dtype):
     # The memory-bound variant (one q tile per CTA, deeper KV ring) and the
-    # ping-pong variant (two tiles per CTA) must give the same bits.
+    # ping-pong variant (two tiles per CTA) must give the same bits, with
+    # bf16 and with E4M3 pages.
     hq, hkv, d = W.HEADS_A
-    prompts = [W.make_prompt(n, hq, hkv, d, seed=60 + i) for i, n in enumerate((5000, 300, 4100, 77))]
-    b = W.layout(prompts, [5000, 3, 900, 40], 16)
+    prompts = [W.make_prompt(n, hq, hkv, d, seed=60 + i, kv_dtype=kv_dtype) for i, n in enumerate((5000, 300, 4100, 77))]
+    b = W.layout(prompts, [5000, 3, 900, 40], 16, kv_dtype=kv_dtype)
     r1 = run_gpu(b, cuda, tiles_per_unit=1)
     r2 = run_gpu(b, cuda, tiles_per_unit=2)
     assert r1[2].info["tiles_per_unit"] == 1 and r2[2].info["tiles_per_unit"] == 2
