@@ -141,6 +141,9 @@ WORKLOADS = {
     # name: (heads, batch, q_len, kv_len)
     "long_q": ((32, 8, 128), 16, 8192, 8192),
     "short_extend": ((32, 8, 128), 16, 4, 32768),
+    # the large-head shape, for --profile
+    "long_q_d256": ((24, 4, 256), 16, 8192, 8192),
+    "short_extend_d256": ((24, 4, 256), 16, 4, 32768),
 }
 
 
@@ -153,13 +156,13 @@ def make_batch(heads, batch, q_len, kv_len, device, kv_dtype="bf16", seed=0, pag
 class Runner:
     """One workload resident on the device, with its plan and buffers."""
 
-    def __init__(self, b, device, window_left: int = 0, mask=None):
+    def __init__(self, b, device, window_left: int = 0, mask=None, tiles_per_unit: int = 0):
         import invariant_paged_prefill_gb300 as bip
         self.bip, self.b, self.device = bip, b, device
         self.mask = mask  # packed custom mask words on the device, or None
         self.plan = bip.Plan(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, num_qo_heads=b.num_qo_heads,
                              num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
-                             kv_dtype=b.kv_dtype, window_left=window_left)
+                             kv_dtype=b.kv_dtype, window_left=window_left, tiles_per_unit=tiles_per_unit)
         self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty_like(b.q)
         self.lse = torch.empty(b.q.shape[0], b.q.shape[1], dtype=torch.float32, device=device)
@@ -705,6 +708,26 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": a_gbs, "peak": hbm, "unit": "GB/s", "frac": a_gbs / hbm,
                          "peak_source": f"hbm_gbs of {peak_kind}", "traffic": recorded_traffic("append")},
             "short_extend_us": sa_ms * 1e3}
+        # custom masks over the long_q and short_extend batches (FLOPs over
+        # the causal pairs: a mask narrows what is visible, not the work)
+        masked = {}
+        for wname, bb, mkind in (("long_q", b, "half"), ("long_q", b, "documents"), ("short_extend", sb, "half")):
+            words, density = profile_mask(bb, mkind)
+            mr = Runner(bb, device, mask=torch.from_numpy(words).to(device))
+            _, mper = mr.timed(args.steps, args.warmup)
+            mms = statistics.mean(mper)
+            hh = heads if wname == "long_q" else sheads
+            ent = {"ms_per_step": mms, "visible_fraction": density,
+                   "tflops": flops_of(hh, bb.q_lens, bb.kv_lens) / mms / 1e9,
+                   "kv_gbs": kv_bytes_of(hh, bb.kv_lens) / mms / 1e6}
+            ent["roofline_frac"] = (ent["tflops"] / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+                                    if wname == "long_q" else
+                                    ent["kv_gbs"] / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
+            masked[f"{wname}_{mkind}"] = ent
+            del mr
+        masked["note"] = ("half: each key visible with probability 1/2; documents: 512-4096-token documents, each "
+                          "row seeing its own; FLOPs and bytes of the unmasked causal work")
+        line["custom_mask"] = masked
         line["configs"] = measure_configs(device)
         line["sweep_points"] = [measure_point(h, q, kv, dt, device, args.steps, args.warmup, peaks, peak_kind)
                                 for h, q, kv, dt in SWEEP_EXTRAS]
@@ -776,6 +799,14 @@ def run_profile(args):
     if args.mask != "none":
         words, density = profile_mask(b, args.mask)
         mask = torch.from_numpy(words).to(device)
+    if args.graph:  # the device-planned launch replayed from a captured graph
+        ms, _, _ = time_graph(b, device, args.steps, args.warmup)
+        fl = flops_of(heads, b.q_lens, b.kv_lens)
+        kvb = kv_bytes_of(heads, b.kv_lens, elem=2 if args.kv_dtype == "bf16" else 1)
+        print(json.dumps({"profile": args.workload, "graph": True, "kv_dtype": args.kv_dtype, "batch": batch,
+                          "ms": ms, "tflops": fl / ms / 1e9, "kv_gbs": kvb / ms / 1e6,
+                          "source_hash": source_hash()}), flush=True)
+        return
     run = Runner(b, device, mask=mask)
     total, per = run.timed(args.steps, args.warmup)
     ms = statistics.mean(per)
@@ -797,9 +828,11 @@ def run_sweep(args):
     device = torch.device("cuda:0")
     peaks, kind = load_peaks()
     for heads, q_len, kv_len in W.sweep_grid():
+        if args.q_lens and q_len not in args.q_lens:
+            continue
         b = make_batch(heads, 16, q_len, kv_len, device, kv_dtype=args.kv_dtype, page_size=args.page_size)
         try:
-            run = Runner(b, device)
+            run = Runner(b, device, tiles_per_unit=args.tiles)
         except Exception as e:  # unsupported shapes are reported, not fatal
             print(json.dumps({"heads": heads, "q_len": q_len, "kv_len": kv_len, "error": str(e)}), flush=True)
             continue
@@ -812,7 +845,8 @@ def run_sweep(args):
                           "kv_len": kv_len, "ms": ms,
                           "tflops": fl / ms / 1e9, "tensor_frac": fl / ms / 1e9 / peaks["bf16_tflops"],
                           "kv_gbs": kvb / ms / 1e6, "hbm_frac": kvb / ms / 1e6 / peaks["hbm_gbs"],
-                          "items": run.plan.info["num_items"], "split_units": run.plan.info["num_split_units"]}),
+                          "items": run.plan.info["num_items"], "split_units": run.plan.info["num_split_units"],
+                          "tiles_per_unit": run.plan.info["tiles_per_unit"]}),
               flush=True)
         del run, b
         torch.cuda.empty_cache()
@@ -832,6 +866,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="with --profile: requests per batch")
     ap.add_argument("--page-size", type=int, default=16, help="with --profile or --sweep: slots per KV page")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16", help="with --sweep or --profile: KV page type")
+    ap.add_argument("--graph", action="store_true", help="with --profile: the device-planned launch, replayed")
+    ap.add_argument("--tiles", type=int, default=0, help="with --sweep: force q tiles per CTA (0 = the plan's)")
+    ap.add_argument("--q-lens", type=int, nargs="*", default=None, help="with --sweep: only these q lengths")
     ap.add_argument("--mask", choices=["none", "half", "documents"], default="none",
                     help="with --profile: a custom mask (random half of the keys, or per-document causal)")
     args = ap.parse_args()
