@@ -23,6 +23,10 @@ namespace bip {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+// Batches of up to this many requests keep each request's offsets in shared
+// memory and write their items one (request, kv head) pair per thread;
+// larger ones write them one request per thread.
+constexpr int kPairRequests = 1536;
 
 struct ReqGeom {
   int32_t q_len, kv_len, g0, groups;  // groups of tiles holding rows of the request
@@ -132,8 +136,47 @@ __device__ __forceinline__ int64_t block_scan(int64_t* s, int64_t v, int64_t& to
   return excl;
 }
 
+// Writes the items of unit (r, gi) for kv head h and, split, its merge
+// units, starting at the given offsets, and advances them.
+__device__ __forceinline__ void write_unit(const DevPlanParams& p, int r, const ReqGeom& g, int gi, int h, bool split,
+                                           int64_t& o, int64_t& part, int64_t& mo) {
+  UnitGeom u = unit_geom(p, r, g, gi);
+  WorkItem w = u.w;
+  w.kv_head = int16_t(h);
+  if (!split || w.seg_hi == w.seg_lo) {
+    p.items[o++] = w;
+    return;
+  }
+  int64_t base[kMaxTilesPerUnit] = {0, 0};
+  for (int t = 0; t < p.tiles_per_unit; ++t) {
+    if (!(w.flags / kSlotPresent >> t & 1)) continue;
+    MergeUnit m;
+    m.q_tok0 = w.q_tok0;
+    m.q_lo = w.q_lo;
+    m.tile = w.tile + t;
+    m.part_base = int32_t(part);
+    m.rows = u.rows[t];
+    m.kv_head = int16_t(h);
+    m.nseg = int16_t(w.nseg[t] - w.seg_lo);  // partials of segments seg_lo .. nseg - 1
+    m.pad[0] = m.pad[1] = 0;
+    p.merges[mo++] = m;
+    base[t] = part;
+    part += int64_t(w.nseg[t] - w.seg_lo) * u.rows[t];
+  }
+  for (int sg = w.seg_lo; sg <= w.seg_hi; ++sg) {
+    WorkItem ws = w;
+    ws.seg_lo = ws.seg_hi = int16_t(sg);
+    ws.flags = int16_t(w.flags | kItemSplit);
+    for (int t = 0; t < p.tiles_per_unit; ++t) ws.part_base[t] = int32_t(base[t] + int64_t(sg - w.seg_lo) * u.rows[t]);
+    p.items[o++] = ws;
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads) bip_device_plan_kernel(const DevPlanParams p) {
   __shared__ int64_t s_sum[kPlanThreads];
+  // small batches: each request's first item, partial row and merge unit
+  __shared__ int32_t s_item[kPairRequests], s_merge[kPairRequests];
+  __shared__ int64_t s_part[kPairRequests];
   __shared__ int s_bad;
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -179,45 +222,48 @@ __global__ void __launch_bounds__(kPlanThreads) bip_device_plan_kernel(const Dev
     return;
   }
 
-  // the items (and, split, the merge units)
+  // the items (and, split, the merge units), in (request, kv head, longest
+  // group first) order
   int64_t o = split ? o_split : o_fold, part = o_part, mo = o_merge;
-  for (int r = r0; r < r1; ++r) {
-    ReqGeom g;
-    request_geom(p, r, g);
-    for (int h = 0; h < p.num_kv_heads; ++h) {
-      for (int gi = g.groups - 1; gi >= 0; --gi) {  // longest group first
-        UnitGeom u = unit_geom(p, r, g, gi);
-        WorkItem w = u.w;
-        w.kv_head = int16_t(h);
-        if (!split || w.seg_hi == w.seg_lo) {
-          p.items[o++] = w;
-          continue;
-        }
-        int64_t base[kMaxTilesPerUnit] = {0, 0};
-        for (int t = 0; t < p.tiles_per_unit; ++t) {
-          if (!(w.flags / kSlotPresent >> t & 1)) continue;
-          MergeUnit m;
-          m.q_tok0 = w.q_tok0;
-          m.q_lo = w.q_lo;
-          m.tile = w.tile + t;
-          m.part_base = int32_t(part);
-          m.rows = u.rows[t];
-          m.kv_head = int16_t(h);
-          m.nseg = int16_t(w.nseg[t] - w.seg_lo);  // partials of segments seg_lo .. nseg - 1
-          m.pad[0] = m.pad[1] = 0;
-          p.merges[mo++] = m;
-          base[t] = part;
-          part += int64_t(w.nseg[t] - w.seg_lo) * u.rows[t];
-        }
-        for (int sg = w.seg_lo; sg <= w.seg_hi; ++sg) {
-          WorkItem ws = w;
-          ws.seg_lo = ws.seg_hi = int16_t(sg);
-          ws.flags = int16_t(w.flags | kItemSplit);
-          for (int t = 0; t < p.tiles_per_unit; ++t)
-            ws.part_base[t] = int32_t(base[t] + int64_t(sg - w.seg_lo) * u.rows[t]);
-          p.items[o++] = ws;
-        }
+  if (p.batch <= kPairRequests) {
+    // each request's offsets, then one (request, kv head) pair per thread:
+    // head h of request r starts h shares into the request's range
+    for (int r = r0; r < r1; ++r) {
+      ReqGeom g;
+      request_geom(p, r, g);
+      int64_t it = 0, pr = 0, mg = 0;
+      for (int gi = 0; gi < g.groups; ++gi) {
+        if (split) split_counts(p, unit_geom(p, r, g, gi), it, pr, mg);
+        else it += 1;
       }
+      s_item[r] = int32_t(o);
+      s_part[r] = part;
+      s_merge[r] = int32_t(mo);
+      o += it * p.num_kv_heads;
+      part += pr * p.num_kv_heads;
+      mo += mg * p.num_kv_heads;
+    }
+    __syncthreads();
+    for (int i = tid; i < p.batch * p.num_kv_heads; i += kPlanThreads) {
+      const int r = i / p.num_kv_heads, h = i - r * p.num_kv_heads;
+      ReqGeom g;
+      request_geom(p, r, g);
+      if (g.groups == 0) continue;
+      // this head's share of the request's items, partial rows and merges
+      int64_t it = 0, pr = 0, mg = 0;
+      for (int gi = 0; gi < g.groups; ++gi) {
+        if (split) split_counts(p, unit_geom(p, r, g, gi), it, pr, mg);
+        else it += 1;
+      }
+      int64_t oi = s_item[r] + int64_t(h) * it, pi = s_part[r] + int64_t(h) * pr, mi = s_merge[r] + int64_t(h) * mg;
+      for (int gi = g.groups - 1; gi >= 0; --gi) write_unit(p, r, g, gi, h, split, oi, pi, mi);
+    }
+  } else {
+    for (int r = r0; r < r1; ++r) {
+      ReqGeom g;
+      request_geom(p, r, g);
+      for (int h = 0; h < p.num_kv_heads; ++h)
+        for (int gi = g.groups - 1; gi >= 0; --gi) write_unit(p, r, g, gi, h, split, o, part, mo);
     }
   }
   __syncthreads();
