@@ -62,7 +62,7 @@ typedef enum bip_status {
 
 typedef enum bip_kv_dtype {
   BIP_KV_BF16 = 0,
-  BIP_KV_FP8_E4M3 = 1 /* OCP E4M3 pages, dequantised to bf16 in the kernel */
+  BIP_KV_FP8_E4M3 = 1 /* OCP E4M3 pages, decoded to f16 operands in the kernel */
 } bip_kv_dtype;
 
 /* How multi-segment units are scheduled.  Numerically neutral: every policy
@@ -177,8 +177,9 @@ bip_status bip_plan_destroy(bip_plan_t plan);
  * must be a multiple of 16 bytes (and, for page sizes below 8, below 2^31
  * bytes, else BIP_ERR_UNSUPPORTED).  k_scale multiplies the logits (folded
  * into the softmax scale) and v_scale the output; use 1.0 for bf16 pages.
- * Page slots at or beyond a request's kv_len may hold anything (NaN too).
- * Calls sharing one workspace must be ordered on the GPU. */
+ * Both must be finite, else BIP_ERR_INVALID_ARG.  Page slots at or beyond a
+ * request's kv_len may hold anything (NaN too).  Calls sharing one workspace
+ * must be ordered on the GPU. */
 bip_status bip_prefill(bip_plan_t plan, const void* q, int64_t num_q_rows, const void* k_pages,
                        const void* v_pages, int64_t num_pages, int64_t page_stride_elems,
                        const int32_t* kv_indices, float k_scale, float v_scale, void* out,

@@ -14,7 +14,7 @@
 //                   writes the segment.
 //   (FP8 pages)     dequant warpgroups (two at head_dim 128 with whole
 //                   pages, on alternate blocks) convert staged E4M3 blocks
-//                   to bf16.
+//                   to f16.
 //   (token pages)   row-gather warps copy K and V rows with cp.async (bf16:
 //                   two warpgroups; FP8: one).
 //   control         warp 0: q tiles and K blocks by TMA through an ST-deep
@@ -48,7 +48,6 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -960,12 +959,20 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
   }
 }
 
-// Two E4M3 codes (low byte first) -> two f16 (low half first), one
-// conversion instruction.  Exact: every E4M3 value, subnormals included, is
-// an f16 normal number (or zero); the NaN codes give NaN.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return uint32_t(h.x) | (uint32_t(h.y) << 16);
+// Four E4M3 codes (the bytes of w, lowest first) -> four f16 (two pairs,
+// lo: bytes 0 and 1, hi: bytes 2 and 3, low half first), one conversion
+// instruction per pair, each reading a 16-bit half of w's register in place
+// (no shift or mask to isolate the pair: measured 6-23 % faster kernels than
+// the same conversions on separately extracted halves).  Exact: every E4M3
+// value, subnormals included, is an f16 normal number or zero; the NaN codes
+// give NaN.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 c01, c23;\n\t"
+      "mov.b32 {c01, c23}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c01;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, c23;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // FP8 pages: the q tile (bf16, 128-byte swizzled rows of 64-column chunks)
@@ -1097,10 +1104,7 @@ __device__ void dequant_role(const Ctx& c, uint32_t sbase, const AttnParams& p, 
             const int r = r0 + k * RSTEP;
             uint32_t o[4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              o[2 * j] = e4m3x2_to_f16x2(raw[k][j]);
-              o[2 * j + 1] = e4m3x2_to_f16x2(raw[k][j] >> 16);
-            }
+            for (int j = 0; j < 2; ++j) e4m3x4_to_f16x4(raw[k][j], o[2 * j], o[2 * j + 1]);
             if (which == 1 && r >= valid_rows) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) o[j] = 0u;

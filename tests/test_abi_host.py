@@ -100,6 +100,11 @@ def test_prefill_rejects_before_touching_memory(lib):
     rc = lib.bip_prefill(tok._h, fake, 3, fake, fake, 1, 1 << 30, fake, 1.0, 1.0, fake, fake, fake,
                          tok.workspace_bytes, None)
     assert rc == 2
+    # scales must be finite
+    for ks, vs in ((float("inf"), 1.0), (1.0, float("nan"))):
+        rc = lib.bip_prefill(plan._h, fake, 3, fake, fake, 1, 16 * 8 * 128, fake, ks, vs, fake, fake, fake,
+                             plan.workspace_bytes, None)
+        assert rc == 1
     # a plan with only q_len = 0 requests has nothing to run
     empty = bip.Plan([0, 0], [0, 1], [5], num_qo_heads=32, num_kv_heads=8, head_dim=128)
     assert lib.bip_prefill(empty._h, None, 0, None, None, 0, 0, None, 1.0, 1.0, None, None, None, 0, None) == 0

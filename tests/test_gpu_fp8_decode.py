@@ -5,6 +5,8 @@ is the decoded V row (v_scale 1, exact in bf16), and with a one-hot q row the
 lse is the selected K entry times 1/sqrt(d).  Every finite E4M3 code, the
 subnormals and both zeros included, is placed in V and probed in K; the
 expected values come from the oracle's decoder (the OCP E4M3 definition).
+Both head dims run (their kernels convert with different dequant warpgroup
+layouts).
 """
 
 import math
@@ -20,12 +22,13 @@ from gpu_helpers import run_gpu
 
 pytestmark = pytest.mark.gpu
 
-HQ, HKV, D = 32, 8, 128
+HEADS = [W.HEADS_A, W.HEADS_B]  # (num_qo_heads, num_kv_heads, head_dim)
 CODES = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)  # 254 finite codes
 
 
-def _one_key_batch(k_codes: np.ndarray, v_codes: np.ndarray, q: torch.Tensor) -> W.PagedBatch:
+def _one_key_batch(k_codes: np.ndarray, v_codes: np.ndarray, q: torch.Tensor, heads) -> W.PagedBatch:
     """len(q) requests, each one key (one page of 16 slots, slot 0 used)."""
+    HQ, HKV, D = heads
     n = q.shape[0]
     k_pages = torch.full((n, 16, HKV, D), 0x7F, dtype=torch.uint8)  # unused slots: NaN codes
     v_pages = torch.full((n, 16, HKV, D), 0x7F, dtype=torch.uint8)
@@ -39,14 +42,16 @@ def _one_key_batch(k_codes: np.ndarray, v_codes: np.ndarray, q: torch.Tensor) ->
                         q_lens=[1] * n, kv_lens=[1] * n)
 
 
-def test_v_codes_decode_exactly(cuda):
+@pytest.mark.parametrize("heads", HEADS, ids=lambda h: f"d{h[2]}")
+def test_v_codes_decode_exactly(cuda, heads):
     # request r's V row holds every finite code (tiled); out row r = decoded V row
+    HQ, HKV, D = heads
     n = 4
     rng = np.random.default_rng(0)
     v = np.stack([rng.permutation(np.resize(CODES, HKV * D)).reshape(HKV, D) for _ in range(n)]).astype(np.uint8)
     k = np.zeros((n, HKV, D), dtype=np.uint8)
     q = torch.randn(n, HQ, D, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
-    b = _one_key_batch(k, v, q)
+    b = _one_key_batch(k, v, q, heads)
     out, lse, _ = run_gpu(b, cuda)
     # the kernel's pages are indexed through kv_indices (reversed): request r reads page n - 1 - r
     want = e4m3_bits_to_f64(v[::-1].copy())                                    # [n, Hkv, D]
@@ -56,8 +61,10 @@ def test_v_codes_decode_exactly(cuda):
     assert torch.equal(lse, torch.zeros_like(lse))  # all-zero keys: one weight of exactly 1
 
 
-def test_k_codes_decode_exactly(cuda):
+@pytest.mark.parametrize("heads", HEADS, ids=lambda h: f"d{h[2]}")
+def test_k_codes_decode_exactly(cuda, heads):
     # every q head is one-hot on its own column: lse = k[kv head, column] / sqrt(d)
+    HQ, HKV, D = heads
     n = math.ceil(len(CODES) / HQ)
     k = np.zeros((n, HKV, D), dtype=np.uint8)
     q = torch.zeros(n, HQ, D, dtype=torch.bfloat16)
@@ -69,9 +76,24 @@ def test_k_codes_decode_exactly(cuda):
         q[r, h, col] = 1.0
         probes.append((r, h, code))
     v = np.zeros((n, HKV, D), dtype=np.uint8)
-    b = _one_key_batch(k, v, q)  # the 4 q heads of a kv head probe 4 different columns
+    b = _one_key_batch(k, v, q, heads)  # the q heads of a kv head probe 4 different columns
     out, lse, _ = run_gpu(b, cuda)
     for r, h, code in probes:
         want = float(e4m3_bits_to_f64(np.array([code], dtype=np.uint8))[0]) / math.sqrt(D)
         got = float(lse[r, h])
         assert abs(got - want) <= 1e-6 * max(1.0, abs(want)), f"code {code:#04x}: lse {got} vs {want}"
+
+
+@pytest.mark.parametrize("heads", HEADS, ids=lambda h: f"d{h[2]}")
+def test_nan_codes_inside_kv_len(cuda, heads):
+    # The NaN codes 0x7F / 0xFF in a V row the softmax weights by exactly 1
+    # give NaN outputs in their columns and touch no other column.
+    HQ, HKV, D = heads
+    v = np.zeros((1, HKV, D), dtype=np.uint8)
+    v[0, :, 0], v[0, :, 1] = 0x7F, 0xFF
+    k = np.zeros((1, HKV, D), dtype=np.uint8)
+    q = torch.randn(1, HQ, D, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    out, _, _ = run_gpu(_one_key_batch(k, v, q, heads), cuda)
+    got = out.float()[0]
+    assert torch.isnan(got[:, :2]).all()
+    assert torch.equal(got[:, 2:], torch.zeros_like(got[:, 2:]))
