@@ -146,8 +146,11 @@ bip_status bip_plan_get_info(bip_plan_t plan, bip_plan_info* info);
 
 /* Work items in launch order, 8 int32 each:
  *   request, kv_head, q_tile, seg_lo, seg_hi, split (0/1), kv_blocks, tile_mask
- * The item carries absolute tiles q_tile + t for every bit t of tile_mask;
- * tile u covers sequence positions [u * tile_positions, (u + 1) * tile_positions).
+ * The item carries tiles q_tile + t for every bit t of tile_mask; tile u of
+ * a request covers sequence positions kv_len - q_len + [u * tile_positions,
+ * (u + 1) * tile_positions), clipped at kv_len (tiles count from the
+ * request's first new row, so q_len rows take ceil(q_len / tile_positions)
+ * tiles).
  * Writes at most capacity items; *count receives the total. */
 bip_status bip_plan_get_items(bip_plan_t plan, int32_t* items, int32_t capacity, int32_t* count);
 

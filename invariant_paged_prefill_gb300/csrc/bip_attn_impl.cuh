@@ -5,8 +5,8 @@
 // bip_attn_gather.cu those that gather token rows (page sizes below 8).
 //
 // One CTA (one per SM) walks work items: a unit = (request, KV head, NT
-// consecutive absolute q tiles that share the same keys) over some of its
-// 4096-key segments.  Roles, whole warpgroups each:
+// consecutive q tiles that share the same keys; tiles are counted from the
+// request's first new row) over some of its 4096-key segments.  Roles, whole warpgroups each:
 //   softmax warps   one warpgroup per q tile slot t: thread i owns packed
 //                   row i (TMEM lane i); masks, keeps the row's running max
 //                   and sum, writes P_t (bf16) over S_t in TMEM, rescales
@@ -237,9 +237,9 @@ __device__ __forceinline__ Geom geom_of(const WorkItem& w, int T) {
   int unit_end = 0;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    g.tile_start[t] = (w.tile + t) * T;
+    g.tile_start[t] = w.q_lo + (w.tile + t) * T;  // tiles count from the request's first new row
     g.tile_end[t] = min(g.tile_start[t] + T - 1, w.kv_len - 1);
-    g.first_valid[t] = max(g.tile_start[t], w.q_lo);
+    g.first_valid[t] = g.tile_start[t];
     if (g.mask >> t & 1) {
       g.last_slot = t;
       unit_end = g.tile_end[t];

@@ -4,9 +4,9 @@
 // The schedule never looks at batch statistics (the failure of the prior
 // art: a tile chosen from avg_packed_qo_len, sglang PR 46351 "Root cause").
 // Every unit's geometry is a function of its own request's lengths only:
-// q tiles are T = floor(128 / group) positions aligned at absolute multiples
-// of T, and keys are cut at absolute multiples of the block and segment
-// lengths.  Batch composition, policy and SM count only decide which CTA
+// q tiles are T = floor(128 / group) consecutive positions counted from the
+// request's first new row, and keys are cut at absolute multiples of the
+// block and segment lengths.  Batch composition, policy and SM count only decide which CTA
 // runs a unit and whether its segments are folded or split, which does not
 // change any row's arithmetic.
 
@@ -36,7 +36,7 @@ constexpr size_t kDefaultSplitBudget = size_t(256) << 20;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct UnitDesc {
-  int32_t request, kv_head, tile;  // tile = absolute tile of slot 0
+  int32_t request, kv_head, tile;  // tile of slot 0, counted from the request's first new row
   int32_t mask;                    // slots present
   int32_t rows[bip::kMaxTilesPerUnit], nseg[bip::kMaxTilesPerUnit];  // nseg: segments 0 .. tile_end / L
   int32_t blk_min, seg_lo, seg_hi;  // first block, first and last segment the unit visits
@@ -161,8 +161,8 @@ extern "C" size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, in
   if (max_batch < 0 || max_total_q < 0 || check_heads(num_qo_heads, num_kv_heads, head_dim) != BIP_OK) return 0;
   const int64_t group = num_qo_heads / num_kv_heads;
   const int64_t T = bip::kTileRows / group;
-  // A request with q_len rows touches at most ceil(q_len / T) + 1 tiles, so
-  // at most that many units (a unit holds one or two tiles).
+  // A request with q_len rows has ceil(q_len / T) tiles, so at most that
+  // many units (a unit holds one or two tiles); the bound allows one more.
   const int64_t units = int64_t(num_kv_heads) * ((int64_t(max_total_q) + T - 1) / T + 2 * int64_t(max_batch));
   // Each extra split item needs at least `group` partial rows of budget.
   const int64_t extra = int64_t(split_budget_bytes / (size_t(group) * partial_row_bytes(head_dim)));
@@ -238,18 +238,22 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     for (int32_t r = 0; r < batch; ++r) {
       if (q_len[r] == 0) continue;
       ++active;
-      tiles += (kv_len[r] - 1) / T - (kv_len[r] - q_len[r]) / T + 1;
+      tiles += (q_len[r] - 1) / T + 1;
     }
     NT = (bip::max_tiles_per_unit_for(head_dim) >= 2 && page_size >= 8 && tiles >= 2 * active) ? 2 : 1;
   }
 
-  // ---- units: (request, kv head, NT consecutive absolute q tiles sharing keys)
+  // ---- units: (request, kv head, NT consecutive q tiles sharing keys).
+  // Tile k of a request holds its new rows at positions q_lo + k T ..
+  // q_lo + k T + T - 1: a row's arithmetic does not depend on which rows
+  // share its tile, so tiles start at the first new row, and an extend of
+  // q_len rows needs ceil(q_len / T) tiles wherever its rows fall.
   std::vector<UnitDesc> units;
   for (int32_t r = 0; r < batch; ++r) {
     if (q_len[r] == 0) continue;
     const int32_t q_lo = kv_len[r] - q_len[r];
-    const int32_t t0 = q_lo / T, t1 = (kv_len[r] - 1) / T;
-    for (int32_t g0 = (t0 / NT) * NT; g0 <= t1; g0 += NT) {
+    const int32_t t1 = (q_len[r] - 1) / T;
+    for (int32_t g0 = 0; g0 <= t1; g0 += NT) {
       UnitDesc u;
       u.request = r;
       u.tile = g0;
@@ -259,9 +263,9 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
         const int32_t tile = g0 + t;
         u.rows[t] = 0;
         u.nseg[t] = 0;
-        if (tile < t0 || tile > t1) continue;
-        const int32_t tile_end = std::min(tile * T + T - 1, kv_len[r] - 1);
-        const int32_t first_valid = std::max(tile * T, q_lo);
+        if (tile > t1) continue;
+        const int32_t first_valid = q_lo + tile * T;
+        const int32_t tile_end = std::min(first_valid + T - 1, kv_len[r] - 1);
         u.mask |= 1 << t;
         u.rows[t] = (tile_end - first_valid + 1) * group;
         u.nseg[t] = tile_end / bip::kSplitLen + 1;
@@ -846,7 +850,7 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
     const uint64_t ns = opts.wait_limit_ns, khz = query_clock_khz();
     p->wait_limit_cycles = ns > (~0ull / khz) ? ~0ull : std::max<uint64_t>(1, ns * khz / 1000000ull);
   }
-  // A request with q_len rows touches at most ceil(q_len / T) + 1 tiles.
+  // A request with q_len rows has ceil(q_len / T) tiles (the bound allows one more).
   const int64_t cap = int64_t(num_kv_heads) * ((int64_t(max_total_q) + p->T - 1) / p->T + 2 * int64_t(max_batch));
   if (cap > INT32_MAX) {
     delete p;

@@ -30,14 +30,14 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == kHeaderBytes, "header size");
 
-// One attention work item: a unit (request x KV head x up to two absolute q
-// tiles that share the same keys) over a range of its segments.  48 bytes.
+// One attention work item: a unit (request x KV head x up to two q tiles
+// that share the same keys) over a range of its segments.  48 bytes.
 struct WorkItem {
   int32_t kv_len;
   int32_t page_base;   // first entry of the request in kv_indices
   int32_t q_tok0;      // q row of sequence position 0 (may be negative)
   int32_t q_lo;        // first position that has a q row (kv_len - q_len)
-  int32_t tile;        // absolute tile of slot 0; slot t covers positions [(tile+t)*T, +T)
+  int32_t tile;        // tile of slot 0; slot t covers positions q_lo + (tile+t)*T .. +T-1
   int16_t kv_head;
   int16_t seg_lo;      // inclusive segment range
   int16_t seg_hi;

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kMergeThreads) bip_merge_kernel(const MergePar
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int ui = blockIdx.x; ui < n_units; ui += gridDim.x) {
     const MergeUnit u = p.units[ui];
-    const int first_valid = max(u.tile * p.tile_pos, u.q_lo);
+    const int first_valid = u.q_lo + u.tile * p.tile_pos;  // the tile's first position
     for (int vr = warp; vr < u.rows; vr += W) {
       float o[E][4];
 #pragma unroll

@@ -1,8 +1,8 @@
 // Device-side planner for graph-replayable prefill launches.  One CTA reads
 // the batch's indptr arrays from device memory, validates them, and writes
 // the work list the attention kernel consumes: for every request with new
-// rows, every kv head and every group of tiles_per_unit consecutive absolute
-// q tiles that hold rows of the request, one unit.  When the batch has few
+// rows, every kv head and every group of tiles_per_unit consecutive q tiles
+// of the request (counted from its first new row), one unit.  When the batch has few
 // units (fewer than 8 per CTA of the launch, the host planner's rule) and
 // the capacities allow, every unit with more than one segment is split into
 // one item per segment writing partial states, with one merge unit per q
@@ -29,7 +29,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPairRequests = 1536;
 
 struct ReqGeom {
-  int32_t q_len, kv_len, g0, groups;  // groups of tiles holding rows of the request
+  int32_t q_len, kv_len, groups;  // groups of tiles_per_unit tiles holding the request's new rows
 };
 
 __device__ __forceinline__ bool request_geom(const DevPlanParams& p, int r, ReqGeom& g) {
@@ -37,7 +37,6 @@ __device__ __forceinline__ bool request_geom(const DevPlanParams& p, int r, ReqG
   const int64_t np = int64_t(p.kv_indptr[r + 1]) - p.kv_indptr[r];
   g.q_len = 0;
   g.kv_len = 0;
-  g.g0 = 0;
   g.groups = 0;
   if (ql < 0 || np < 0) return false;
   int64_t kl = 0;
@@ -51,11 +50,7 @@ __device__ __forceinline__ bool request_geom(const DevPlanParams& p, int r, ReqG
   if (p.mask_row_words > 0 && ql > 0 && kl > 32 * p.mask_row_words) return false;
   g.q_len = int32_t(ql);
   g.kv_len = int32_t(kl);
-  if (ql > 0) {
-    const int32_t t0 = (g.kv_len - g.q_len) / p.tile_pos, t1 = (g.kv_len - 1) / p.tile_pos;
-    g.g0 = (t0 / p.tiles_per_unit) * p.tiles_per_unit;
-    g.groups = (t1 - g.g0) / p.tiles_per_unit + 1;
-  }
+  if (ql > 0) g.groups = ((g.q_len - 1) / p.tile_pos) / p.tiles_per_unit + 1;
   return true;
 }
 
@@ -69,22 +64,22 @@ struct UnitGeom {
 __device__ __forceinline__ UnitGeom unit_geom(const DevPlanParams& p, int r, const ReqGeom& g, int gi) {
   UnitGeom u;
   const int32_t q_lo = g.kv_len - g.q_len;
-  const int32_t t0 = q_lo / p.tile_pos, t1 = (g.kv_len - 1) / p.tile_pos;
+  const int32_t t1 = (g.q_len - 1) / p.tile_pos;  // tile k: positions q_lo + k tile_pos ..
   WorkItem& w = u.w;
   w.kv_len = g.kv_len;
   w.page_base = p.kv_indptr[r];
   w.q_tok0 = p.qo_indptr[r] - q_lo;
   w.q_lo = q_lo;
-  w.tile = g.g0 + gi * p.tiles_per_unit;
+  w.tile = gi * p.tiles_per_unit;
   w.kv_head = 0;
   int mask = 0, unit_end = -1, unit_first = INT_MAX;
   w.nseg[0] = w.nseg[1] = 0;
   u.rows[0] = u.rows[1] = 0;
   for (int t = 0; t < p.tiles_per_unit; ++t) {
     const int32_t tile = w.tile + t;
-    if (tile < t0 || tile > t1) continue;
-    const int32_t tile_end = min(tile * p.tile_pos + p.tile_pos - 1, g.kv_len - 1);
-    const int32_t first = max(tile * p.tile_pos, q_lo);
+    if (tile > t1) continue;
+    const int32_t first = q_lo + tile * p.tile_pos;
+    const int32_t tile_end = min(first + p.tile_pos - 1, g.kv_len - 1);
     mask |= 1 << t;
     w.nseg[t] = int16_t(tile_end / kSplitLen + 1);
     u.rows[t] = (tile_end - first + 1) * p.group;

@@ -264,7 +264,7 @@ def test_large_head_workspace_is_small():
 
 
 def unit_geometry(plan, request):
-    """(kv_head, absolute q tile) pairs and item geometry of one request."""
+    """(kv_head, q tile) pairs and item geometry of one request."""
     it = plan.items()
     mine = it[it[:, 0] == request]
     tiles = {(int(r[1]), int(r[2]) + t) for r in mine for t in range(2) if r[7] >> t & 1}
@@ -284,11 +284,11 @@ def test_schedule_of_a_request_does_not_depend_on_its_batch_mates(lib):
             t_units, t_items = unit_geometry(together, r)
             a_units, a_items = unit_geometry(alone, 0)
             assert t_units == a_units and t_items == a_items
-            # the tiles are the absolute ones: tile t covers positions [32 t, 32 t + 32)
-            kv_len = (np_ - 1) * 16 + last[r] if np_ else 0
+            # tiles count from the request's first new row: tile t covers
+            # positions kv_len - ql + [32 t, 32 t + 32), ceil(ql / 32) tiles
             if ql:
                 tiles = sorted({t for _, t in a_units})
-                assert tiles == list(range((kv_len - ql) // 32, (kv_len - 1) // 32 + 1))
+                assert tiles == list(range((ql + 31) // 32))
 
 
 def test_split_policies_cover_the_same_units():
