@@ -6,7 +6,8 @@
 //
 // One CTA (one per SM) walks work items: a unit = (request, KV head, NT
 // consecutive q tiles that share the same keys; tiles are counted from the
-// request's first new row) over some of its 4096-key segments.  Roles, whole warpgroups each:
+// request's first new row) over some of its 4096-key segments.  Roles,
+// whole warpgroups each:
 //   softmax warps   one warpgroup per q tile slot t: thread i owns packed
 //                   row i (TMEM lane i); masks, keeps the row's running max
 //                   and sum, writes P_t (bf16) over S_t in TMEM, rescales

@@ -101,14 +101,19 @@ __device__ __forceinline__ float out_scale(float l, float v_scale) { return __fm
 
 __device__ __forceinline__ float final_lse(float m, float l) { return __fmul_rn(__fadd_rn(m, lg2(l)), kLn2); }
 
+// Two fp32 -> a bf16 (or f16) pair, each rounded to nearest even, lo in
+// the low half: one conversion instruction (the second source lands in
+// the low half).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 }  // namespace bip
