@@ -40,9 +40,12 @@ class _Bar:
         return (self.phase & 1) != parity
 
 
-def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
+def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1, HP=False):
     """items: list of (nb, mask); SS > 0 models FP8 staging + dequant (DQ
-    dequant warpgroups taking alternate blocks); GW > 0
+    dequant warpgroups taking alternate blocks); HP models the early first
+    half of P (P_HALF: the issuer starts the PV of the first 64 keys, then
+    waits P_FULL for the rest; a warp that rescales O publishes its half only
+    at the end of the block); GW > 0
     models token-granular pages: GW row-gather warps per stream, whose 32
     lanes each arrive on the landing barrier when their own copies land,
     and a q/K producer that loads q tiles only."""
@@ -62,6 +65,7 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
     for t in range(NT):
         for s in range(NS):
             bar(f"S_FULL{t}{s}"), bar(f"P_FULL{t}{s}", 32 * warps), bar(f"O_DONE{t}{s}")
+            bar(f"P_HALF{t}{s}", 32 * warps)
     bar("Q_FULL"), bar("Q_FREE"), bar("V_TX")
     bar("Q_READY", 128), bar("QS_FREE", 32 * warps * NT)  # FP8: q tile converted / its row scales read
     clock, pending, last_mma = [0], [], [0]
@@ -193,10 +197,12 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
                 for t in range(NT):
                     if not mask >> t & 1:
                         continue
-                    yield wait(f"P_FULL{t}{pv_cnt[t] % NS}", pv_cnt[t] // NS)
+                    yield wait(f"{'P_HALF' if HP else 'P_FULL'}{t}{pv_cnt[t] % NS}", pv_cnt[t] // NS)
                     if not vready:
                         yield wait(f"V_FULL{vb % ST}", vb // ST)
                         vready = True
+                    if HP:  # the first 64 keys' PV is queued; the rest needs all of P
+                        yield wait(f"P_FULL{t}{pv_cnt[t] % NS}", pv_cnt[t] // NS)
                     commit(f"O_DONE{t}{pv_cnt[t] % NS}")
                     pv_cnt[t] += 1
                     if j + NS < nb:
@@ -223,8 +229,16 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
                 continue
             for blk in range(nb):
                 yield wait(f"S_FULL{t}{cnt % NS}", cnt // NS)
-                if blk > 0 and NS == 2 and rnd.random() < 0.3:   # a row's max moved: rescale O
+                rescale = blk > 0 and rnd.random() < 0.3            # a row's max moved: rescale O
+                if HP and not rescale:                               # first half of P out early
+                    for _ in range(32):
+                        B[f"P_HALF{t}{cnt % NS}"].arrive()
+                    yield None
+                if rescale and NS == 2:
                     yield from wait_pv(cnt - 1)
+                if HP and rescale:
+                    for _ in range(32):
+                        B[f"P_HALF{t}{cnt % NS}"].arrive()
                 for _ in range(32):
                     B[f"P_FULL{t}{cnt % NS}"].arrive()
                 cnt += 1
@@ -272,23 +286,23 @@ def _simulate(NT, NS, ST, SS, items, seed, warps=4, GW=0, DQ=1):
 
 
 VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, GW gather warps per stream,
-    #           DQ dequant warpgroups)
-    "d128_two_tiles": (2, 1, 2, 0, 0, 1),
-    "d128_one_tile": (1, 2, 3, 0, 0, 1),
-    "d256": (1, 2, 2, 0, 0, 1),
-    "d128_fp8": (1, 2, 2, 2, 0, 2),
-    "d128_fp8_two_tiles": (2, 1, 2, 1, 0, 1),
-    "d256_fp8": (1, 2, 2, 1, 0, 1),
-    "d128_rows": (1, 2, 3, 0, 4, 1),
-    "d256_rows": (1, 2, 2, 0, 4, 1),
-    "d128_fp8_rows": (1, 2, 2, 2, 2, 1),
-    "d256_fp8_rows": (1, 2, 2, 1, 2, 1),
+    #           DQ dequant warpgroups, HP early half of P: FP8 pages with 128-key blocks)
+    "d128_two_tiles": (2, 1, 2, 0, 0, 1, False),
+    "d128_one_tile": (1, 2, 3, 0, 0, 1, False),
+    "d256": (1, 2, 2, 0, 0, 1, False),
+    "d128_fp8": (1, 2, 2, 2, 0, 2, True),
+    "d128_fp8_two_tiles": (2, 1, 2, 1, 0, 1, True),
+    "d256_fp8": (1, 2, 2, 1, 0, 1, False),
+    "d128_rows": (1, 2, 3, 0, 4, 1, False),
+    "d256_rows": (1, 2, 2, 0, 4, 1, False),
+    "d128_fp8_rows": (1, 2, 2, 2, 2, 1, True),
+    "d256_fp8_rows": (1, 2, 2, 1, 2, 1, False),
 }
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 def test_schedule_never_deadlocks_or_aliases(variant):
-    NT, NS, ST, SS, GW, DQ = VARIANTS[variant]
+    NT, NS, ST, SS, GW, DQ, HP = VARIANTS[variant]
     full = (1 << NT) - 1
     item_sets = [[(1, full)], [(9, full)], [(4, full), (1, full), (17, full)], [(3, 1), (2, full), (5, 1)],
                  [(6, full), (1, full), (1, full), (2, full), (1, full), (5, full)]]  # short items run ahead
@@ -296,4 +310,4 @@ def test_schedule_never_deadlocks_or_aliases(variant):
         item_sets.append([(6, 2), (2, 1), (7, 3)])
     for items in item_sets:
         for seed in range(60 if not GW else 25):
-            _simulate(NT, NS, ST, SS, items, seed, GW=GW, DQ=DQ)
+            _simulate(NT, NS, ST, SS, items, seed, GW=GW, DQ=DQ, HP=HP)
