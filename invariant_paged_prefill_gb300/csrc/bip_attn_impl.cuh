@@ -13,8 +13,8 @@
 //                   and sum, writes P_t (bf16) over S_t in TMEM, rescales
 //                   O_t when needed, and at each segment end folds or
 //                   writes the segment.
-//   (FP8 pages)     dequant warpgroups (two at head_dim 128 with whole
-//                   pages, on alternate blocks) convert staged E4M3 blocks
+//   (FP8 pages)     dequant warpgroups (two with one q-tile slot and whole
+//                   pages, one per K/V stream) convert staged E4M3 blocks
 //                   to f16.
 //   (token pages)   row-gather warps copy K and V rows with cp.async (bf16:
 //                   two warpgroups; FP8: one).
@@ -108,10 +108,11 @@ struct Cfg {
   // other every V block, so a K stage is released as soon as its codes are
   // in registers even while a V block waits for its ring slot; each walks
   // its stream's stages and slots in order, so its parity waits never run
-  // two phases ahead of a barrier.  One warpgroup converts both (d = 256,
-  // and next to the row-gather warpgroup).  Two give up registers
-  // (setmaxnreg); one keeps its launch count.
-  static constexpr int DQ_WGS = KV8 ? ((D == 128 && NT == 1 && !GATHER) ? 2 : 1) : 0;
+  // two phases ahead of a barrier (at head_dim 256 each stream has one
+  // staging stage).  One warpgroup converts both next to the row-gather
+  // warpgroup.  Two give up registers (setmaxnreg); one keeps its launch
+  // count.
+  static constexpr int DQ_WGS = KV8 ? ((NT == 1 && !GATHER) ? 2 : 1) : 0;
   static constexpr int DQ_REGS = 80;
   static constexpr int GA_WARP0 = SM_WARPS + 4 * DQ_WGS;
   static constexpr int GA_WARPS = GATHER ? (KV8 ? 4 : 8) : 0;

@@ -292,7 +292,7 @@ VARIANTS = {  # (NT slots, NS S buffers, ST ring stages, SS FP8 staging stages, 
     "d256": (1, 2, 2, 0, 0, 1, False),
     "d128_fp8": (1, 2, 2, 2, 0, 2, True),
     "d128_fp8_two_tiles": (2, 1, 2, 1, 0, 1, True),
-    "d256_fp8": (1, 2, 2, 1, 0, 1, False),
+    "d256_fp8": (1, 2, 2, 1, 0, 2, False),
     "d128_rows": (1, 2, 3, 0, 4, 1, False),
     "d256_rows": (1, 2, 2, 0, 4, 1, False),
     "d128_fp8_rows": (1, 2, 2, 2, 2, 1, True),
