@@ -113,7 +113,7 @@ struct Cfg {
   // warpgroup.  Two give up registers (setmaxnreg); one keeps its launch
   // count.
   static constexpr int DQ_WGS = KV8 ? ((NT == 1 && !GATHER) ? 2 : 1) : 0;
-  static constexpr int DQ_REGS = 80;
+  static constexpr int DQ_REGS = D == 256 ? 104 : 80;  // head_dim 256: its q-tile conversion spilled at 80
   static constexpr int GA_WARP0 = SM_WARPS + 4 * DQ_WGS;
   static constexpr int GA_WARPS = GATHER ? (KV8 ? 4 : 8) : 0;
   static constexpr int GW = GATHER ? (KV8 ? 2 : 4) : 0;  // gather warps per stream (K or V)
