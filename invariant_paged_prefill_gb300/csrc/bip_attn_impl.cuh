@@ -18,12 +18,12 @@
 //                   to f16.
 //   (token pages)   row-gather warps copy K and V rows with cp.async (bf16:
 //                   two warpgroups; FP8: one).
-//   control         warp 0: q tiles and K blocks by TMA through an ST-deep
-//                   ring (q only when rows are gathered); warp 1: the
-//                   tcgen05 issuer, S_t = Q_t K^T into TMEM, then
-//                   O_t += P_t V with P_t read from TMEM; warp 2: V blocks
-//                   by TMA (its own ring), zeroing V rows past kv_len
-//                   before they enter a product; warp 3: spare.
+//   control         warp 0: spare; warp 1: the tcgen05 issuer,
+//                   S_t = Q_t K^T into TMEM, then O_t += P_t V with P_t read
+//                   from TMEM; warp 2: V blocks by TMA (its own ring),
+//                   zeroing V rows past kv_len before they enter a product;
+//                   warp 3: q tiles and K blocks by TMA through an ST-deep
+//                   ring (q only when rows are gathered).
 // With two slots (head_dim 128) the softmax of one tile overlaps the MMAs of
 // the other.  Slots, ring depth and the way pages are fetched only decide
 // scheduling; every row's arithmetic is the same in every variant.
@@ -100,8 +100,8 @@ struct Cfg {
   // t = warp / 4, TMEM lane quarter = warp % 4), then the FP8 dequant
   // warpgroups, then (GATHER) the row-gather warps, half for K and half for
   // V (bf16: two warpgroups; FP8: one, next to a single dequant warpgroup),
-  // then the control warpgroup: q/K producer, MMA issuer, V producer and
-  // one spare warp.
+  // then the control warpgroup: a spare warp, the MMA issuer, the V
+  // producer and the q/K producer.
   static constexpr int SM_WARPS = 4 * NT;
   static constexpr int DQ_WARP0 = SM_WARPS;
   // FP8 dequant warpgroups.  With two, one converts every K block and the
@@ -1274,8 +1274,12 @@ __global__ void __launch_bounds__(Cfg<D, NT, ST, KV8, GATHER>::THREADS, 1)
     }
   } else {
     if constexpr (C::SPLIT_REGS) reg_dealloc<C::CTL_REGS>();
+    // Warp w runs on the scheduler w % 4.  The q/K producer takes the
+    // control group's last warp and the spare its first, so that the
+    // scheduler of softmax warp 0 (the rows of a short extend, which sit at
+    // the start of their tile) has one busy warp fewer.
     const int role = warp - C::CTL_WARP0;
-    if (role == 0) {
+    if (role == 3) {
       if (lane == 0) {
         prefetch_tmap(&tm_q);
         if (!GATHER) prefetch_tmap(&tm_k);
