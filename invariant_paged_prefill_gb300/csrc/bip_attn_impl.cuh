@@ -860,7 +860,25 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           } else {
             tmem_ld_x64(sa, sv);
           }
-          mx = whole ? block_max(std::true_type{}) : block_max(std::false_type{});
+          if constexpr (MK == 2) {
+            // Custom mask: hidden columns become -inf in S itself (written
+            // back to TMEM), so the max and exponential passes run unmasked:
+            // one visibility test per column instead of two.  2^(-inf) is
+            // exactly the zero the masked loops would have substituted.
+            if (!whole) {
+#pragma unroll
+              for (int j = 0; j < C::BN; ++j) sv[j] = seen(j) ? sv[j] : 0xff800000u;
+              if constexpr (C::BN == 128) {
+                tmem_st_x64(sa, sv);
+                tmem_st_x64(sa + 64, sv + 64);
+              } else {
+                tmem_st_x64(sa, sv);
+              }
+            }
+            mx = block_max(std::true_type{});
+          } else {
+            mx = whole ? block_max(std::true_type{}) : block_max(std::false_type{});
+          }
         }
         float alpha = 1.f;
         if (mx != -INFINITY) {
@@ -915,7 +933,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                 hv[j / 2] = KV8 ? pack_f16x2(f2_lo(e), f2_hi(e)) : pack_bf16x2(f2_lo(e), f2_hi(e));
               }
             };
-            if (whole) exp_pass(std::true_type{});
+            if (MK == 2 || whole) exp_pass(std::true_type{});  // custom mask: S already masked
             else exp_pass(std::false_type{});
           } else {
 #pragma unroll
