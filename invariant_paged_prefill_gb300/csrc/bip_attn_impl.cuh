@@ -788,7 +788,7 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           whole = __all_sync(0xffffffffu, !valid || (lim >= C::BN - 1 && (MK == 0 || lo <= 0)));
           live = __any_sync(0xffffffffu, lim >= 0 && (MK == 0 || lo < C::BN));
         }
-        // column j visible (masked loops only)
+        // column j visible (blocks that are not whole)
         auto seen = [&](int j) -> bool {
           if constexpr (MK == 2) return (vis[j >> 5] >> (j & 31)) & 1u;
           else return col_visible<MK>(j, lim, lo, mb);
@@ -805,6 +805,12 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         // eight independent partial maxima over column pairs (max is exact in
         // any order); masked columns enter as -inf.  Whole blocks and masked
         // blocks get separately compiled loops.
+        // Blocks that are not whole: all kernels but the bf16 two-slot kernel
+        // without a custom mask set the hidden columns of S to -inf first
+        // (below) and then run the unmasked loops; that kernel (224 registers
+        // a thread, where the fold measured 1 % slower) keeps masked copies of
+        // the loops.
+        constexpr bool kFold = MK == 2 || KV8 || NT == 1 || NARROW_LD;
         auto block_max = [&](auto whole_c) {
           constexpr bool kWhole = decltype(whole_c)::value;
           float m8[8];
@@ -831,23 +837,17 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
             float m8[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-            auto max_half = [&](int h, auto whole_c) {
-              constexpr bool kWhole = decltype(whole_c)::value;
-#pragma unroll
-              for (int j = 0; j < 64; j += 2) {
-                float a = __uint_as_float(sv[j]), b = __uint_as_float(sv[j + 1]);
-                if (!kWhole) {
-                  a = seen(h * 64 + j) ? a : -INFINITY;
-                  b = seen(h * 64 + j + 1) ? b : -INFINITY;
-                }
-                m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], a, b);
-              }
-            };
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
               tmem_ld_x64(sa + h * 64, *reinterpret_cast<uint32_t(*)[64]>(sv));
-              if (whole) max_half(h, std::true_type{});
-              else max_half(h, std::false_type{});
+              if (!whole) {  // hidden columns become -inf in S itself (see below)
+#pragma unroll
+                for (int j = 0; j < 64; ++j) sv[j] = seen(h * 64 + j) ? sv[j] : 0xff800000u;
+                tmem_st_x64(sa + h * 64, sv);
+              }
+#pragma unroll
+              for (int j = 0; j < 64; j += 2)
+                m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]));
             }
             mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
           }
@@ -860,11 +860,12 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
           } else {
             tmem_ld_x64(sa, sv);
           }
-          if constexpr (MK == 2) {
-            // Custom mask: hidden columns become -inf in S itself (written
-            // back to TMEM), so the max and exponential passes run unmasked:
-            // one visibility test per column instead of two.  2^(-inf) is
-            // exactly the zero the masked loops would have substituted.
+          // A block that is not whole for the warp: hidden columns become
+          // -inf in S itself (written back to TMEM), so the max and
+          // exponential passes run one unmasked loop each: one visibility
+          // test per column instead of two, and no masked copies of the
+          // loops.  2^(-inf) is exactly the zero a masked loop substitutes.
+          if constexpr (kFold) {
             if (!whole) {
 #pragma unroll
               for (int j = 0; j < C::BN; ++j) sv[j] = seen(j) ? sv[j] : 0xff800000u;
@@ -901,9 +902,10 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
         if constexpr (C::HALF_P) rescale = !seg_first && __any_sync(0xffffffffu, valid && alpha != 1.f);
 
         // Probabilities, the row sum and P (bf16 pairs, packed in place)
-        // written back over the S columns already read; 2^x on MUFU.  Masked
-        // columns are computed and then replaced by exact zeros, so a row gets
-        // the same bits through the whole-block and the masked path.
+        // written back over the S columns already read; 2^x on MUFU.  Hidden
+        // columns hold -inf (or, in the masked loops, are computed and then
+        // replaced), so their probabilities are exact zeros, which add
+        // nothing to the row sum: a row gets the same bits either way.
         // Row-sum partials: acc[i] holds columns 2i, 2i + 1 (mod 8), each
         // pair summed with one packed add (four chains, so that the adds do
         // not wait on each other); they are combined pairwise at the end.
@@ -933,8 +935,12 @@ __device__ void softmax_role(const Ctx& c, uint32_t tmem, const AttnParams& p, c
                 hv[j / 2] = KV8 ? pack_f16x2(f2_lo(e), f2_hi(e)) : pack_bf16x2(f2_lo(e), f2_hi(e));
               }
             };
-            if (MK == 2 || whole) exp_pass(std::true_type{});  // custom mask: S already masked
-            else exp_pass(std::false_type{});
+            if constexpr (kFold) {
+              exp_pass(std::true_type{});
+            } else {
+              if (whole) exp_pass(std::true_type{});
+              else exp_pass(std::false_type{});
+            }
           } else {
 #pragma unroll
             for (int k = 0; k < HW / 2; ++k) hv[k] = 0u;
