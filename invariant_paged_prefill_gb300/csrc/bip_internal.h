@@ -168,8 +168,8 @@ struct DevPlanParams {
   const int32_t* qo_indptr;
   const int32_t* kv_indptr;
   const int32_t* kv_last_page_len;
-  WorkItem* items;
-  MergeUnit* merges;
+  WorkItem* items;      // 16-byte aligned
+  MergeUnit* merges;    // 16-byte aligned
   WsHeader* header;
 };
 
