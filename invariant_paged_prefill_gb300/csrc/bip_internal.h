@@ -82,7 +82,7 @@ struct AttnParams {
   uint16_t* out;        // bf16 bits
   float* lse;
   float* partials;      // [rows][head_dim + 4]: m, l, 0, 0, o[head_dim]
-  float* scratch;       // [grid][128][head_dim]
+  float* scratch;       // [grid][tiles per CTA][head_dim / 4][128] float4: fold state, row-fastest
   WsHeader* header;
   float scale_log2;     // log2(e) * k_scale / sqrt(head_dim)
   float v_scale;
