@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 SOURCES = ["bip_host.cpp", "bip_attn.cu", "bip_attn_gather.cu", "bip_attn_mask.cu", "bip_merge.cu", "bip_append.cu",
-           "bip_plan_dev.cu", "bip_upload.cu", "bip_no_alloc.cu"]
+           "bip_plan_dev.cu", "bip_mask_skip.cu", "bip_upload.cu", "bip_no_alloc.cu"]
 HEADERS = ["bip_internal.h", "bip_numerics.cuh", "bip_ptx.cuh", "bip_attn_impl.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 # -fmad=false: no silent contraction of a*b+c in device code; the numerics

@@ -32,6 +32,8 @@ using bip::WorkItem;
 namespace {
 
 constexpr size_t kDefaultSplitBudget = size_t(256) << 20;
+// CTAs of the custom-mask block-skip pass (items by stride).
+constexpr int32_t kMaskSkipCtas = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -687,6 +689,22 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
   set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
   ap.mask = mask;
   ap.mask_row_words = mask ? mask_row_words : 0;
+  if (mask) {
+    // start every item at the first block one of its rows sees
+    bip::MaskSkipParams sp;
+    sp.items = reinterpret_cast<WorkItem*>(ws + p->off_items);
+    sp.n_items = int32_t(p->items.size());
+    sp.n_items_dev = nullptr;
+    sp.mask = mask;
+    sp.mask_row_words = mask_row_words;
+    sp.group = p->group;
+    sp.tile_pos = p->T;
+    sp.kv_block = bip::kv_block_for(p->d);
+    sp.tiles_per_unit = p->nt;
+    sp.window_left = p->opts.window_left;
+    if (bip::launch_mask_skip(sp, std::min<int32_t>(sp.n_items, kMaskSkipCtas), stream) != cudaSuccess)
+      return BIP_ERR_CUDA;
+  }
   const cudaError_t le = mask ? bip::launch_attention_masked(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream)
                               : bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream);
   if (le != cudaSuccess) return BIP_ERR_CUDA;
@@ -963,6 +981,22 @@ static bip_status prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t
   ap.mask = mask;
   ap.mask_row_words = mask ? mask_row_words : 0;
   set_pools(ap, k_pages, v_pages, page_stride_elems * elem, p->hkv * p->d * int32_t(elem));
+  if (mask) {
+    // start every item the planner wrote at the first block one of its rows sees
+    bip::MaskSkipParams sp;
+    sp.items = dp.items;
+    sp.n_items = p->capacity;
+    sp.n_items_dev = &header->n_items;
+    sp.mask = mask;
+    sp.mask_row_words = mask_row_words;
+    sp.group = p->group;
+    sp.tile_pos = p->T;
+    sp.kv_block = bip::kv_block_for(p->d);
+    sp.tiles_per_unit = p->nt;
+    sp.window_left = p->window_left;
+    if (bip::launch_mask_skip(sp, std::min<int32_t>(p->capacity, kMaskSkipCtas), stream) != cudaSuccess)
+      return BIP_ERR_CUDA;
+  }
   const cudaError_t le = mask ? bip::launch_attention_masked(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream)
                               : bip::launch_attention(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream);
   if (le != cudaSuccess) return BIP_ERR_CUDA;

@@ -150,6 +150,21 @@ struct AppendParams {
 // (count in the header), when they fit the capacities; otherwise every unit
 // folds its segments in one CTA.  Validation failures set the header status
 // and leave zero items.
+// Custom masks: the first KV block any row of each work item sees
+// (bip_mask_skip.cu), written into the items before the attention launch.
+struct MaskSkipParams {
+  WorkItem* items;
+  int32_t n_items;
+  const uint32_t* n_items_dev;  // if set, the item count is read here (device-planned launches)
+  const uint32_t* mask;
+  int64_t mask_row_words;
+  int32_t group;
+  int32_t tile_pos;
+  int32_t kv_block;
+  int32_t tiles_per_unit;
+  int32_t window_left;
+};
+
 struct DevPlanParams {
   int32_t batch;
   int32_t max_total_q;   // q rows the buffers hold
@@ -174,7 +189,7 @@ struct DevPlanParams {
 };
 
 // Kernel launchers (bip_attn.cu / bip_attn_gather.cu / bip_attn_mask.cu / bip_merge.cu /
-// bip_append.cu / bip_plan_dev.cu / bip_upload.cu).  launch_attention hands page sizes below
+// bip_append.cu / bip_plan_dev.cu / bip_mask_skip.cu / bip_upload.cu).  launch_attention hands page sizes below
 // 8 to launch_attention_gather.
 cudaError_t launch_attention(int head_dim, int tiles_per_unit, bool kv_fp8, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnParams& p, int grid,
@@ -189,6 +204,7 @@ cudaError_t launch_attention_masked(int head_dim, int tiles_per_unit, bool kv_fp
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int head_dim, bool kv_fp8, const AppendParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_device_plan(const DevPlanParams& p, cudaStream_t stream);
+cudaError_t launch_mask_skip(const MaskSkipParams& p, int grid, cudaStream_t stream);
 // bytes (a multiple of 16) from a device-visible pinned host buffer to the
 // workspace, by SM loads (bip_upload.cu).
 cudaError_t launch_upload(const void* src_dev, void* dst, size_t bytes, cudaStream_t stream);

@@ -151,3 +151,62 @@ def test_mask_rows_too_short_are_rejected(cuda):
         bip.prefill(plan, b.q, b.k_pages, b.v_pages, b.kv_indices, custom_mask=short)
     with pytest.raises(bip.BipError):
         bip.prefill(plan, b.q, b.k_pages, b.v_pages, b.kv_indices, custom_mask=short[:-1, :].contiguous())
+
+
+def _doc_masks(b, seed, lo=300, hi=1500, dead=()):
+    """Per request, its rows of a document mask over the prompt: the prompt is
+    cut into documents of lo..hi tokens and a row sees only its own document's
+    keys.  Requests in `dead` see keys only from the last document on, and the
+    rows before it see nothing (whole items with no visible key)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for r, (n, ql) in enumerate(zip(b.kv_lens, b.q_lens)):
+        doc = np.zeros(n, dtype=np.int64)
+        cut = 0
+        while cut < n:
+            step = int(rng.integers(lo, hi + 1))
+            doc[cut:cut + step] = doc[cut - 1] + 1 if cut else 0
+            cut += step
+        m = doc[:, None] == doc[None, :]
+        if r in dead:
+            m &= doc[None, :] == doc[-1]
+        out.append(m[n - ql:, :n])
+    return out
+
+
+def test_document_masks_skip_blocks_and_keep_the_bits(cuda):
+    # Items start at the first block one of their rows sees: under document
+    # masks most blocks before the diagonal are skipped.  Rows match the
+    # oracle (rows with no visible key: zeros, lse -inf), extend rows equal
+    # full-prefill rows bit for bit, split / fold / tiles per CTA change no
+    # bit, and making key 0 visible to the last row of each request (so that
+    # the items holding it cannot skip) changes no bit of any other row.
+    prompts = [W.make_prompt(n, *W.HEADS_A, seed=140 + i) for i, n in enumerate((6000, 4500, 2100))]
+    full = W.layout(prompts, [p.n for p in prompts], 16, seed_pages=3, poison=True)
+    ext = W.layout(prompts, [700, 33, 2], 16, seed_pages=6, poison=True)
+    fm, em = _doc_masks(full, 5, dead=(1,)), _doc_masks(ext, 5, dead=(1,))
+    fo, fl, _ = run_gpu(full, cuda, custom_mask=fm, policy="never")
+    rows = _rows(full, fm, seed=3)
+    ro, rl = oracle(full, rows=rows, custom_mask=fm)
+    assert _check(fo, fl, ro, rl, rows) > 0
+    eo, el, _ = run_gpu(ext, cuda, custom_mask=em)
+    for r in range(3):
+        f0, e0 = int(full.qo_indptr[r]), int(ext.qo_indptr[r])
+        n, off = ext.q_lens[r], full.q_lens[r] - ext.q_lens[r]
+        assert_bitwise(eo[e0:e0 + n], fo[f0 + off:f0 + off + n], f"request {r} out")
+        assert torch.equal(el[e0:e0 + n], fl[f0 + off:f0 + off + n]), f"request {r} lse"
+    for kw in (dict(policy="always"), dict(policy="auto"), dict(tiles_per_unit=1), dict(tiles_per_unit=2)):
+        o, l, _ = run_gpu(full, cuda, custom_mask=fm, **kw)
+        assert_bitwise(o, fo, f"documents {kw}")
+        assert torch.equal(l, fl), f"documents {kw} lse"
+    opened = [m.copy() for m in fm]
+    moved = []
+    for r, m in enumerate(opened):
+        i = m.shape[0] - 1          # the request's last row
+        m[i, 0] = True
+        moved.append(int(full.qo_indptr[r]) + i)
+    oo, ol, _ = run_gpu(full, cuda, custom_mask=opened, policy="never")
+    keep = torch.ones(fo.shape[0], dtype=torch.bool)
+    keep[moved] = False
+    assert_bitwise(oo[keep], fo[keep], "rows of items that can no longer skip")
+    assert torch.equal(ol[keep], fl[keep])
