@@ -61,7 +61,7 @@ struct bip_plan_s {
   bool need_scratch = false;
   uint64_t wait_limit_cycles = 0;  // in-kernel wait bound, SM cycles at the peak clock
   int32_t sms = 0;                 // CTAs to fill (the planned device's SM count, capped)
-  size_t off_items = 0, off_merges = 0, off_reqs = 0, off_partials = 0, off_scratch = 0;
+  size_t off_items = 0, off_merges = 0, off_reqs = 0, off_partials = 0, off_scratch = 0, off_keys = 0;
   size_t partial_bytes = 0, scratch_bytes = 0, ws_bytes = 0, upload_bytes = 0;
   uint8_t* upload = nullptr;  // header + items + merges, as copied to the workspace
   const void* upload_dev = nullptr;  // the same pinned buffer as the device sees it (mapped), if it is
@@ -99,9 +99,12 @@ bip_status check_heads(int32_t hq, int32_t hkv, int32_t d) {
 
 size_t partial_row_bytes(int32_t d) { return size_t(d + 4) * sizeof(float); }
 
+// Bytes of the custom-mask pass's first-visible-key array: one int32 per q row.
+size_t key_bytes_for(int64_t q_rows) { return size_t(q_rows) * sizeof(int32_t); }
+
 size_t layout_bytes(size_t n_items, size_t n_merges, size_t n_reqs, size_t partial_bytes, size_t scratch_bytes,
-                    size_t* off_items, size_t* off_merges, size_t* off_reqs, size_t* off_partials,
-                    size_t* off_scratch, size_t* upload_bytes) {
+                    size_t key_bytes, size_t* off_items, size_t* off_merges, size_t* off_reqs, size_t* off_partials,
+                    size_t* off_scratch, size_t* off_keys, size_t* upload_bytes) {
   // header | request rows | work items | merge units: the append uploads only
   // the prefix before the work items.
   size_t o = bip::kHeaderBytes;
@@ -117,7 +120,9 @@ size_t layout_bytes(size_t n_items, size_t n_merges, size_t n_reqs, size_t parti
   *off_partials = o;
   o = align_up(o + partial_bytes, 256);
   *off_scratch = o;
-  o += scratch_bytes;
+  o = align_up(o + scratch_bytes, 256);
+  *off_keys = o;
+  o += key_bytes;
   return align_up(o, 256);
 }
 
@@ -170,9 +175,9 @@ extern "C" size_t bip_workspace_bound(int32_t max_batch, int32_t max_total_q, in
   const int64_t extra = int64_t(split_budget_bytes / (size_t(group) * partial_row_bytes(head_dim)));
   const size_t scratch =
       size_t(bip::kMaxCtas) * bip::max_tiles_per_unit_for(head_dim) * bip::kTileRows * head_dim * sizeof(float);
-  size_t a, b, c, e, u, rq;
-  return layout_bytes(size_t(units + extra), size_t(units), size_t(max_batch), split_budget_bytes, scratch, &a, &b,
-                      &rq, &c, &e, &u);
+  size_t a, b, c, e, k, u, rq;
+  return layout_bytes(size_t(units + extra), size_t(units), size_t(max_batch), split_budget_bytes, scratch,
+                      key_bytes_for(max_total_q), &a, &b, &rq, &c, &e, &k, &u);
 }
 
 extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, const int32_t* kv_indptr,
@@ -439,8 +444,8 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   p->scratch_bytes =
       p->need_scratch ? size_t(p->grid) * NT * bip::kTileRows * head_dim * sizeof(float) : 0;
   p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->reqs.size(), p->partial_bytes, p->scratch_bytes,
-                             &p->off_items, &p->off_merges, &p->off_reqs, &p->off_partials, &p->off_scratch,
-                             &p->upload_bytes);
+                             key_bytes_for(p->total_q), &p->off_items, &p->off_merges, &p->off_reqs,
+                             &p->off_partials, &p->off_scratch, &p->off_keys, &p->upload_bytes);
 
   // ---- host image of what each call uploads: header + items + merge units
   void* buf = nullptr;
@@ -693,6 +698,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
     // start every item at the first block one of its rows sees
     bip::MaskSkipParams sp;
     sp.items = reinterpret_cast<WorkItem*>(ws + p->off_items);
+    sp.first_key = reinterpret_cast<int32_t*>(ws + p->off_keys);
     sp.n_items = int32_t(p->items.size());
     sp.n_items_dev = nullptr;
     sp.mask = mask;
@@ -702,6 +708,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
     sp.kv_block = bip::kv_block_for(p->d);
     sp.tiles_per_unit = p->nt;
     sp.window_left = p->opts.window_left;
+    sp.num_kv_heads = p->hkv;
     if (bip::launch_mask_skip(sp, std::min<int32_t>(sp.n_items, kMaskSkipCtas), stream) != cudaSuccess)
       return BIP_ERR_CUDA;
   }
@@ -802,7 +809,7 @@ struct bip_graph_plan_s {
   bip_kv_dtype kv_dtype = BIP_KV_BF16;
   uint64_t wait_limit_cycles = 0;
   int32_t window_left = 0;
-  size_t off_items = 0, off_merges = 0, off_partials = 0, off_scratch = 0, ws_bytes = 0;
+  size_t off_items = 0, off_merges = 0, off_partials = 0, off_scratch = 0, off_keys = 0, ws_bytes = 0;
 };
 
 // Split budget of a graph plan when the caller gives no options: batches
@@ -892,7 +899,8 @@ extern "C" bip_status bip_graph_plan(bip_graph_plan_t* plan_out, int32_t max_bat
   p->off_merges = align_up(p->off_items + size_t(item_cap) * sizeof(WorkItem), 256);
   p->off_partials = align_up(p->off_merges + size_t(merge_cap) * sizeof(MergeUnit), 256);
   p->off_scratch = align_up(p->off_partials + size_t(part_cap) * partial_row_bytes(head_dim), 256);
-  p->ws_bytes = align_up(p->off_scratch + size_t(p->grid) * p->nt * bip::kTileRows * head_dim * sizeof(float), 256);
+  p->off_keys = align_up(p->off_scratch + size_t(p->grid) * p->nt * bip::kTileRows * head_dim * sizeof(float), 256);
+  p->ws_bytes = align_up(p->off_keys + key_bytes_for(max_total_q), 256);
   *plan_out = p;
   if (workspace_bytes) *workspace_bytes = p->ws_bytes;
   return BIP_OK;
@@ -985,6 +993,7 @@ static bip_status prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t
     // start every item the planner wrote at the first block one of its rows sees
     bip::MaskSkipParams sp;
     sp.items = dp.items;
+    sp.first_key = reinterpret_cast<int32_t*>(ws + p->off_keys);
     sp.n_items = p->capacity;
     sp.n_items_dev = &header->n_items;
     sp.mask = mask;
@@ -994,6 +1003,7 @@ static bip_status prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t
     sp.kv_block = bip::kv_block_for(p->d);
     sp.tiles_per_unit = p->nt;
     sp.window_left = p->window_left;
+    sp.num_kv_heads = p->hkv;
     if (bip::launch_mask_skip(sp, std::min<int32_t>(p->capacity, kMaskSkipCtas), stream) != cudaSuccess)
       return BIP_ERR_CUDA;
   }

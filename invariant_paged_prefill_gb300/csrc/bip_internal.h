@@ -154,6 +154,7 @@ struct AppendParams {
 // (bip_mask_skip.cu), written into the items before the attention launch.
 struct MaskSkipParams {
   WorkItem* items;
+  int32_t* first_key;  // [q rows]: each row's first visible key (INT32_MAX: none), in the workspace
   int32_t n_items;
   const uint32_t* n_items_dev;  // if set, the item count is read here (device-planned launches)
   const uint32_t* mask;
@@ -163,6 +164,7 @@ struct MaskSkipParams {
   int32_t kv_block;
   int32_t tiles_per_unit;
   int32_t window_left;
+  int32_t num_kv_heads;
 };
 
 struct DevPlanParams {

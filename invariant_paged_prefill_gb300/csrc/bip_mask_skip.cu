@@ -5,16 +5,21 @@
 // item at the first block some row sees, as a sliding window does.
 //
 // Runs after the work list is in the workspace (uploaded, or written by the
-// device planner) and before the attention launch.  For each item, one
-// thread per tile row (the first q head of each position: the heads of a
-// position share its mask row) scans the row's mask words from the first key
-// the causal and window rules allow up to the row's own position and stops
-// at the first visible key; the item's first block becomes the block of the
-// smallest such key over its rows.  A folded item also starts at that
-// block's segment (the segments before it hold no visible key for any row
-// and are not visited, as under a window); a split item keeps its segment.
-// An item none of whose rows sees a key in its range keeps only its last
-// block, which still writes the rows' empty state (m = -inf, l = 0).
+// device planner) and before the attention launch, in two launches.  First,
+// the items of one kv head per unit (every q row of the batch lies in one of
+// them; the other kv heads' items hold the same rows) find each of their rows' first
+// visible key, from the first key the causal and window rules allow up to
+// the row's own position, into a per-row array in the workspace: the rows
+// are spread over the CTA's warps, eight at a time per warp; lane i loads
+// word i of a 32-word window of each of the eight rows (eight independent,
+// coalesced loads), a ballot finds a row's first nonzero word, and the
+// window moves on until every row has its key.  Then every item takes the
+// smallest key over its rows and starts at that key's block.  A folded item
+// also starts at that block's segment (the segments before it hold no
+// visible key for any row and are not visited, as under a window); a split
+// item keeps its segment.  An item none of whose rows sees a key in its
+// range keeps only its last block, which still writes the rows' empty state
+// (m = -inf, l = 0).
 //
 // Whether a block is visited changes no bit of any row: a row that sees no
 // key of a block gets p = 0 for all of its columns, an unchanged running
@@ -31,42 +36,101 @@
 namespace bip {
 namespace {
 
-constexpr int kSkipThreads = kMaxTilesPerUnit * kTileRows;  // one thread per row of each tile slot
+constexpr int kSkipThreads = 256;
+constexpr int kSkipWarps = kSkipThreads / 32;
+constexpr int kRowsAtOnce = 8;  // rows a warp scans together
 
-__global__ void __launch_bounds__(kSkipThreads) bip_mask_skip_kernel(const MaskSkipParams p) {
-  __shared__ int s_min[kSkipThreads / 32];
+// Position of row r (slot-major over the item's tiles), and whether the
+// item holds it.
+__device__ __forceinline__ bool item_row(const MaskSkipParams& p, const WorkItem& w, int r, int& pos) {
+  const int t = r / p.tile_pos;
+  pos = w.q_lo + (w.tile + t) * p.tile_pos + (r - t * p.tile_pos);
+  const int present = (w.flags / kSlotPresent) & ((1 << kMaxTilesPerUnit) - 1);
+  return r < p.tiles_per_unit * p.tile_pos && (present >> t & 1) && pos < w.kv_len;
+}
+
+__global__ void __launch_bounds__(kSkipThreads, 2) bip_mask_keys_kernel(const MaskSkipParams p) {
   const int n_items = p.n_items_dev ? int(*p.n_items_dev) : p.n_items;
-  const int tid = threadIdx.x, t = tid / kTileRows, row = tid % kTileRows;
-  const int local_pos = row / p.group, hg = row - local_pos * p.group;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int npos = p.tiles_per_unit * p.tile_pos;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const WorkItem w = p.items[it];
-    const int present = (w.flags / kSlotPresent) & ((1 << kMaxTilesPerUnit) - 1);
-    int first = INT_MAX;
-    if (t < p.tiles_per_unit && (present >> t & 1) && hg == 0 && local_pos < p.tile_pos) {
-      const int tile_start = w.q_lo + (w.tile + t) * p.tile_pos;
-      const int pos = tile_start + local_pos;
-      if (pos < w.kv_len) {
-        const uint32_t* mrow = p.mask + int64_t(w.q_tok0 + pos) * p.mask_row_words;
-        const int lo = p.window_left > 0 ? max(0, pos - p.window_left) : 0;
-        for (int wd = lo >> 5; wd <= (pos >> 5); ++wd) {
-          uint32_t bits = __ldg(mrow + wd);
-          if (wd == (lo >> 5)) bits &= ~0u << (lo & 31);                            // keys from lo on
-          if (wd == (pos >> 5)) bits &= (pos & 31) == 31 ? ~0u : (2u << (pos & 31)) - 1u;  // up to pos
-          if (bits) {
-            first = wd * 32 + __ffs(int(bits)) - 1;
-            break;
+    // One kv head's items per unit scan its rows (the others hold the same
+    // rows); which head depends on the unit, so that a work list that keeps
+    // a unit's heads together does not leave the scans to every
+    // num_kv_heads-th CTA.
+    const uint32_t pick = (uint32_t(w.tile) * 2654435761u + uint32_t(w.page_base)) % uint32_t(p.num_kv_heads);
+    if (uint32_t(w.kv_head) != pick) continue;  // uniform over the CTA
+    for (int r0 = warp; r0 < npos; r0 += kSkipWarps * kRowsAtOnce) {
+      int lo_w[kRowsAtOnce], hi_w[kRowsAtOnce], lo[kRowsAtOnce], pos[kRowsAtOnce], key[kRowsAtOnce];
+      const uint32_t* mrow[kRowsAtOnce];
+      bool act[kRowsAtOnce], has[kRowsAtOnce];
+#pragma unroll
+      for (int i = 0; i < kRowsAtOnce; ++i) {
+        has[i] = item_row(p, w, r0 + i * kSkipWarps, pos[i]);
+        act[i] = has[i];
+        key[i] = INT_MAX;
+        lo[i] = p.window_left > 0 ? max(0, pos[i] - p.window_left) : 0;
+        lo_w[i] = lo[i] >> 5;
+        hi_w[i] = pos[i] >> 5;
+        mrow[i] = has[i] ? p.mask + int64_t(w.q_tok0 + pos[i]) * p.mask_row_words : p.mask;
+      }
+      for (int cw = 0;; cw += 32) {
+        uint32_t bits[kRowsAtOnce];
+#pragma unroll
+        for (int i = 0; i < kRowsAtOnce; ++i) {
+          const int wd = lo_w[i] + cw + lane;
+          bits[i] = (act[i] && wd <= hi_w[i]) ? __ldg(mrow[i] + wd) : 0u;
+          if (wd == lo_w[i]) bits[i] &= ~0u << (lo[i] & 31);  // keys from lo on
+          if (wd == hi_w[i]) bits[i] &= (pos[i] & 31) == 31 ? ~0u : (2u << (pos[i] & 31)) - 1u;  // up to pos
+        }
+        bool more = false;
+#pragma unroll
+        for (int i = 0; i < kRowsAtOnce; ++i) {
+          if (!act[i]) continue;  // uniform over the warp
+          const unsigned ball = __ballot_sync(0xffffffffu, bits[i] != 0u);
+          if (ball) {
+            const int src = __ffs(int(ball)) - 1;
+            const uint32_t b = __shfl_sync(0xffffffffu, bits[i], src);
+            key[i] = (lo_w[i] + cw + src) * 32 + __ffs(int(b)) - 1;
+            act[i] = false;
+          } else if (lo_w[i] + cw + 32 > hi_w[i]) {
+            act[i] = false;  // no visible key
+          } else {
+            more = true;
           }
         }
+        if (!more) break;
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kRowsAtOnce; ++i)
+          if (has[i]) p.first_key[w.q_tok0 + pos[i]] = key[i];
       }
     }
-    first = __reduce_min_sync(0xffffffffu, first);
-    if ((tid & 31) == 0) s_min[tid / 32] = first;
+  }
+}
+
+__global__ void __launch_bounds__(kSkipThreads) bip_mask_skip_kernel(const MaskSkipParams p) {
+  __shared__ int s_min[kSkipWarps];
+  const int n_items = p.n_items_dev ? int(*p.n_items_dev) : p.n_items;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int npos = p.tiles_per_unit * p.tile_pos;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const WorkItem w = p.items[it];
+    int m = INT_MAX;
+    for (int r = threadIdx.x; r < npos; r += kSkipThreads) {
+      int pos;
+      if (item_row(p, w, r, pos)) m = min(m, p.first_key[w.q_tok0 + pos]);
+    }
+    m = __reduce_min_sync(0xffffffffu, m);
+    if (lane == 0) s_min[warp] = m;
     __syncthreads();
-    if (tid == 0) {
-      int m = INT_MAX;
+    if (threadIdx.x == 0) {
 #pragma unroll
-      for (int i = 0; i < kSkipThreads / 32; ++i) m = min(m, s_min[i]);
+      for (int i = 0; i < kSkipWarps; ++i) m = min(m, s_min[i]);
       // the item's block range, as the attention kernel derives it
+      const int present = (w.flags / kSlotPresent) & ((1 << kMaxTilesPerUnit) - 1);
       int unit_end = 0;
       for (int s = 0; s < p.tiles_per_unit; ++s)
         if (present >> s & 1) unit_end = min(w.q_lo + (w.tile + s + 1) * p.tile_pos - 1, w.kv_len - 1);
@@ -87,6 +151,7 @@ __global__ void __launch_bounds__(kSkipThreads) bip_mask_skip_kernel(const MaskS
 
 cudaError_t launch_mask_skip(const MaskSkipParams& p, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+  bip_mask_keys_kernel<<<grid, kSkipThreads, 0, stream>>>(p);
   bip_mask_skip_kernel<<<grid, kSkipThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
