@@ -210,3 +210,51 @@ def test_document_masks_skip_blocks_and_keep_the_bits(cuda):
     keep[moved] = False
     assert_bitwise(oo[keep], fo[keep], "rows of items that can no longer skip")
     assert torch.equal(ol[keep], fl[keep])
+
+
+@pytest.mark.parametrize("window", [0, 1500])
+def test_document_masks_in_graph_launches_and_with_windows(cuda, window):
+    # The skip passes in device-planned launches (split on the device for a
+    # short batch) and under a sliding window (rows scan from position -
+    # window): bits equal the host-planned masked launch, extend rows equal
+    # full-prefill rows, and sampled rows match the oracle.
+    prompts = [W.make_prompt(n, *W.HEADS_A, seed=160 + i) for i, n in enumerate((9000, 5100))]
+    full = W.layout(prompts, [p.n for p in prompts], 16, seed_pages=4, poison=True)
+    ext = W.layout(prompts, [40, 3], 16, seed_pages=8, poison=True)
+    fm, em = _doc_masks(full, 9, lo=400, hi=2500), _doc_masks(ext, 9, lo=400, hi=2500)
+    fo, fl, _ = run_gpu(full, cuda, custom_mask=fm, window_left=window)
+    eo, el, _ = run_gpu(ext, cuda, custom_mask=em, window_left=window)
+    for r in range(2):
+        f0, e0 = int(full.qo_indptr[r]), int(ext.qo_indptr[r])
+        n, off = ext.q_lens[r], full.q_lens[r] - ext.q_lens[r]
+        assert_bitwise(eo[e0:e0 + n], fo[f0 + off:f0 + off + n], f"request {r} out")
+        assert torch.equal(el[e0:e0 + n], fl[f0 + off:f0 + off + n]), f"request {r} lse"
+    rows = _rows(full, fm, seed=4)
+    ro, rl = oracle(full, rows=rows, custom_mask=fm, window_left=window)
+    _check(fo, fl, ro, rl, rows)
+    # the extend through the graph-replayable launch (device planner, device-side split)
+    d = to_device(ext, cuda)
+    words = (max(ext.kv_lens) + 31) // 32
+    gp = bip.GraphPlan(4, 64, num_qo_heads=32, num_kv_heads=8, head_dim=128, window_left=window)
+    i32 = dict(dtype=torch.int32, device=cuda)
+    qo = torch.zeros(5, **i32)
+    kv = torch.zeros(5, **i32)
+    last = torch.ones(4, **i32)
+    qo[:3] = torch.as_tensor(np.asarray(ext.qo_indptr), dtype=torch.int32)
+    kv[:3] = torch.as_tensor(np.asarray(ext.kv_indptr), dtype=torch.int32)
+    qo[3:] = int(ext.qo_indptr[-1])
+    kv[3:] = int(ext.kv_indptr[-1])
+    last[:2] = torch.as_tensor(np.asarray(ext.kv_last_page_len), dtype=torch.int32)
+    q = torch.zeros(64, 32, 128, dtype=torch.bfloat16, device=cuda)
+    n = ext.q.shape[0]
+    q[:n].copy_(d.q)
+    mask_buf = torch.zeros(64, words, dtype=torch.int32, device=cuda)
+    mask_buf[:n].copy_(torch.from_numpy(bip.pack_mask(em, words)))
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((64, 32), float("nan"), dtype=torch.float32, device=cuda)
+    ws = torch.empty(gp.workspace_bytes, dtype=torch.uint8, device=cuda)
+    bip.prefill_graph(gp, 4, qo, kv, last, q, d.k_pages, d.v_pages, d.kv_indices, out, lse, ws, custom_mask=mask_buf)
+    torch.cuda.synchronize()
+    assert bip.read_device_status(ws) == 0
+    assert_bitwise(out[:n].cpu(), eo, "graph launch out")
+    assert torch.equal(lse[:n].cpu(), el), "graph launch lse"
