@@ -32,8 +32,6 @@ using bip::WorkItem;
 namespace {
 
 constexpr size_t kDefaultSplitBudget = size_t(256) << 20;
-// CTAs of the custom-mask block-skip pass (items by stride).
-constexpr int32_t kMaskSkipCtas = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -709,7 +707,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
     sp.tiles_per_unit = p->nt;
     sp.window_left = p->opts.window_left;
     sp.num_kv_heads = p->hkv;
-    if (bip::launch_mask_skip(sp, std::min<int32_t>(sp.n_items, kMaskSkipCtas), stream) != cudaSuccess)
+    if (bip::launch_mask_skip(sp, sp.n_items, stream) != cudaSuccess)
       return BIP_ERR_CUDA;
   }
   const cudaError_t le = mask ? bip::launch_attention_masked(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream)
@@ -1004,7 +1002,7 @@ static bip_status prefill_graph(bip_graph_plan_t p, int32_t batch, const int32_t
     sp.tiles_per_unit = p->nt;
     sp.window_left = p->window_left;
     sp.num_kv_heads = p->hkv;
-    if (bip::launch_mask_skip(sp, std::min<int32_t>(p->capacity, kMaskSkipCtas), stream) != cudaSuccess)
+    if (bip::launch_mask_skip(sp, p->capacity, stream) != cudaSuccess)
       return BIP_ERR_CUDA;
   }
   const cudaError_t le = mask ? bip::launch_attention_masked(p->d, p->nt, fp8, tm_q, tm_k, tm_v, ap, p->grid, stream)

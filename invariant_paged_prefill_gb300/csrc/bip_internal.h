@@ -206,7 +206,7 @@ cudaError_t launch_attention_masked(int head_dim, int tiles_per_unit, bool kv_fp
 cudaError_t launch_merge(int head_dim, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int head_dim, bool kv_fp8, const AppendParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_device_plan(const DevPlanParams& p, cudaStream_t stream);
-cudaError_t launch_mask_skip(const MaskSkipParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_mask_skip(const MaskSkipParams& p, int max_items, cudaStream_t stream);  // max_items: the count or a bound
 // bytes (a multiple of 16) from a device-visible pinned host buffer to the
 // workspace, by SM loads (bip_upload.cu).
 cudaError_t launch_upload(const void* src_dev, void* dst, size_t bytes, cudaStream_t stream);

@@ -13,8 +13,9 @@
 // are spread over the CTA's warps, eight at a time per warp; lane i loads
 // word i of a 32-word window of each of the eight rows (eight independent,
 // coalesced loads), a ballot finds a row's first nonzero word, and the
-// window moves on until every row has its key.  Then every item takes the
-// smallest key over its rows and starts at that key's block.  A folded item
+// window moves on until every row has its key.  Then every item (one warp
+// each) takes the smallest key over its rows and starts at that key's
+// block.  A folded item
 // also starts at that block's segment (the segments before it hold no
 // visible key for any row and are not visited, as under a window); a split
 // item keeps its segment.  An item none of whose rows sees a key in its
@@ -112,23 +113,19 @@ __global__ void __launch_bounds__(kSkipThreads, 2) bip_mask_keys_kernel(const Ma
 }
 
 __global__ void __launch_bounds__(kSkipThreads) bip_mask_skip_kernel(const MaskSkipParams p) {
-  __shared__ int s_min[kSkipWarps];
+  // one warp per item
   const int n_items = p.n_items_dev ? int(*p.n_items_dev) : p.n_items;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int npos = p.tiles_per_unit * p.tile_pos;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  for (int it = blockIdx.x * kSkipWarps + warp; it < n_items; it += gridDim.x * kSkipWarps) {
     const WorkItem w = p.items[it];
     int m = INT_MAX;
-    for (int r = threadIdx.x; r < npos; r += kSkipThreads) {
+    for (int r = lane; r < npos; r += 32) {
       int pos;
       if (item_row(p, w, r, pos)) m = min(m, p.first_key[w.q_tok0 + pos]);
     }
     m = __reduce_min_sync(0xffffffffu, m);
-    if (lane == 0) s_min[warp] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-#pragma unroll
-      for (int i = 0; i < kSkipWarps; ++i) m = min(m, s_min[i]);
+    if (lane == 0) {
       // the item's block range, as the attention kernel derives it
       const int present = (w.flags / kSlotPresent) & ((1 << kMaxTilesPerUnit) - 1);
       int unit_end = 0;
@@ -143,16 +140,16 @@ __global__ void __launch_bounds__(kSkipThreads) bip_mask_skip_kernel(const MaskS
         if (!(w.flags & kItemSplit)) p.items[it].seg_lo = int16_t(blk / bps);
       }
     }
-    __syncthreads();
   }
 }
 
 }  // namespace
 
-cudaError_t launch_mask_skip(const MaskSkipParams& p, int grid, cudaStream_t stream) {
-  if (grid <= 0) return cudaSuccess;
-  bip_mask_keys_kernel<<<grid, kSkipThreads, 0, stream>>>(p);
-  bip_mask_skip_kernel<<<grid, kSkipThreads, 0, stream>>>(p);
+cudaError_t launch_mask_skip(const MaskSkipParams& p, int max_items, cudaStream_t stream) {
+  if (max_items <= 0) return cudaSuccess;
+  constexpr int kMaxCtas = 1024;
+  bip_mask_keys_kernel<<<min(max_items, kMaxCtas), kSkipThreads, 0, stream>>>(p);  // a CTA per item
+  bip_mask_skip_kernel<<<min((max_items + kSkipWarps - 1) / kSkipWarps, kMaxCtas), kSkipThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
