@@ -10,10 +10,10 @@
 // them; the other kv heads' items hold the same rows) find each of their rows' first
 // visible key, from the first key the causal and window rules allow up to
 // the row's own position, into a per-row array in the workspace: the rows
-// are spread over the CTA's warps, eight at a time per warp; lane i loads
-// word i of a 32-word window of each of the eight rows (eight independent,
-// coalesced loads), a ballot finds a row's first nonzero word, and the
-// window moves on until every row has its key.  Then every item (one warp
+// are spread over the CTA's warps, four at a time per warp; lane i loads
+// words i, 32 + i, 64 + i and 96 + i of a 128-word window of each of the
+// four rows (sixteen independent, coalesced loads), ballots find a row's
+// first nonzero word, and the window moves on until every row has its key.  Then every item (one warp
 // each) takes the smallest key over its rows and starts at that key's
 // block.  A folded item
 // also starts at that block's segment (the segments before it hold no
@@ -39,7 +39,8 @@ namespace {
 
 constexpr int kSkipThreads = 256;
 constexpr int kSkipWarps = kSkipThreads / 32;
-constexpr int kRowsAtOnce = 8;  // rows a warp scans together
+constexpr int kKeyRows = 4;  // rows a warp scans together
+constexpr int kKeyWins = 4;  // 32-word windows of each row loaded at once
 
 // Position of row r (slot-major over the item's tiles), and whether the
 // item holds it.
@@ -62,12 +63,12 @@ __global__ void __launch_bounds__(kSkipThreads, 2) bip_mask_keys_kernel(const Ma
     // num_kv_heads-th CTA.
     const uint32_t pick = (uint32_t(w.tile) * 2654435761u + uint32_t(w.page_base)) % uint32_t(p.num_kv_heads);
     if (uint32_t(w.kv_head) != pick) continue;  // uniform over the CTA
-    for (int r0 = warp; r0 < npos; r0 += kSkipWarps * kRowsAtOnce) {
-      int lo_w[kRowsAtOnce], hi_w[kRowsAtOnce], lo[kRowsAtOnce], pos[kRowsAtOnce], key[kRowsAtOnce];
-      const uint32_t* mrow[kRowsAtOnce];
-      bool act[kRowsAtOnce], has[kRowsAtOnce];
+    for (int r0 = warp; r0 < npos; r0 += kSkipWarps * kKeyRows) {
+      int lo_w[kKeyRows], hi_w[kKeyRows], lo[kKeyRows], pos[kKeyRows], key[kKeyRows];
+      const uint32_t* mrow[kKeyRows];
+      bool act[kKeyRows], has[kKeyRows];
 #pragma unroll
-      for (int i = 0; i < kRowsAtOnce; ++i) {
+      for (int i = 0; i < kKeyRows; ++i) {
         has[i] = item_row(p, w, r0 + i * kSkipWarps, pos[i]);
         act[i] = has[i];
         key[i] = INT_MAX;
@@ -76,26 +77,38 @@ __global__ void __launch_bounds__(kSkipThreads, 2) bip_mask_keys_kernel(const Ma
         hi_w[i] = pos[i] >> 5;
         mrow[i] = has[i] ? p.mask + int64_t(w.q_tok0 + pos[i]) * p.mask_row_words : p.mask;
       }
-      for (int cw = 0;; cw += 32) {
-        uint32_t bits[kRowsAtOnce];
+      for (int cw = 0;; cw += 32 * kKeyWins) {
+        uint32_t bits[kKeyRows][kKeyWins];
 #pragma unroll
-        for (int i = 0; i < kRowsAtOnce; ++i) {
-          const int wd = lo_w[i] + cw + lane;
-          bits[i] = (act[i] && wd <= hi_w[i]) ? __ldg(mrow[i] + wd) : 0u;
-          if (wd == lo_w[i]) bits[i] &= ~0u << (lo[i] & 31);  // keys from lo on
-          if (wd == hi_w[i]) bits[i] &= (pos[i] & 31) == 31 ? ~0u : (2u << (pos[i] & 31)) - 1u;  // up to pos
-        }
+        for (int i = 0; i < kKeyRows; ++i)
+#pragma unroll
+          for (int h = 0; h < kKeyWins; ++h) {
+            const int wd = lo_w[i] + cw + 32 * h + lane;
+            uint32_t v = (act[i] && wd <= hi_w[i]) ? __ldg(mrow[i] + wd) : 0u;
+            if (wd == lo_w[i]) v &= ~0u << (lo[i] & 31);                                      // keys from lo on
+            if (wd == hi_w[i]) v &= (pos[i] & 31) == 31 ? ~0u : (2u << (pos[i] & 31)) - 1u;  // up to pos
+            bits[i][h] = v;
+          }
         bool more = false;
 #pragma unroll
-        for (int i = 0; i < kRowsAtOnce; ++i) {
+        for (int i = 0; i < kKeyRows; ++i) {
           if (!act[i]) continue;  // uniform over the warp
-          const unsigned ball = __ballot_sync(0xffffffffu, bits[i] != 0u);
-          if (ball) {
-            const int src = __ffs(int(ball)) - 1;
-            const uint32_t b = __shfl_sync(0xffffffffu, bits[i], src);
-            key[i] = (lo_w[i] + cw + src) * 32 + __ffs(int(b)) - 1;
+          bool found = false;
+          int k = 0;
+#pragma unroll
+          for (int h = 0; h < kKeyWins; ++h) {
+            const unsigned ball = __ballot_sync(0xffffffffu, bits[i][h] != 0u);
+            if (!found && ball) {  // uniform over the warp
+              const int src = __ffs(int(ball)) - 1;
+              const uint32_t b = __shfl_sync(0xffffffffu, bits[i][h], src);
+              k = (lo_w[i] + cw + 32 * h + src) * 32 + __ffs(int(b)) - 1;
+              found = true;
+            }
+          }
+          if (found) {
+            key[i] = k;
             act[i] = false;
-          } else if (lo_w[i] + cw + 32 > hi_w[i]) {
+          } else if (lo_w[i] + cw + 32 * kKeyWins > hi_w[i]) {
             act[i] = false;  // no visible key
           } else {
             more = true;
@@ -105,7 +118,7 @@ __global__ void __launch_bounds__(kSkipThreads, 2) bip_mask_keys_kernel(const Ma
       }
       if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < kRowsAtOnce; ++i)
+        for (int i = 0; i < kKeyRows; ++i)
           if (has[i]) p.first_key[w.q_tok0 + pos[i]] = key[i];
       }
     }
