@@ -52,7 +52,7 @@ extern "C" {
 typedef enum bip_status {
   BIP_OK = 0,
   BIP_ERR_INVALID_ARG = 1,          /* malformed lengths, pointers, sizes */
-  BIP_ERR_UNSUPPORTED = 2,          /* a valid request this build does not run */
+  BIP_ERR_UNSUPPORTED = 2,          /* a valid request this library does not run */
   BIP_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the plan's need */
   BIP_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
   BIP_ERR_DEVICE_TIMEOUT = 5,       /* a bounded in-kernel wait gave up */
