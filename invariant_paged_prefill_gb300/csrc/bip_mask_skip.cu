@@ -5,22 +5,21 @@
 // item at the first block some row sees, as a sliding window does.
 //
 // Runs after the work list is in the workspace (uploaded, or written by the
-// device planner) and before the attention launch, in two launches.  First,
-// the items of one kv head per unit (every q row of the batch lies in one of
-// them; the other kv heads' items hold the same rows) find each of their rows' first
-// visible key, from the first key the causal and window rules allow up to
-// the row's own position, into a per-row array in the workspace: the rows
-// are spread over the CTA's warps, four at a time per warp; lane i loads
-// words i, 32 + i, 64 + i and 96 + i of a 128-word window of each of the
-// four rows (sixteen independent, coalesced loads), ballots find a row's
-// first nonzero word, and the window moves on until every row has its key.  Then every item (one warp
-// each) takes the smallest key over its rows and starts at that key's
-// block.  A folded item
-// also starts at that block's segment (the segments before it hold no
-// visible key for any row and are not visited, as under a window); a split
-// item keeps its segment.  An item none of whose rows sees a key in its
-// range keeps only its last block, which still writes the rows' empty state
-// (m = -inf, l = 0).
+// device planner) and before the attention launch, in two launches.  First, the
+// items of one kv head per unit (every q row of the batch lies in one of them;
+// the other kv heads' items hold the same rows) find each of their rows' first
+// visible key, from the first key the causal and window rules allow up to the
+// row's own position, into a per-row array in the workspace: the rows are
+// spread over the CTA's warps, four at a time per warp; lane i loads words i,
+// 32 + i, 64 + i and 96 + i of a 128-word window of each of the four rows
+// (sixteen independent, coalesced loads), ballots find a row's first nonzero
+// word, and the window moves on until every row has its key.  Then every item
+// (one warp each) takes the smallest key over its rows and starts at that key's
+// block.  A folded item also starts at that block's segment (the segments
+// before it hold no visible key for any row and are not visited, as under a
+// window); a split item keeps its segment.  An item none of whose rows sees a
+// key in its range keeps only its last block, which still writes the rows'
+// empty state (m = -inf, l = 0).
 //
 // Whether a block is visited changes no bit of any row: a row that sees no
 // key of a block gets p = 0 for all of its columns, an unchanged running
