@@ -50,7 +50,7 @@ struct bip_plan_s {
   int32_t group = 0, T = 0, bn = 0, nt = 1, total_q = 0;
   int32_t max_kv_q = 0;  // longest kv_len among requests with q rows (custom mask row length)
   bip_plan_options opts{};
-  std::vector<WorkItem> items;
+  int32_t n_items = 0;               // work items (in the host image, after the header)
   std::vector<MergeUnit> merges;
   std::vector<int32_t> item_desc;  // 8 int32 per item, see bip_plan_get_items
   std::vector<bip::AppendRow> reqs;  // requests with new rows, for bip_append_kv
@@ -254,6 +254,12 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   // share its tile, so tiles start at the first new row, and an extend of
   // q_len rows needs ceil(q_len / T) tiles wherever its rows fall.
   std::vector<UnitDesc> units;
+  {
+    size_t n = 0;
+    for (int32_t r = 0; r < batch; ++r)
+      if (q_len[r] > 0) n += size_t(((q_len[r] - 1) / T) / NT + 1) * num_kv_heads;
+    units.reserve(n);
+  }
   for (int32_t r = 0; r < batch; ++r) {
     if (q_len[r] == 0) continue;
     const int32_t q_lo = kv_len[r] - q_len[r];
@@ -361,88 +367,77 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
     p->reqs.push_back(row);
   }
 
-  struct Pending {
-    WorkItem w;
-    int32_t desc[8];
-    int32_t order_blocks;
-  };
-  std::vector<Pending> pend;
-  pend.reserve(size_t(n_items));
+  // Merge units and partial rows, in unit order; each split unit's first
+  // partial row per slot.
+  const int32_t bps = bip::kSplitLen / bn;
   int64_t part_rows = 0;
+  std::vector<int64_t> ubase;  // [unit][slot], split units only
   for (size_t i = 0; i < units.size(); ++i) {
+    if (!split[i]) continue;
+    if (ubase.empty()) ubase.assign(units.size() * bip::kMaxTilesPerUnit, 0);
     const UnitDesc& u = units[i];
     const int32_t r = u.request;
-    WorkItem w;
-    std::memset(&w, 0, sizeof(w));
-    w.kv_len = kv_len[r];
-    w.page_base = kv_indptr[r];
-    w.q_tok0 = qo_indptr[r] - (kv_len[r] - q_len[r]);
-    w.q_lo = kv_len[r] - q_len[r];
-    w.tile = u.tile;
-    w.kv_head = int16_t(u.kv_head);
-    w.flags = int16_t(u.mask * bip::kSlotPresent);
-    for (int t = 0; t < NT; ++t) w.nseg[t] = int16_t(u.nseg[t]);
-    w.blk_min = u.blk_min;
-    const int32_t bps = bip::kSplitLen / bn;
-    if (!split[i]) {
-      w.seg_lo = int16_t(u.seg_lo);
-      w.seg_hi = int16_t(u.seg_hi);
-      pend.push_back({w, {r, u.kv_head, u.tile, u.seg_lo, u.seg_hi, 0, u.blocks, u.mask}, u.blocks});
-    } else {
-      int64_t base[bip::kMaxTilesPerUnit] = {0, 0};
-      for (int t = 0; t < NT; ++t) {
-        if (!(u.mask >> t & 1)) continue;
-        MergeUnit m;
-        std::memset(&m, 0, sizeof(m));
-        m.q_tok0 = w.q_tok0;
-        m.q_lo = w.q_lo;
-        m.tile = u.tile + t;
-        m.part_base = int32_t(part_rows);
-        m.rows = u.rows[t];
-        m.kv_head = int16_t(u.kv_head);
-        m.nseg = int16_t(u.nseg[t] - u.seg_lo);  // partials of segments seg_lo .. nseg - 1
-        p->merges.push_back(m);
-        base[t] = part_rows;
-        part_rows += int64_t(u.nseg[t] - u.seg_lo) * u.rows[t];
-      }
-      const int32_t blk_end = u.blk_min + u.blocks;  // one past the last block
-      for (int32_t sg = u.seg_lo; sg <= u.seg_hi; ++sg) {
-        WorkItem ws = w;
-        ws.seg_lo = ws.seg_hi = int16_t(sg);
-        ws.flags = int16_t(w.flags | bip::kItemSplit);
-        for (int t = 0; t < NT; ++t) ws.part_base[t] = int32_t(base[t] + int64_t(sg - u.seg_lo) * u.rows[t]);
-        const int32_t blocks = std::min(blk_end, (sg + 1) * bps) - std::max(u.blk_min, sg * bps);
-        pend.push_back({ws, {r, u.kv_head, u.tile, sg, sg, 1, blocks, u.mask}, blocks});
-      }
-      p->num_split_units++;
+    for (int t = 0; t < NT; ++t) {
+      if (!(u.mask >> t & 1)) continue;
+      MergeUnit m;
+      std::memset(&m, 0, sizeof(m));
+      m.q_tok0 = qo_indptr[r] - (kv_len[r] - q_len[r]);
+      m.q_lo = kv_len[r] - q_len[r];
+      m.tile = u.tile + t;
+      m.part_base = int32_t(part_rows);
+      m.rows = u.rows[t];
+      m.kv_head = int16_t(u.kv_head);
+      m.nseg = int16_t(u.nseg[t] - u.seg_lo);  // partials of segments seg_lo .. nseg - 1
+      p->merges.push_back(m);
+      ubase[i * bip::kMaxTilesPerUnit + t] = part_rows;
+      part_rows += int64_t(u.nseg[t] - u.seg_lo) * u.rows[t];
     }
+    p->num_split_units++;
   }
-  // Order: by (request, KV head) group, longest first inside a group, ties in
-  // construction order.  Concurrent CTAs then stream the same group's pages,
-  // so each KV block comes from HBM about once and from L2 for the other q
-  // tiles; the short tiles of the last group fill the tail.
-  std::stable_sort(pend.begin(), pend.end(), [](const Pending& a, const Pending& b) {
-    const int64_t ga = int64_t(a.desc[0]) * 65536 + a.desc[1], gb = int64_t(b.desc[0]) * 65536 + b.desc[1];
-    if (ga != gb) return ga < gb;
-    return a.order_blocks > b.order_blocks;
+
+  // The items in construction order (each unit, or each segment of a split
+  // unit), as compact entries; then their launch order: by (request, KV
+  // head) group, longest first inside a group, ties in construction order.
+  // Concurrent CTAs then stream the same group's pages, so each KV block
+  // comes from HBM about once and from L2 for the other q tiles; the short
+  // tiles of the last group fill the tail.
+  struct Ent {
+    uint32_t unit;
+    int32_t seg;     // split: the segment; fold: -1
+    int32_t blocks;  // KV blocks the item visits
+  };
+  std::vector<Ent> ents;
+  ents.reserve(size_t(n_items));
+  for (size_t i = 0; i < units.size(); ++i) {
+    const UnitDesc& u = units[i];
+    if (!split[i]) {
+      ents.push_back({uint32_t(i), -1, u.blocks});
+      continue;
+    }
+    const int32_t blk_end = u.blk_min + u.blocks;  // one past the last block
+    for (int32_t sg = u.seg_lo; sg <= u.seg_hi; ++sg)
+      ents.push_back({uint32_t(i), sg, std::min(blk_end, (sg + 1) * bps) - std::max(u.blk_min, sg * bps)});
+  }
+  std::stable_sort(ents.begin(), ents.end(), [&](const Ent& a, const Ent& b) {
+    const UnitDesc& ua = units[a.unit];
+    const UnitDesc& ub = units[b.unit];
+    if (ua.request != ub.request) return ua.request < ub.request;
+    if (ua.kv_head != ub.kv_head) return ua.kv_head < ub.kv_head;
+    return a.blocks > b.blocks;
   });
-  p->items.reserve(pend.size());
-  p->item_desc.reserve(pend.size() * 8);
-  for (const Pending& e : pend) {
-    p->items.push_back(e.w);
-    p->item_desc.insert(p->item_desc.end(), e.desc, e.desc + 8);
-    p->kv_blocks += e.order_blocks;
-    if (!(e.w.flags & bip::kItemSplit) && e.w.seg_hi > e.w.seg_lo) p->need_scratch = true;
-  }
+
+  p->n_items = int32_t(ents.size());
+  for (const Ent& e : ents)
+    if (e.seg < 0 && units[e.unit].seg_hi > units[e.unit].seg_lo) p->need_scratch = true;
   p->partial_rows = part_rows;
   p->partial_bytes = size_t(part_rows) * partial_row_bytes(head_dim);
-  p->grid = int32_t(std::min<int64_t>(int64_t(p->items.size()), num_sms));
+  p->grid = int32_t(std::min<int64_t>(int64_t(p->n_items), num_sms));
   p->wait_limit_cycles = wait_limit_cycles;
   p->sms = num_sms;
   p->scratch_bytes =
       p->need_scratch ? size_t(p->grid) * NT * bip::kTileRows * head_dim * sizeof(float) : 0;
-  p->ws_bytes = layout_bytes(p->items.size(), p->merges.size(), p->reqs.size(), p->partial_bytes, p->scratch_bytes,
-                             key_bytes_for(p->total_q), &p->off_items, &p->off_merges, &p->off_reqs,
+  p->ws_bytes = layout_bytes(size_t(p->n_items), p->merges.size(), p->reqs.size(), p->partial_bytes,
+                             p->scratch_bytes, key_bytes_for(p->total_q), &p->off_items, &p->off_merges, &p->off_reqs,
                              &p->off_partials, &p->off_scratch, &p->off_keys, &p->upload_bytes);
 
   // ---- host image of what each call uploads: header + items + merge units
@@ -464,8 +459,49 @@ extern "C" bip_status bip_plan(bip_plan_t* plan_out, const int32_t* qo_indptr, c
   }
   p->upload = static_cast<uint8_t*>(buf);
   std::memset(p->upload, 0, bip::kHeaderBytes);
-  if (!p->items.empty())
-    std::memcpy(p->upload + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem));
+
+  // the items, in launch order, straight into the image
+  WorkItem* out_items = reinterpret_cast<WorkItem*>(p->upload + p->off_items);
+  p->item_desc.resize(size_t(p->n_items) * 8);
+  for (size_t k = 0; k < ents.size(); ++k) {
+    const Ent& e = ents[k];
+    const UnitDesc& u = units[e.unit];
+    const int32_t r = u.request;
+    WorkItem w;
+    std::memset(&w, 0, sizeof(w));
+    w.kv_len = kv_len[r];
+    w.page_base = kv_indptr[r];
+    w.q_tok0 = qo_indptr[r] - (kv_len[r] - q_len[r]);
+    w.q_lo = kv_len[r] - q_len[r];
+    w.tile = u.tile;
+    w.kv_head = int16_t(u.kv_head);
+    w.flags = int16_t(u.mask * bip::kSlotPresent);
+    for (int t = 0; t < NT; ++t) w.nseg[t] = int16_t(u.nseg[t]);
+    w.blk_min = u.blk_min;
+    int32_t* d = p->item_desc.data() + k * 8;
+    if (e.seg < 0) {
+      w.seg_lo = int16_t(u.seg_lo);
+      w.seg_hi = int16_t(u.seg_hi);
+      d[3] = u.seg_lo;
+      d[4] = u.seg_hi;
+      d[5] = 0;
+    } else {
+      w.seg_lo = w.seg_hi = int16_t(e.seg);
+      w.flags = int16_t(w.flags | bip::kItemSplit);
+      for (int t = 0; t < NT; ++t)
+        w.part_base[t] =
+            int32_t(ubase[size_t(e.unit) * bip::kMaxTilesPerUnit + t] + int64_t(e.seg - u.seg_lo) * u.rows[t]);
+      d[3] = d[4] = e.seg;
+      d[5] = 1;
+    }
+    d[0] = r;
+    d[1] = u.kv_head;
+    d[2] = u.tile;
+    d[6] = e.blocks;
+    d[7] = u.mask;
+    p->kv_blocks += e.blocks;
+    std::memcpy(out_items + k, &w, sizeof(w));
+  }
   if (!p->merges.empty())
     std::memcpy(p->upload + p->off_merges, p->merges.data(), p->merges.size() * sizeof(MergeUnit));
   if (!p->reqs.empty())
@@ -491,7 +527,7 @@ extern "C" bip_status bip_plan_get_info(bip_plan_t p, bip_plan_info* info) {
   info->kv_block = p->bn;
   info->split_len = bip::kSplitLen;
   info->num_units = p->num_units;
-  info->num_items = int32_t(p->items.size());
+  info->num_items = p->n_items;
   info->num_split_units = p->num_split_units;
   info->grid = p->grid;
   info->tiles_per_unit = p->nt;
@@ -506,7 +542,7 @@ extern "C" bip_status bip_plan_get_info(bip_plan_t p, bip_plan_info* info) {
 
 extern "C" bip_status bip_plan_get_items(bip_plan_t p, int32_t* items, int32_t capacity, int32_t* count) {
   if (!p || capacity < 0 || (capacity > 0 && !items)) return BIP_ERR_INVALID_ARG;
-  const int32_t n = int32_t(p->items.size());
+  const int32_t n = p->n_items;
   if (count) *count = n;
   const int32_t m = std::min(n, capacity);
   if (m > 0) std::memcpy(items, p->item_desc.data(), size_t(m) * 8 * sizeof(int32_t));
@@ -648,7 +684,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
   if (!p) return BIP_ERR_INVALID_ARG;
   if (num_q_rows != p->total_q) return BIP_ERR_INVALID_ARG;
   if (mask && mask_row_words < (int64_t(p->max_kv_q) + 31) / 32) return BIP_ERR_INVALID_ARG;
-  if (p->items.empty()) return BIP_OK;  // nothing to compute (all q_len = 0)
+  if (p->n_items == 0) return BIP_OK;  // nothing to compute (all q_len = 0)
   if (!q || !k_pages || !v_pages || !kv_indices || !out || !lse || !workspace) return BIP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return BIP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return BIP_ERR_INVALID_ARG;
@@ -672,7 +708,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
 
   bip::AttnParams ap;
   ap.items = reinterpret_cast<const WorkItem*>(ws + p->off_items);
-  ap.n_items = int32_t(p->items.size());
+  ap.n_items = p->n_items;
   ap.n_items_dev = nullptr;
   ap.num_qo_heads = p->hq;
   ap.group = p->group;
@@ -697,7 +733,7 @@ static bip_status prefill(bip_plan_t p, const void* q, int64_t num_q_rows, const
     bip::MaskSkipParams sp;
     sp.items = reinterpret_cast<WorkItem*>(ws + p->off_items);
     sp.first_key = reinterpret_cast<int32_t*>(ws + p->off_keys);
-    sp.n_items = int32_t(p->items.size());
+    sp.n_items = p->n_items;
     sp.n_items_dev = nullptr;
     sp.mask = mask;
     sp.mask_row_words = mask_row_words;
