@@ -388,3 +388,19 @@ def test_entry_points_refuse_host_tensors_instead_of_computing_on_the_cpu(lib):
     with pytest.raises(bip.BipError, match="CUDA tensor"):
         bip.prefill_graph(gp, 2, i32, i32, i32[:2], out, b.k_pages, b.v_pages, b.kv_indices, out, lse,
                           torch.empty(gp.workspace_bytes, dtype=torch.uint8))
+
+
+def test_equal_length_items_keep_construction_order():
+    # Inside a (request, kv head) group, items of equal length (the full
+    # 4096-key segments of split units, fold units of equal reach) stay in
+    # construction order: units by tile, a split unit's segments in order.
+    qo, kv, last = [0, 70, 72, 700], [0, 1000, 1600, 2000], [16, 16, 16]
+    for pol in ("always", "never", "auto"):
+        it = bip.Plan(qo, kv, last, num_qo_heads=32, num_kv_heads=8, head_dim=128, split_policy=pol).items()
+        keys = it[:, 0] * 65536 + it[:, 1]
+        for k in np.unique(keys):
+            g = it[keys == k]
+            for b in np.unique(g[:, 6]):
+                same = g[g[:, 6] == b]
+                order = [(int(r[2]), int(r[3])) for r in same]
+                assert order == sorted(order), (pol, order)
