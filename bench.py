@@ -144,6 +144,10 @@ WORKLOADS = {
     # the large-head shape, for --profile
     "long_q_d256": ((24, 4, 256), 16, 8192, 8192),
     "short_extend_d256": ((24, 4, 256), 16, 4, 32768),
+    # sweep points below their targets, for --profile
+    "extend32_d256": ((24, 4, 256), 16, 32, 32768),
+    "ridge_q128": ((32, 8, 128), 16, 128, 32768),
+    "prefill_1028": ((32, 8, 128), 16, 1028, 1028),
 }
 
 
