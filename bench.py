@@ -423,6 +423,29 @@ def windowed_work(heads, q_lens, kv_lens, window: int):
     return 4 * d * hq * pairs, keys * 2 * hkv * d * 2
 
 
+def measure_host_planning(reps: int = 5) -> dict:
+    """Host planning time (bip_plan: validation, units, split choice, launch
+    order, the upload image) for the long_q and short_extend batches, median
+    of ``reps`` plans; no device work and outside every timed region."""
+    import invariant_paged_prefill_gb300 as bip
+    out = {}
+    for name in ("long_q", "short_extend"):
+        heads, batch, q_len, kv_len = WORKLOADS[name]
+        pages = (kv_len + 15) // 16
+        qo = np.arange(batch + 1, dtype=np.int32) * q_len
+        kv = np.arange(batch + 1, dtype=np.int32) * pages
+        last = np.full(batch, kv_len - (pages - 1) * 16, dtype=np.int32)
+        ts, items = [], 0
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            p = bip.Plan(qo, kv, last, num_qo_heads=heads[0], num_kv_heads=heads[1], head_dim=heads[2])
+            ts.append((time.perf_counter() - t0) * 1e3)
+            items = p.info["num_items"]
+            p.close()
+        out[name] = {"ms": statistics.median(ts), "items": items}
+    return out
+
+
 def measure_configs(device, reps: int = 20):
     """The smaller configurations of the benchmark's list: bit-exactness checks
     and latencies (median of ``reps`` CUDA-event timings per call, inputs
@@ -736,6 +759,7 @@ def run_ours(args):
                           "they can exceed the dense peak); visible_tflops counts the visible pairs only")
         line["custom_mask"] = masked
         line["configs"] = measure_configs(device)
+        line["host_plan_ms"] = measure_host_planning()
         line["sweep_points"] = [measure_point(h, q, kv, dt, device, args.steps, args.warmup, peaks, peak_kind)
                                 for h, q, kv, dt in SWEEP_EXTRAS]
         print(json.dumps(line), flush=True)
